@@ -1,0 +1,442 @@
+/*
+ * ttt_oracle.c -- plain fp64 CPU oracle of the Test-Time Training inner loop.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the CUDA library calls, links or
+ * includes this file, and the two share no code.  Only the test suite, the
+ * smoke check and the benchmark's CPU-baseline leg load it.
+ *
+ * What is computed, and where it is stated:
+ *
+ *  [CM]  "Test-Time Training Layers: How Inner-Loop Gradient Descent Replaces
+ *        the Transformer KV Cache with Expressive Hidden Models"
+ *        (news.premlal.in), section "The Core Mechanism": the per-token loss
+ *        l(W; x_t) = 1/2 ||f(k_t; W) - v_t||^2 (step 1), the descent step
+ *        W_t = W_{t-1} - eta * grad_W l (step 2), and the readout
+ *        y_t = f(q_t; W_t) through the weights *after* the token's own step
+ *        (step 3).
+ *  [HP]  same page, section "Hardware Parallelization: The Dual Form and
+ *        Mini-Batch GPU Acceleration": tokens are grouped into mini-batches of
+ *        b tokens.
+ *  [ES]  TTT essay (ren-xubin.github.io), paragraph on mini-batches and the
+ *        dual form: inside a block every gradient is taken at the block-start
+ *        parameters, and the effects are accumulated in causal order.
+ *  [MF]  "Test-Time Training (TTT) Layers for Sequence Modeling"
+ *        (dileepadev.github.io), sections "Mathematical Formulation" and
+ *        "Variants: TTT-Linear vs. TTT-MLP": f is a linear map (TTT-Linear) or
+ *        a two-layer MLP (TTT-MLP).
+ *
+ * Readings taken where the pages are silent or disagree (each one is also
+ * listed in the design notes of the repository):
+ *   R1  loss carries the factor 1/2 ([CM] step 1; the dileepadev page and the
+ *       essay print it without), so grad = k^T (f(k;W) - v) for TTT-Linear.
+ *   R2  readout after the token's own step, so the causal mask includes the
+ *       diagonal.
+ *   R3  the per-token step size eta_j belongs to the key/gradient token j.
+ *   R4  gradients inside a mini-batch are summed, not averaged.
+ *   R5  W is stored [d_in][d_out] and f(k;W) = kW (the page code's W is the
+ *       transpose of this).
+ *   R6  the MLP is f(x) = GELU(x W1) W2, no biases, with the tanh form of GELU
+ *       and its exact derivative.
+ *   R7  a final mini-batch shorter than b is processed as a shorter block.
+ *
+ * Layouts (row-major, contiguous): Q,K,V,Z [B][H][T][d]; eta [B][H][T];
+ * W [B][H][d][d]; W1 [B][H][d][hd]; W2 [B][H][hd][d].  All arrays are double.
+ *
+ * Two evaluations are provided for each prefill variant:
+ *   *_primal : the token-level definition, with every intermediate W_i formed
+ *              explicitly (the loop of [CM] with gradients at the block start
+ *              as in [ES]);
+ *   *_dual   : the matrix ("dual") form of the same mini-batch step, written
+ *              from the formulas Z = Q W0 - tril(eta . Q K^T)(K W0 - V) and
+ *              W <- W0 - K^T diag(eta)(K W0 - V) and their MLP counterparts.
+ * Their agreement to ~1e-12 is one of the oracle's self-checks.
+ */
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* ------------------------------------------------------------------ */
+/* GELU, tanh form (Hendrycks & Gimpel 2016), and its exact derivative */
+/* ------------------------------------------------------------------ */
+
+static const double GELU_C = 0.79788456080286535587989211986876; /* sqrt(2/pi) */
+static const double GELU_A = 0.044715;
+
+double oracle_gelu(double x)
+{
+    double t = tanh(GELU_C * (x + GELU_A * x * x * x));
+    return 0.5 * x * (1.0 + t);
+}
+
+/* d/dx of 0.5 x (1 + tanh(c (x + a x^3))) */
+double oracle_gelu_prime(double x)
+{
+    double t = tanh(GELU_C * (x + GELU_A * x * x * x));
+    double dinner = GELU_C * (1.0 + 3.0 * GELU_A * x * x);
+    return 0.5 * (1.0 + t) + 0.5 * x * (1.0 - t * t) * dinner;
+}
+
+/* ------------------------------------------------------------------ */
+/* small dense helpers (plain loops)                                   */
+/* ------------------------------------------------------------------ */
+
+/* y[n] = x[m] * A[m][n] */
+static void vecmat(const double *x, const double *A, double *y, int m, int n)
+{
+    for (int j = 0; j < n; ++j) y[j] = 0.0;
+    for (int i = 0; i < m; ++i) {
+        double xi = x[i];
+        const double *row = A + (size_t)i * n;
+        for (int j = 0; j < n; ++j) y[j] += xi * row[j];
+    }
+}
+
+/* A[m][n] -= s * x[m]^T y[n]   (rank-one update) */
+static void rank1_sub(double *A, double s, const double *x, const double *y, int m, int n)
+{
+    for (int i = 0; i < m; ++i) {
+        double sx = s * x[i];
+        double *row = A + (size_t)i * n;
+        for (int j = 0; j < n; ++j) row[j] -= sx * y[j];
+    }
+}
+
+static double dot(const double *x, const double *y, int n)
+{
+    double s = 0.0;
+    for (int i = 0; i < n; ++i) s += x[i] * y[i];
+    return s;
+}
+
+static void *xmalloc(size_t n)
+{
+    void *p = malloc(n ? n : 1);
+    if (!p) abort();
+    return p;
+}
+
+/* ------------------------------------------------------------------ */
+/* TTT-Linear                                                          */
+/* ------------------------------------------------------------------ */
+
+/*
+ * Per-token gradient of l = 1/2 ||k W - v||^2 at W (R1, R5):
+ *   e = k W - v,  grad = k^T e.
+ * Only e is returned; the caller applies the rank-one k^T e.
+ */
+void oracle_linear_token_error(const double *k, const double *v, const double *W,
+                               double *e, int d)
+{
+    vecmat(k, W, e, d, d);
+    for (int j = 0; j < d; ++j) e[j] -= v[j];
+}
+
+/*
+ * Token-level definition ([CM] steps 1-3, [ES]) for one (batch, head):
+ * for every block of `chunk` tokens starting at state Ws,
+ *   for each token i of the block:  W <- W - eta_i k_i^T (k_i Ws - v_i);
+ *                                   z_i = q_i W.
+ */
+static void linear_primal_head(const double *Q, const double *K, const double *V,
+                               const double *eta, const double *W0, double *Z,
+                               double *W, int T, int d, int chunk)
+{
+    size_t dd = (size_t)d * d;
+    double *Ws = xmalloc(dd * sizeof(double));
+    double *e = xmalloc((size_t)d * sizeof(double));
+    if (W != W0) memcpy(W, W0, dd * sizeof(double)); /* W may alias W0 (in-place step) */
+    for (int t0 = 0; t0 < T; t0 += chunk) {
+        int n = (T - t0 < chunk) ? (T - t0) : chunk; /* R7 */
+        memcpy(Ws, W, dd * sizeof(double));            /* block-start state */
+        for (int i = t0; i < t0 + n; ++i) {
+            const double *k = K + (size_t)i * d;
+            oracle_linear_token_error(k, V + (size_t)i * d, Ws, e, d); /* at Ws */
+            rank1_sub(W, eta[i], k, e, d, d);                          /* step */
+            vecmat(Q + (size_t)i * d, W, Z + (size_t)i * d, d, d);     /* readout */
+        }
+    }
+    free(Ws);
+    free(e);
+}
+
+/*
+ * Dual (matrix) form of the same block step, per block with start state W0:
+ *   E = K W0 - V                         (b x d)
+ *   A = tril(Q K^T) with column j scaled by eta_j, diagonal included (R2, R3)
+ *   Z = Q W0 - A E
+ *   W = W0 - K^T diag(eta) E
+ */
+static void linear_dual_head(const double *Q, const double *K, const double *V,
+                             const double *eta, const double *W0, double *Z,
+                             double *W, int T, int d, int chunk)
+{
+    size_t dd = (size_t)d * d;
+    double *E = xmalloc((size_t)chunk * d * sizeof(double));
+    double *A = xmalloc((size_t)chunk * chunk * sizeof(double));
+    double *Wn = xmalloc(dd * sizeof(double));
+    if (W != W0) memcpy(W, W0, dd * sizeof(double));
+    for (int t0 = 0; t0 < T; t0 += chunk) {
+        int n = (T - t0 < chunk) ? (T - t0) : chunk;
+        const double *Qc = Q + (size_t)t0 * d, *Kc = K + (size_t)t0 * d;
+        const double *Vc = V + (size_t)t0 * d, *ec = eta + t0;
+        double *Zc = Z + (size_t)t0 * d;
+        /* E = K W0 - V */
+        for (int i = 0; i < n; ++i) {
+            vecmat(Kc + (size_t)i * d, W, E + (size_t)i * d, d, d);
+            for (int c = 0; c < d; ++c) E[(size_t)i * d + c] -= Vc[(size_t)i * d + c];
+        }
+        /* A = tril(eta . Q K^T) */
+        for (int i = 0; i < n; ++i)
+            for (int j = 0; j < n; ++j)
+                A[(size_t)i * n + j] = (j <= i) ? ec[j] * dot(Qc + (size_t)i * d, Kc + (size_t)j * d, d) : 0.0;
+        /* Z = Q W0 - A E */
+        for (int i = 0; i < n; ++i) {
+            double *z = Zc + (size_t)i * d;
+            vecmat(Qc + (size_t)i * d, W, z, d, d);
+            for (int j = 0; j <= i; ++j) {
+                double a = A[(size_t)i * n + j];
+                const double *ej = E + (size_t)j * d;
+                for (int c = 0; c < d; ++c) z[c] -= a * ej[c];
+            }
+        }
+        /* W = W0 - K^T diag(eta) E */
+        memcpy(Wn, W, dd * sizeof(double));
+        for (int j = 0; j < n; ++j) rank1_sub(Wn, ec[j], Kc + (size_t)j * d, E + (size_t)j * d, d, d);
+        memcpy(W, Wn, dd * sizeof(double));
+    }
+    free(E);
+    free(A);
+    free(Wn);
+}
+
+typedef void (*linear_head_fn)(const double *, const double *, const double *, const double *,
+                               const double *, double *, double *, int, int, int);
+
+static void linear_all(linear_head_fn fn, const double *Q, const double *K, const double *V,
+                       const double *eta, const double *W0, double *Z, double *W,
+                       int B, int H, int T, int d, int chunk)
+{
+    long BH = (long)B * H;
+    size_t td = (size_t)T * d, dd = (size_t)d * d;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (long bh = 0; bh < BH; ++bh)
+        fn(Q + bh * td, K + bh * td, V + bh * td, eta + bh * (size_t)T, W0 + bh * dd,
+           Z + bh * td, W + bh * dd, T, d, chunk);
+}
+
+void oracle_linear_primal(const double *Q, const double *K, const double *V, const double *eta,
+                          const double *W0, double *Z, double *W, int B, int H, int T, int d,
+                          int chunk)
+{
+    linear_all(linear_primal_head, Q, K, V, eta, W0, Z, W, B, H, T, d, chunk);
+}
+
+void oracle_linear_dual(const double *Q, const double *K, const double *V, const double *eta,
+                        const double *W0, double *Z, double *W, int B, int H, int T, int d,
+                        int chunk)
+{
+    linear_all(linear_dual_head, Q, K, V, eta, W0, Z, W, B, H, T, d, chunk);
+}
+
+/*
+ * One online step (b = 1) for every (batch, head), in place on W:
+ *   e = k W - v;  W <- W - eta k^T e;  z = q W.
+ * This is the per-token loop of [CM]/[MF] applied to a single token.
+ * q,k,v,z [B][H][d]; eta [B][H]; W [B][H][d][d].
+ */
+void oracle_linear_decode(const double *q, const double *k, const double *v, const double *eta,
+                          double *W, double *z, int B, int H, int d)
+{
+    linear_all(linear_primal_head, q, k, v, eta, W, z, W, B, H, 1, d, 1);
+}
+
+/* ------------------------------------------------------------------ */
+/* TTT-MLP:  f(x; W1, W2) = GELU(x W1) W2   (R6)                        */
+/* ------------------------------------------------------------------ */
+
+/*
+ * Loss and gradient of l = 1/2 ||GELU(k W1) W2 - v||^2 for one token, by the
+ * chain rule:
+ *   u = k W1, a = GELU(u), p = a W2, e2 = p - v,
+ *   e1 = (e2 W2^T) . GELU'(u),
+ *   dl/dW2 = a^T e2,   dl/dW1 = k^T e1.
+ * Outputs a [hd], e1 [hd], e2 [d]; returns the loss.
+ */
+double oracle_mlp_token_grad(const double *k, const double *v, const double *W1, const double *W2,
+                             double *a, double *e1, double *e2, int d, int hd)
+{
+    double *u = xmalloc((size_t)hd * sizeof(double));
+    vecmat(k, W1, u, d, hd);
+    for (int m = 0; m < hd; ++m) a[m] = oracle_gelu(u[m]);
+    vecmat(a, W2, e2, hd, d);
+    double loss = 0.0;
+    for (int c = 0; c < d; ++c) {
+        e2[c] -= v[c];
+        loss += 0.5 * e2[c] * e2[c];
+    }
+    for (int m = 0; m < hd; ++m) {
+        /* (e2 W2^T)[m] = sum_c e2[c] W2[m][c] */
+        double s = dot(e2, W2 + (size_t)m * d, d);
+        e1[m] = s * oracle_gelu_prime(u[m]);
+    }
+    free(u);
+    return loss;
+}
+
+/* Forward f(x; W1, W2) for one row: y[d] */
+void oracle_mlp_forward(const double *x, const double *W1, const double *W2, double *y, int d,
+                        int hd)
+{
+    double *h = xmalloc((size_t)hd * sizeof(double));
+    vecmat(x, W1, h, d, hd);
+    for (int m = 0; m < hd; ++m) h[m] = oracle_gelu(h[m]);
+    vecmat(h, W2, y, hd, d);
+    free(h);
+}
+
+/* Token-level definition for one (batch, head), gradients at the block start. */
+static void mlp_primal_head(const double *Q, const double *K, const double *V, const double *eta,
+                            const double *W1_0, const double *W2_0, double *Z, double *W1,
+                            double *W2, int T, int d, int hd, int chunk)
+{
+    size_t n1 = (size_t)d * hd;
+    double *W1s = xmalloc(n1 * sizeof(double)), *W2s = xmalloc(n1 * sizeof(double));
+    double *a = xmalloc((size_t)hd * sizeof(double)), *e1 = xmalloc((size_t)hd * sizeof(double));
+    double *e2 = xmalloc((size_t)d * sizeof(double));
+    memcpy(W1, W1_0, n1 * sizeof(double));
+    memcpy(W2, W2_0, n1 * sizeof(double));
+    for (int t0 = 0; t0 < T; t0 += chunk) {
+        int n = (T - t0 < chunk) ? (T - t0) : chunk;
+        memcpy(W1s, W1, n1 * sizeof(double));
+        memcpy(W2s, W2, n1 * sizeof(double));
+        for (int i = t0; i < t0 + n; ++i) {
+            const double *k = K + (size_t)i * d;
+            oracle_mlp_token_grad(k, V + (size_t)i * d, W1s, W2s, a, e1, e2, d, hd);
+            rank1_sub(W1, eta[i], k, e1, d, hd);  /* W1 -= eta k^T e1 */
+            rank1_sub(W2, eta[i], a, e2, hd, d);  /* W2 -= eta a^T e2 */
+            oracle_mlp_forward(Q + (size_t)i * d, W1, W2, Z + (size_t)i * d, d, hd);
+        }
+    }
+    free(W1s); free(W2s); free(a); free(e1); free(e2);
+}
+
+/*
+ * Dual form of the MLP block step, per block with start state (W1, W2):
+ *   Zk = K W1, Hk = GELU(Zk), E2 = Hk W2 - V, E1 = (E2 W2^T) . GELU'(Zk)
+ *   A1 = tril(eta . Q K^T)            (carries the layer-1 delta)
+ *   Hq = GELU(Q W1 - A1 E1)
+ *   A2 = tril(eta . Hq Hk^T)          (carries the layer-2 delta)
+ *   Z  = Hq W2 - A2 E2
+ *   W1 <- W1 - K^T diag(eta) E1,  W2 <- W2 - Hk^T diag(eta) E2
+ */
+static void mlp_dual_head(const double *Q, const double *K, const double *V, const double *eta,
+                          const double *W1_0, const double *W2_0, double *Z, double *W1,
+                          double *W2, int T, int d, int hd, int chunk)
+{
+    size_t n1 = (size_t)d * hd;
+    double *Zk = xmalloc((size_t)chunk * hd * sizeof(double));
+    double *Hk = xmalloc((size_t)chunk * hd * sizeof(double));
+    double *E1 = xmalloc((size_t)chunk * hd * sizeof(double));
+    double *E2 = xmalloc((size_t)chunk * d * sizeof(double));
+    double *Hq = xmalloc((size_t)chunk * hd * sizeof(double));
+    double *W1n = xmalloc(n1 * sizeof(double)), *W2n = xmalloc(n1 * sizeof(double));
+    memcpy(W1, W1_0, n1 * sizeof(double));
+    memcpy(W2, W2_0, n1 * sizeof(double));
+    for (int t0 = 0; t0 < T; t0 += chunk) {
+        int n = (T - t0 < chunk) ? (T - t0) : chunk;
+        const double *Qc = Q + (size_t)t0 * d, *Kc = K + (size_t)t0 * d;
+        const double *Vc = V + (size_t)t0 * d, *ec = eta + t0;
+        double *Zc = Z + (size_t)t0 * d;
+        for (int i = 0; i < n; ++i) {
+            double *zk = Zk + (size_t)i * hd, *hk = Hk + (size_t)i * hd;
+            double *e2 = E2 + (size_t)i * d, *e1 = E1 + (size_t)i * hd;
+            vecmat(Kc + (size_t)i * d, W1, zk, d, hd);
+            for (int m = 0; m < hd; ++m) hk[m] = oracle_gelu(zk[m]);
+            vecmat(hk, W2, e2, hd, d);
+            for (int c = 0; c < d; ++c) e2[c] -= Vc[(size_t)i * d + c];
+            for (int m = 0; m < hd; ++m)
+                e1[m] = dot(e2, W2 + (size_t)m * d, d) * oracle_gelu_prime(zk[m]);
+        }
+        for (int i = 0; i < n; ++i) {
+            /* layer 1 through the delta carried by tril(eta . Q K^T) */
+            double *hq = Hq + (size_t)i * hd;
+            vecmat(Qc + (size_t)i * d, W1, hq, d, hd);
+            for (int j = 0; j <= i; ++j) {
+                double a1 = ec[j] * dot(Qc + (size_t)i * d, Kc + (size_t)j * d, d);
+                const double *e1 = E1 + (size_t)j * hd;
+                for (int m = 0; m < hd; ++m) hq[m] -= a1 * e1[m];
+            }
+            for (int m = 0; m < hd; ++m) hq[m] = oracle_gelu(hq[m]);
+            /* layer 2 through the delta carried by tril(eta . Hq Hk^T) */
+            double *z = Zc + (size_t)i * d;
+            vecmat(hq, W2, z, hd, d);
+            for (int j = 0; j <= i; ++j) {
+                double a2 = ec[j] * dot(hq, Hk + (size_t)j * hd, hd);
+                const double *e2 = E2 + (size_t)j * d;
+                for (int c = 0; c < d; ++c) z[c] -= a2 * e2[c];
+            }
+        }
+        memcpy(W1n, W1, n1 * sizeof(double));
+        memcpy(W2n, W2, n1 * sizeof(double));
+        for (int j = 0; j < n; ++j) {
+            rank1_sub(W1n, ec[j], Kc + (size_t)j * d, E1 + (size_t)j * hd, d, hd);
+            rank1_sub(W2n, ec[j], Hk + (size_t)j * hd, E2 + (size_t)j * d, hd, d);
+        }
+        memcpy(W1, W1n, n1 * sizeof(double));
+        memcpy(W2, W2n, n1 * sizeof(double));
+    }
+    free(Zk); free(Hk); free(E1); free(E2); free(Hq); free(W1n); free(W2n);
+}
+
+typedef void (*mlp_head_fn)(const double *, const double *, const double *, const double *,
+                            const double *, const double *, double *, double *, double *, int,
+                            int, int, int);
+
+static void mlp_all(mlp_head_fn fn, const double *Q, const double *K, const double *V,
+                    const double *eta, const double *W1_0, const double *W2_0, double *Z,
+                    double *W1, double *W2, int B, int H, int T, int d, int hd, int chunk)
+{
+    long BH = (long)B * H;
+    size_t td = (size_t)T * d, n1 = (size_t)d * hd;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (long bh = 0; bh < BH; ++bh)
+        fn(Q + bh * td, K + bh * td, V + bh * td, eta + bh * (size_t)T, W1_0 + bh * n1,
+           W2_0 + bh * n1, Z + bh * td, W1 + bh * n1, W2 + bh * n1, T, d, hd, chunk);
+}
+
+void oracle_mlp_primal(const double *Q, const double *K, const double *V, const double *eta,
+                       const double *W1_0, const double *W2_0, double *Z, double *W1, double *W2,
+                       int B, int H, int T, int d, int hd, int chunk)
+{
+    mlp_all(mlp_primal_head, Q, K, V, eta, W1_0, W2_0, Z, W1, W2, B, H, T, d, hd, chunk);
+}
+
+void oracle_mlp_dual(const double *Q, const double *K, const double *V, const double *eta,
+                     const double *W1_0, const double *W2_0, double *Z, double *W1, double *W2,
+                     int B, int H, int T, int d, int hd, int chunk)
+{
+    mlp_all(mlp_dual_head, Q, K, V, eta, W1_0, W2_0, Z, W1, W2, B, H, T, d, hd, chunk);
+}
+
+/* Threads OpenMP will use (1 when built without OpenMP). */
+int oracle_num_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+void oracle_set_num_threads(int n)
+{
+#ifdef _OPENMP
+    if (n > 0) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
