@@ -1,0 +1,449 @@
+#!/usr/bin/env python3
+"""Throughput of the TTT inner-loop scan library on one B300 (or N, one process each).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--rows all|none]
+
+A step is one TTT-Linear prefill over the headline workload (B=8, H=12,
+d=64, T=2048, chunk 16, bf16 Q/K/V/Z, fp32 state): the §-named "linear
+prefill" configuration the metric is quoted on.  Four copies of the inputs
+(4 x 105 MB > 126 MB L2) rotate from step to step so every step reads from HBM.
+The JSON line printed by rank 0 carries the headline value (tokens/s over all
+ranks), its roofline fraction, the clocks seen during the timed region, the
+end-to-end number through the public API with host buffers, the oracle's CPU
+baseline, and under "rows" the other workloads (TTT-MLP prefill, the
+long-context chunk sweep and the decode step), each timed the same way.
+
+--impl reference times the fp64 CPU oracle (test infrastructure) on the host
+cores on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import sys
+import threading
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from test_sequence_layers_07_b300 import workloads as WL  # noqa: E402
+
+METRIC = "TTT-Linear/MLP prefill tokens/s & % roofline; decode tokens/s & HBM GB/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+NROT = 4  # rotating input copies for the L2-sized workloads
+
+
+# ------------------------------------------------------------------ helpers
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def linear_bytes(B, H, T, d, elt=2):
+    """Algorithmic HBM bytes of one TTT-Linear prefill: Q,K,V read + Z written, eta, W0 read + W written."""
+    return 4 * B * H * T * d * elt + 4 * B * H * T + 2 * B * H * d * d * 4
+
+
+def linear_flops(B, H, T, d, b):
+    """Dual-form FLOPs: Q W0, K W0, K^T E (2d^2 each per token) + causal Q K^T and A E ((b+1)d each)."""
+    return B * H * T * (6 * d * d + 2 * (b + 1) * d)
+
+
+def mlp_flops(B, H, T, d, hd, b):
+    return B * H * T * (14 * d * hd + 2 * (b + 1) * (d + hd))
+
+
+def mlp_bytes(B, H, T, d, hd, elt=2):
+    return 4 * B * H * T * d * elt + 4 * B * H * T + 2 * 2 * B * H * d * hd * 4
+
+
+def decode_bytes(B, H, d, elt=2):
+    """Per step: state read + written once, q,k,v read, z written, eta read."""
+    return 2 * B * H * d * d * 4 + 4 * B * H * d * elt + 4 * B * H
+
+
+def kernel_source_hash(files):
+    h = hashlib.sha256()
+    for f in files:
+        h.update(open(os.path.join(ROOT, "test_sequence_layers_07_b300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel_key, src_files):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on the current source."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p)).get(kernel_key)
+    if not d or d.get("source_sha") != kernel_source_hash(src_files):
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """Samples SM clock and clock-event reasons with NVML while the timed region runs."""
+
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+               0x80: "hw_power_brake_slowdown", 0x2: "applications_clocks_setting", 0x1: "gpu_idle",
+               0x10: "sync_boost"}
+
+    def __init__(self, device=0, interval=0.005):
+        self.interval = interval
+        self.samples, self.reasons = [], set()
+        self.max_mhz = None
+        self._stop = threading.Event()
+        self._h = None
+        try:
+            import pynvml
+            pynvml.nvmlInit()
+            self._nv = pynvml
+            uuid = str(torch.cuda.get_device_properties(device).uuid)
+            try:
+                self._h = pynvml.nvmlDeviceGetHandleByUUID(("GPU-" + uuid) if not uuid.startswith("GPU-") else uuid)
+            except Exception:
+                self._h = pynvml.nvmlDeviceGetHandleByIndex(device)
+            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self._h, pynvml.NVML_CLOCK_SM)
+        except Exception as e:  # no NVML: report nothing rather than guess
+            self._err = str(e)
+
+    def _run(self):
+        nv = self._nv
+        while not self._stop.is_set():
+            try:
+                self.samples.append(nv.nvmlDeviceGetClockInfo(self._h, nv.NVML_CLOCK_SM))
+                r = nv.nvmlDeviceGetCurrentClocksEventReasons(self._h)
+                for bit, name in self.REASONS.items():
+                    if r & bit:
+                        self.reasons.add(name)
+            except Exception:
+                pass
+            time.sleep(self.interval)
+
+    def __enter__(self):
+        if self._h is not None:
+            self._t = threading.Thread(target=self._run, daemon=True)
+            self._t.start()
+        return self
+
+    def __exit__(self, *a):
+        if self._h is not None:
+            self._stop.set()
+            self._t.join()
+
+    def summary(self):
+        if self._h is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvml unavailable"], "samples": 0}
+        reasons = sorted(self.reasons - {"gpu_idle"})
+        return {"sm_mhz": statistics.median(self.samples) if self.samples else None, "sm_max_mhz": self.max_mhz,
+                "reasons": reasons, "samples": len(self.samples)}
+
+
+def dist_setup(gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return rank, world
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    """Max of a per-rank scalar (host-side bookkeeping; no data-path collective)."""
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def timed_loop(fn, steps, warmup, world, stream=None, sampler=None):
+    """Runs `fn(i)` warmup times untimed, then `steps` times between two barriers + syncs.
+
+    Returns (ms_per_step over the whole region, max over ranks; mean per-launch ms from
+    per-call CUDA events on the launching stream).
+    """
+    stream = stream or torch.cuda.current_stream()
+    for i in range(warmup):
+        fn(i)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    ctx = sampler if sampler is not None else _Null()
+    with ctx:
+        t0.record(stream)
+        for i in range(steps):
+            ev[i][0].record(stream)
+            fn(warmup + i)
+            ev[i][1].record(stream)
+        t1.record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    total = t0.elapsed_time(t1)
+    per_launch = sum(a.elapsed_time(b) for a, b in ev) / steps
+    return max_over_ranks(total / steps, world), per_launch
+
+
+class _Null:
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *a):
+        return False
+
+
+# ---------------------------------------------------------------- our arm
+
+def rotating_copies(x: dict, n: int) -> list:
+    base = {k: v.cuda() for k, v in x.items()}
+    return [base] + [{k: v.clone() for k, v in base.items()} for _ in range(n - 1)]
+
+
+def bench_linear(T_mod, w, chunk, steps, warmup, world, peaks, sampler=None, nrot=NROT):
+    x = WL.workload_inputs(w)
+    sets = rotating_copies(x, nrot)
+    outs = [(torch.empty_like(s["Q"]), torch.empty_like(s["W0"])) for s in sets]
+
+    def step(i):
+        s, (Z, W) = sets[i % nrot], outs[i % nrot]
+        T_mod.ttt_linear_prefill(s["Q"], s["K"], s["V"], s["eta"], s["W0"], Z, W, chunk)
+
+    ms, ms_launch = timed_loop(step, steps, warmup, world, sampler=sampler)
+    toks = w.B * w.T
+    nbytes = linear_bytes(w.B, w.H, w.T, w.d)
+    flops = linear_flops(w.B, w.H, w.T, w.d, chunk)
+    t_roof = max(nbytes / (peaks["hbm_gbs"] * 1e9), flops / (peaks["bf16_tflops"] * 1e12))
+    del sets, outs
+    return {"tokens_per_s": toks / (ms * 1e-3), "ms_per_step": ms, "ms_per_launch": ms_launch,
+            "bytes_per_launch": nbytes, "flops_per_launch": flops,
+            "achieved_gbs": nbytes / (ms_launch * 1e-3) / 1e9, "roofline_us": t_roof * 1e6,
+            "frac": t_roof / (ms_launch * 1e-3), "bound": "hbm"}
+
+
+def bench_mlp(T_mod, w, steps, warmup, world, peaks):
+    x = WL.workload_inputs(w)
+    sets = rotating_copies(x, NROT)
+    outs = [(torch.empty_like(s["Q"]), torch.empty_like(s["W1"]), torch.empty_like(s["W2"])) for s in sets]
+
+    def step(i):
+        s, (Z, W1, W2) = sets[i % NROT], outs[i % NROT]
+        T_mod.ttt_mlp_prefill(s["Q"], s["K"], s["V"], s["eta"], s["W1"], s["W2"], Z, W1, W2, w.chunk)
+
+    ms, ms_launch = timed_loop(step, steps, warmup, world)
+    flops = mlp_flops(w.B, w.H, w.T, w.d, w.hidden, w.chunk)
+    nbytes = mlp_bytes(w.B, w.H, w.T, w.d, w.hidden)
+    t_tensor = flops / (peaks["bf16_tflops"] * 1e12)
+    t_hbm = nbytes / (peaks["hbm_gbs"] * 1e9)
+    del sets, outs
+    return {"tokens_per_s": w.B * w.T / (ms * 1e-3), "ms_per_step": ms, "ms_per_launch": ms_launch,
+            "flops_per_launch": flops, "bytes_per_launch": nbytes,
+            "achieved_tflops": flops / (ms_launch * 1e-3) / 1e12, "roofline_us": max(t_tensor, t_hbm) * 1e6,
+            "frac": max(t_tensor, t_hbm) / (ms_launch * 1e-3), "bound": "tensor" if t_tensor > t_hbm else "hbm"}
+
+
+def bench_decode(T_mod, w, steps, warmup, world, peaks, graph_steps=1024, nrot=NROT):
+    """A CUDA graph of `graph_steps` decode steps; `nrot` state copies rotate so the state streams from HBM."""
+    x = WL.decode_inputs(w.B, w.H, w.d, graph_steps, w.seed)
+    q, k, v, e = (x[n].cuda() for n in ("q", "k", "v", "eta"))
+    states = [x["W"].cuda() for _ in range(nrot)]
+    z = torch.empty_like(q)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):  # one eager pass also serves as warm-up of the library
+        for i in range(2):
+            T_mod.ttt_linear_decode_step(q[i], k[i], v[i], e[i], states[i % nrot], z[i])
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for i in range(graph_steps):
+            T_mod.ttt_linear_decode_step(q[i], k[i], v[i], e[i], states[i % nrot], z[i])
+    ms, ms_launch = timed_loop(lambda i: g.replay(), steps, warmup, world)
+    per_step = ms_launch / graph_steps
+    nbytes = decode_bytes(w.B, w.H, w.d)
+    state_bytes = 2 * w.B * w.H * w.d * w.d * 4
+    t_roof = nbytes / (peaks["hbm_gbs"] * 1e9)
+    return {"tokens_per_s": w.B / (per_step * 1e-3), "us_per_step": per_step * 1e3, "graph_steps": graph_steps,
+            "bytes_per_step": nbytes, "achieved_gbs": nbytes / (per_step * 1e-3) / 1e9,
+            "state_gbs": state_bytes / (per_step * 1e-3) / 1e9, "roofline_us": t_roof * 1e6,
+            "frac": t_roof / (per_step * 1e-3), "bound": "hbm", "state_copies": nrot}
+
+
+def bench_e2e(T_mod, w, steps, warmup, world):
+    """Public API with pinned host buffers: H2D of the inputs, the prefill, D2H of Z and W, every step."""
+    x = WL.workload_inputs(w)
+    host = {k: v.pin_memory() for k, v in x.items()}
+    dev = {k: torch.empty_like(v, device="cuda") for k, v in x.items()}
+    Z = torch.empty_like(dev["Q"])
+    W = torch.empty_like(dev["W0"])
+    Zh = torch.empty_like(host["Q"]).pin_memory()
+    Wh = torch.empty_like(host["W0"]).pin_memory()
+
+    def step(i):
+        for k in dev:
+            dev[k].copy_(host[k], non_blocking=True)
+        T_mod.ttt_linear_prefill(dev["Q"], dev["K"], dev["V"], dev["eta"], dev["W0"], Z, W, w.chunk)
+        Zh.copy_(Z, non_blocking=True)
+        Wh.copy_(W, non_blocking=True)
+
+    ms, _ = timed_loop(step, steps, warmup, world)
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = Zh.numel() * Zh.element_size() + Wh.numel() * Wh.element_size()
+    return {"value": w.B * w.T / (ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": ms}
+
+
+def cpu_baseline(w, target_s=12.0, heads=None):
+    """The fp64 oracle (dual form) on a sample of the workload's heads, scaled to tokens/s."""
+    from oracle import oracle as O
+    x = WL.workload_inputs(w)
+    r = {k: WL.to_f64(v) for k, v in x.items()}
+    BH = w.B * w.H
+    flat = {k: v.reshape((1, BH) + v.shape[2:]) for k, v in r.items()}
+    n = heads or 1
+    while True:
+        sub = {k: v[:, :n] for k, v in flat.items()}
+        t0 = time.perf_counter()
+        O.linear_dual(sub["Q"], sub["K"], sub["V"], sub["eta"], sub["W0"], w.chunk)
+        dt = time.perf_counter() - t0
+        if heads or dt * 2 >= target_s or n >= BH:
+            break
+        n = min(BH, max(n + 1, int(n * min(8.0, target_s / max(dt, 1e-3)))))
+    full_s = dt * BH / n
+    return {"value": w.B * w.T / full_s, "unit": "tokens/s", "cores": O.num_threads(), "kind": "oracle",
+            "sample": f"fp64 dual form on {n} of {BH} (batch, head) sequences of the {w.name} workload "
+                      f"({w.T} tokens each, {dt:.2f} s), scaled to all {BH}", "seconds": dt}
+
+
+def run_ours(args):
+    rank, world = dist_setup(args.gpus)
+    from test_sequence_layers_07_b300 import ttt as T_mod
+    T_mod.load_library()
+    peaks, peaks_kind = load_peaks()
+    w = WL.WORKLOADS["linear_prefill"]
+    dev = torch.cuda.current_device()
+    sampler = ClockSampler(dev)
+    head = bench_linear(T_mod, w, w.chunk, args.steps, args.warmup, world, peaks, sampler=sampler)
+    clocks = sampler.summary()
+    value = world * w.B * w.T / (head["ms_per_step"] * 1e-3)
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": head["ms_per_step"], "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "TTT-Linear prefill B=8 H=12 d=64 T=2048 chunk=16 (bf16 Q/K/V/Z, fp32 state)",
+                   "global_batch": w.B * world, "seq_len": w.T, "heads": w.H, "head_dim": w.d, "chunk": w.chunk,
+                   "parallelism": f"dp{world}" if world > 1 else "single-gpu",
+                   "l2": f"{NROT} rotating input copies ({NROT * linear_bytes(w.B, w.H, w.T, w.d) / 1e6:.0f} MB > "
+                         f"126 MB L2)"},
+        "roofline": {"bound": "hbm", "achieved": head["achieved_gbs"],
+                     "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": head["achieved_gbs"] / peaks["hbm_gbs"],
+                     "traffic": ncu_traffic("linear_prefill", LINEAR_SRC),
+                     "peak_kind": f"{peaks_kind} copy bandwidth", "bytes_per_launch": head["bytes_per_launch"],
+                     "ms_per_launch": head["ms_per_launch"]},
+        "clocks": clocks,
+        "gpu_launches": args.steps,
+    }
+    if not args.no_e2e:
+        line["e2e"] = bench_e2e(T_mod, w, max(3, args.steps // 4), args.warmup, world)
+    if args.rows == "all":
+        rows = {}
+        rows["linear_prefill"] = head
+        wm = WL.WORKLOADS["mlp_prefill"]
+        rows["mlp_prefill"] = bench_mlp(T_mod, wm, max(3, args.steps // 4), args.warmup, world, peaks)
+        wl = WL.WORKLOADS["long_context"]
+        for b in wl.chunks:
+            rows[f"long_context_b{b}"] = bench_linear(T_mod, wl, b, max(3, args.steps // 8), args.warmup, world,
+                                                      peaks, nrot=1)
+        wd = WL.WORKLOADS["decode"]
+        rows["decode"] = bench_decode(T_mod, wd, max(3, args.steps // 20), args.warmup, world, peaks)
+        line["rows"] = rows
+    if rank == 0 and world == 1 and not args.no_cpu:
+        line["cpu_baseline"] = cpu_baseline(w)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    from oracle import oracle as O
+    w = WL.WORKLOADS["linear_prefill"]
+    x = WL.workload_inputs(w)
+    r = {k: WL.to_f64(v) for k, v in x.items()}
+    BH = w.B * w.H
+    flat = {k: v.reshape((1, BH) + v.shape[2:]) for k, v in r.items()}
+    n = 2  # sequences per step: keeps the whole run within a few minutes
+    sub = {k: v[:, :n] for k, v in flat.items()}
+    times = []
+    for i in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        O.linear_dual(sub["Q"], sub["K"], sub["V"], sub["eta"], sub["W0"], w.chunk)
+        if i >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    step_s = sum(times) / len(times) * BH / n  # scaled to the whole workload
+    value = w.B * w.T / step_s
+    sample = f"fp64 oracle dual form on {n} of {BH} sequences per step, scaled to all {BH}"
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_s * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "TTT-Linear prefill B=8 H=12 d=64 T=2048 chunk=16", "global_batch": w.B,
+                       "seq_len": w.T},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": O.num_threads(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+LINEAR_SRC = ["linear_prefill_generic.cu"]
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--rows", choices=["all", "none"], default="all")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    args = ap.parse_args(argv)
+    args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps
+    args.steps = max(1, args.steps)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

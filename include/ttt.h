@@ -1,0 +1,159 @@
+/*
+ * ttt.h -- C ABI of libttt.so: the chunked inner-loop gradient-descent scan of
+ * Test-Time Training (TTT) layers on NVIDIA B300 (sm_103a).
+ *
+ * What the library computes
+ * -------------------------
+ * Each (batch, head) carries fast weights W.  Tokens are taken in blocks
+ * ("mini-batches") of `chunk` tokens.  Inside a block every token's
+ * self-supervised loss  l = 1/2 ||f(k; W) - v||^2  is differentiated at the
+ * block-start weights W0, the steps are applied in causal order, and each
+ * token is read out through the weights after its own step.  In matrix
+ * ("dual") form, for TTT-Linear (f(x; W) = x W):
+ *
+ *     E = K W0 - V
+ *     Z = Q W0 - tril(eta . Q K^T) E       (mask includes the diagonal; column
+ *                                          j is scaled by the key token's eta_j)
+ *     W = W0 - K^T diag(eta) E             (state handed to the next block)
+ *
+ * Sources: "Test-Time Training Layers: How Inner-Loop Gradient Descent Replaces
+ * the Transformer KV Cache with Expressive Hidden Models" (news.premlal.in),
+ * section "The Core Mechanism" (loss with the factor 1/2, descent step,
+ * readout through the updated weights) and section "Hardware Parallelization:
+ * The Dual Form and Mini-Batch GPU Acceleration" (mini-batches of tokens);
+ * the TTT essay (ren-xubin.github.io), paragraph on mini-batches and the dual
+ * form (gradients at the block start, effects accumulated in causal order);
+ * "Test-Time Training (TTT) Layers for Sequence Modeling" (dileepadev.github.io),
+ * "Mathematical Formulation" and "Variants: TTT-Linear vs. TTT-MLP".
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - All pointers are DEVICE pointers (cudaMalloc'd or equivalent) unless
+ *    stated otherwise, owned by the caller.  The library allocates no device
+ *    memory and keeps no per-call state.
+ *  - Layouts are dense row-major: Q, K, V, Z are [B][H][T][d]; eta is
+ *    [B][H][T] fp32; a weight matrix W is [B][H][d_in][d_out] fp32 with
+ *    f(x; W) = x W (row = input dimension).
+ *  - `dtype` is the element type of Q, K, V and Z (TTT_F32 or TTT_BF16).
+ *    Fast weights and eta are always fp32.  Kernels accumulate in fp32; bf16
+ *    contractions run on the tensor cores with fp32 accumulation; Z is rounded
+ *    to the output type with round-to-nearest-even.
+ *  - Every pointer must be 16-byte aligned.  Inputs must not overlap outputs,
+ *    except where an entry point allows the state to be updated in place.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *    stream).  Calls are asynchronous on that stream: on TTT_OK the work has
+ *    been enqueued, not finished.
+ *  - Errors: a bad argument returns TTT_ERR_INVALID_ARG (or
+ *    TTT_ERR_UNSUPPORTED for a well-formed shape outside the supported set)
+ *    before anything is launched; a failed CUDA launch returns TTT_ERR_CUDA
+ *    (text from ttt_last_error()).  A kernel never traps: a device-side
+ *    fault it can detect (an expired bounded wait) is recorded in a device
+ *    status word read by ttt_get_device_status().
+ *  - Empty problems (B*H == 0, or T == 0) launch nothing except the copy of
+ *    the initial state to the output state when T == 0 and they differ.
+ */
+#ifndef TTT_H_
+#define TTT_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum ttt_status {
+    TTT_OK = 0,
+    TTT_ERR_INVALID_ARG = 1, /* null/misaligned pointer, negative size, bad chunk; nothing launched */
+    TTT_ERR_UNSUPPORTED = 2, /* well-formed but outside the supported shapes; nothing launched */
+    TTT_ERR_CUDA = 3,        /* a CUDA runtime call failed (see ttt_last_error) */
+    TTT_ERR_TIMEOUT = 4      /* a bounded device-side wait expired (from ttt_get_device_status) */
+} ttt_status;
+
+typedef enum ttt_dtype {
+    TTT_F32 = 0,  /* float32 Q/K/V/Z */
+    TTT_BF16 = 1  /* bfloat16 Q/K/V/Z */
+} ttt_dtype;
+
+/*
+ * TTT-Linear prefill: the whole chunked scan over T tokens.
+ *
+ *   Q, K, V  [B][H][T][d]  dtype     queries, keys (training inputs), values (targets)
+ *   eta      [B][H][T]     fp32      per-token inner-loop step size
+ *   W0       [B][H][d][d]  fp32      initial fast weights (input)
+ *   Z        [B][H][T][d]  dtype     outputs z_t = q_t W_t (written)
+ *   W_out    [B][H][d][d]  fp32      fast weights after the last token (written);
+ *                                    may be the same buffer as W0 (in place)
+ *   chunk    1..512; the last block may be shorter when chunk does not divide T
+ *   d        16, 32, 64 or 128 (else TTT_ERR_UNSUPPORTED)
+ *
+ * Source: "Test-Time Training Layers ...", sections "The Core Mechanism" and
+ * "Hardware Parallelization"; TTT essay, paragraph on the dual form.
+ */
+ttt_status ttt_linear_prefill(const void* Q, const void* K, const void* V, const float* eta,
+                              const float* W0, void* Z, float* W_out, int B, int H, int T, int d,
+                              int chunk, ttt_dtype dtype, void* stream);
+
+/*
+ * TTT-MLP prefill: f(x; W1, W2) = GELU(x W1) W2 with the tanh form of GELU,
+ * no biases.  Per block, with start state (W1, W2):
+ *
+ *   Zk = K W1, Hk = GELU(Zk), E2 = Hk W2 - V, E1 = (E2 W2^T) . GELU'(Zk)
+ *   Hq = GELU(Q W1 - tril(eta . Q K^T) E1)
+ *   Z  = Hq W2 - tril(eta . Hq Hk^T) E2
+ *   W1 <- W1 - K^T diag(eta) E1,   W2 <- W2 - Hk^T diag(eta) E2
+ *
+ *   W1_0, W1_out  [B][H][d][hidden]  fp32  (W1_out may equal W1_0)
+ *   W2_0, W2_out  [B][H][hidden][d]  fp32  (W2_out may equal W2_0)
+ *   d in {16, 32, 64}; hidden a multiple of 16 with d*hidden <= 16384;
+ *   chunk 1..512 with chunk*hidden <= 8192 (last block may be shorter).
+ *
+ * Source: "Test-Time Training (TTT) Layers for Sequence Modeling", section
+ * "Variants: TTT-Linear vs. TTT-MLP" (two-layer MLP inner model); loss, step
+ * and readout as for TTT-Linear.
+ */
+ttt_status ttt_mlp_prefill(const void* Q, const void* K, const void* V, const float* eta,
+                           const float* W1_0, const float* W2_0, void* Z, float* W1_out,
+                           float* W2_out, int B, int H, int T, int d, int hidden, int chunk,
+                           ttt_dtype dtype, void* stream);
+
+/*
+ * TTT-Linear decode: one online step (a block of one token) for every
+ * (batch, head), updating the state in place:
+ *
+ *   e = k W - v;   W <- W - eta k^T e;   z = q W  (new W)
+ *
+ *   q, k, v, z  [B][H][d]     dtype
+ *   eta         [B][H]        fp32
+ *   W           [B][H][d][d]  fp32, read and written in place
+ *   d           16, 32, 64 or 128
+ *
+ * Source: "Test-Time Training Layers ...", section "The Core Mechanism" and
+ * the per-token forward step of its section "Python / PyTorch TTT-Linear Layer
+ * Implementation".
+ */
+ttt_status ttt_linear_decode_step(const void* q, const void* k, const void* v, const float* eta,
+                                  float* W, void* z, int B, int H, int d, ttt_dtype dtype,
+                                  void* stream);
+
+/*
+ * Reads and clears the device status word for the current device.
+ * Synchronises `stream`.  Returns TTT_OK, or the first error a kernel
+ * recorded since the last call (TTT_ERR_TIMEOUT for an expired bounded wait),
+ * or TTT_ERR_CUDA if the read itself failed.
+ */
+ttt_status ttt_get_device_status(void* stream);
+
+/* Static English text for a status code. */
+const char* ttt_status_string(ttt_status s);
+
+/* Text of the last TTT_ERR_* condition raised on the calling thread ("" if none). */
+const char* ttt_last_error(void);
+
+/* Library ABI version (major*10000 + minor*100 + patch). */
+int ttt_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TTT_H_ */

@@ -1,0 +1,190 @@
+// ttt_api.cu -- the C ABI of include/ttt.h: argument validation, kernel
+// selection, launch, status codes and the device status word.
+//
+// Every entry point validates all arguments before launching anything, so an
+// invalid call has no side effect on the device.  Kernel selection is by shape
+// and dtype only; there is exactly one implementation per shape.
+#include <cuda_runtime.h>
+
+#include <mutex>
+#include <stdio.h>
+#include <string.h>
+
+#include "../../include/ttt.h"
+#include "ttt_internal.h"
+
+namespace {
+
+thread_local char g_last_error[256] = "";
+
+ttt_status fail(ttt_status s, const char* fmt, const char* detail = "") {
+    snprintf(g_last_error, sizeof(g_last_error), fmt, detail);
+    return s;
+}
+
+ttt_status cuda_fail(cudaError_t e, const char* where) {
+    snprintf(g_last_error, sizeof(g_last_error), "%s: %s", where, cudaGetErrorString(e));
+    return TTT_ERR_CUDA;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool supported_d(int d) { return d == 16 || d == 32 || d == 64 || d == 128; }
+
+// Device status word: written by kernels (first error wins), read and cleared
+// by ttt_get_device_status().  One copy per device (a __device__ variable is
+// instantiated in every context that loads the module).
+__device__ int g_device_status;
+
+constexpr int kMaxDevices = 64;
+std::mutex g_status_mu;
+int* g_status_ptr[kMaxDevices] = {};
+
+cudaError_t status_ptr(int** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lk(g_status_mu);
+    if (!g_status_ptr[dev]) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_device_status);
+        if (e != cudaSuccess) return e;
+        g_status_ptr[dev] = static_cast<int*>(p);
+    }
+    *out = g_status_ptr[dev];
+    return cudaSuccess;
+}
+
+#define CHECK_PTR(p)                                                              \
+    do {                                                                          \
+        if (!(p)) return fail(TTT_ERR_INVALID_ARG, "null pointer argument: %s", #p); \
+        if (!aligned16(p)) return fail(TTT_ERR_INVALID_ARG, "pointer not 16-byte aligned: %s", #p); \
+    } while (0)
+
+}  // namespace
+
+extern "C" {
+
+ttt_status ttt_linear_prefill(const void* Q, const void* K, const void* V, const float* eta, const float* W0,
+                              void* Z, float* W_out, int B, int H, int T, int d, int chunk, ttt_dtype dtype,
+                              void* stream) {
+    g_last_error[0] = 0;
+    if (B < 0 || H < 0 || T < 0) return fail(TTT_ERR_INVALID_ARG, "negative size%s");
+    if (chunk < 1 || chunk > 512) return fail(TTT_ERR_INVALID_ARG, "chunk must be in 1..512%s");
+    if (dtype != TTT_F32 && dtype != TTT_BF16) return fail(TTT_ERR_INVALID_ARG, "unknown dtype%s");
+    if (d <= 0) return fail(TTT_ERR_INVALID_ARG, "head dim must be positive%s");
+    if (!supported_d(d)) return fail(TTT_ERR_UNSUPPORTED, "head dim must be 16, 32, 64 or 128%s");
+    if (size_t(B) * H == 0) return TTT_OK;
+    CHECK_PTR(W0);
+    CHECK_PTR(W_out);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (T == 0) {
+        if (W_out != W0) {
+            cudaError_t e = cudaMemcpyAsync(W_out, W0, size_t(B) * H * d * d * sizeof(float),
+                                            cudaMemcpyDeviceToDevice, s);
+            if (e != cudaSuccess) return cuda_fail(e, "ttt_linear_prefill copy");
+        }
+        return TTT_OK;
+    }
+    CHECK_PTR(Q);
+    CHECK_PTR(K);
+    CHECK_PTR(V);
+    CHECK_PTR(eta);
+    CHECK_PTR(Z);
+    ttt::LinearArgs a{Q, K, V, eta, W0, Z, W_out, B, H, T, d, chunk, dtype == TTT_BF16 ? 1 : 0};
+    cudaError_t e = ttt::launch_linear_prefill_generic(a, s);
+    if (e != cudaSuccess) return cuda_fail(e, "ttt_linear_prefill launch");
+    return TTT_OK;
+}
+
+ttt_status ttt_mlp_prefill(const void* Q, const void* K, const void* V, const float* eta, const float* W1_0,
+                           const float* W2_0, void* Z, float* W1_out, float* W2_out, int B, int H, int T, int d,
+                           int hidden, int chunk, ttt_dtype dtype, void* stream) {
+    g_last_error[0] = 0;
+    if (B < 0 || H < 0 || T < 0) return fail(TTT_ERR_INVALID_ARG, "negative size%s");
+    if (chunk < 1 || chunk > 512) return fail(TTT_ERR_INVALID_ARG, "chunk must be in 1..512%s");
+    if (dtype != TTT_F32 && dtype != TTT_BF16) return fail(TTT_ERR_INVALID_ARG, "unknown dtype%s");
+    if (d <= 0 || hidden <= 0) return fail(TTT_ERR_INVALID_ARG, "dimensions must be positive%s");
+    if (!(d == 16 || d == 32 || d == 64)) return fail(TTT_ERR_UNSUPPORTED, "MLP head dim must be 16, 32 or 64%s");
+    if (hidden % 16 != 0 || size_t(d) * hidden > 16384)
+        return fail(TTT_ERR_UNSUPPORTED, "MLP hidden must be a multiple of 16 with d*hidden <= 16384%s");
+    if (size_t(chunk) * hidden > 4096 || chunk > 64)
+        return fail(TTT_ERR_UNSUPPORTED, "MLP chunk must satisfy chunk <= 64 and chunk*hidden <= 4096%s");
+    if (size_t(B) * H == 0) return TTT_OK;
+    CHECK_PTR(W1_0);
+    CHECK_PTR(W2_0);
+    CHECK_PTR(W1_out);
+    CHECK_PTR(W2_out);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const size_t nw = size_t(B) * H * d * hidden * sizeof(float);
+    if (T == 0) {
+        cudaError_t e = cudaSuccess;
+        if (W1_out != W1_0) e = cudaMemcpyAsync(W1_out, W1_0, nw, cudaMemcpyDeviceToDevice, s);
+        if (e == cudaSuccess && W2_out != W2_0) e = cudaMemcpyAsync(W2_out, W2_0, nw, cudaMemcpyDeviceToDevice, s);
+        if (e != cudaSuccess) return cuda_fail(e, "ttt_mlp_prefill copy");
+        return TTT_OK;
+    }
+    CHECK_PTR(Q);
+    CHECK_PTR(K);
+    CHECK_PTR(V);
+    CHECK_PTR(eta);
+    CHECK_PTR(Z);
+    ttt::MlpArgs a{Q, K, V, eta, W1_0, W2_0, Z, W1_out, W2_out, B, H, T, d, hidden, chunk, dtype == TTT_BF16 ? 1 : 0};
+    cudaError_t e = ttt::launch_mlp_prefill_generic(a, s);
+    if (e != cudaSuccess) return cuda_fail(e, "ttt_mlp_prefill launch");
+    return TTT_OK;
+}
+
+ttt_status ttt_linear_decode_step(const void* q, const void* k, const void* v, const float* eta, float* W, void* z,
+                                  int B, int H, int d, ttt_dtype dtype, void* stream) {
+    g_last_error[0] = 0;
+    if (B < 0 || H < 0) return fail(TTT_ERR_INVALID_ARG, "negative size%s");
+    if (dtype != TTT_F32 && dtype != TTT_BF16) return fail(TTT_ERR_INVALID_ARG, "unknown dtype%s");
+    if (d <= 0) return fail(TTT_ERR_INVALID_ARG, "head dim must be positive%s");
+    if (!supported_d(d)) return fail(TTT_ERR_UNSUPPORTED, "head dim must be 16, 32, 64 or 128%s");
+    if (size_t(B) * H == 0) return TTT_OK;
+    if (size_t(B) * H > 0x7fffffffu) return fail(TTT_ERR_UNSUPPORTED, "B*H too large%s");
+    CHECK_PTR(q);
+    CHECK_PTR(k);
+    CHECK_PTR(v);
+    CHECK_PTR(eta);
+    CHECK_PTR(W);
+    CHECK_PTR(z);
+    ttt::DecodeArgs a{q, k, v, eta, W, z, B, H, d, dtype == TTT_BF16 ? 1 : 0};
+    cudaError_t e = ttt::launch_linear_decode(a, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "ttt_linear_decode_step launch");
+    return TTT_OK;
+}
+
+ttt_status ttt_get_device_status(void* stream) {
+    int* p = nullptr;
+    cudaError_t e = status_ptr(&p);
+    if (e != cudaSuccess) return cuda_fail(e, "ttt_get_device_status");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int h = 0;
+    e = cudaMemcpyAsync(&h, p, sizeof(int), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(p, 0, sizeof(int), s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e, "ttt_get_device_status");
+    if (h == 0) return TTT_OK;
+    if (h == TTT_ERR_TIMEOUT) return fail(TTT_ERR_TIMEOUT, "a bounded device-side wait expired%s");
+    return fail(static_cast<ttt_status>(h), "device reported status %s", "");
+}
+
+const char* ttt_status_string(ttt_status s) {
+    switch (s) {
+        case TTT_OK: return "ok";
+        case TTT_ERR_INVALID_ARG: return "invalid argument";
+        case TTT_ERR_UNSUPPORTED: return "unsupported shape";
+        case TTT_ERR_CUDA: return "CUDA error";
+        case TTT_ERR_TIMEOUT: return "device-side wait timed out";
+    }
+    return "unknown status";
+}
+
+const char* ttt_last_error(void) { return g_last_error; }
+
+int ttt_version(void) { return 100; }
+
+}  // extern "C"

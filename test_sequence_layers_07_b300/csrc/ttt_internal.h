@@ -1,0 +1,61 @@
+// ttt_internal.h -- host-side launchers shared between the C-ABI layer and the
+// kernel translation units.  Not part of the public ABI (see include/ttt.h).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace ttt {
+
+// Problem description handed from the validated C-ABI call to a launcher.
+struct LinearArgs {
+    const void* Q;
+    const void* K;
+    const void* V;
+    const float* eta;
+    const float* W0;
+    void* Z;
+    float* W_out;
+    int B, H, T, d, chunk;
+    int bf16;  // 1: Q/K/V/Z are bfloat16, 0: float32
+};
+
+struct MlpArgs {
+    const void* Q;
+    const void* K;
+    const void* V;
+    const float* eta;
+    const float* W1_0;
+    const float* W2_0;
+    void* Z;
+    float* W1_out;
+    float* W2_out;
+    int B, H, T, d, hidden, chunk;
+    int bf16;
+};
+
+struct DecodeArgs {
+    const void* q;
+    const void* k;
+    const void* v;
+    const float* eta;
+    float* W;
+    void* z;
+    int B, H, d;
+    int bf16;
+};
+
+// Generic SIMT kernels: every supported shape, fp32 accumulation.
+cudaError_t launch_linear_prefill_generic(const LinearArgs& a, cudaStream_t s);
+cudaError_t launch_mlp_prefill_generic(const MlpArgs& a, cudaStream_t s);
+size_t mlp_generic_smem_bytes(int d, int hidden, int chunk);
+
+// Tensor-core TTT-Linear prefill (bf16, register-resident state).  Returns
+// cudaErrorNotSupported when the shape is not covered, so the caller can use
+// the generic kernel instead.
+cudaError_t launch_linear_prefill_mma(const LinearArgs& a, cudaStream_t s, int* status);
+
+// Bandwidth-bound single-token step.
+cudaError_t launch_linear_decode(const DecodeArgs& a, cudaStream_t s);
+
+}  // namespace ttt

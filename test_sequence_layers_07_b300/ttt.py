@@ -1,0 +1,183 @@
+"""Python binding of libttt.so (include/ttt.h): argument marshalling only.
+
+The functions named like the C entry points (``ttt_linear_prefill``,
+``ttt_mlp_prefill``, ``ttt_linear_decode_step``) take torch CUDA tensors,
+check their dtype/shape/contiguity, pass raw device pointers and the current
+CUDA stream to the library and raise :class:`TTTError` on a non-OK status.
+Every step of the computation runs in the library's CUDA kernels; there is no
+CPU or PyTorch fallback.  If libttt.so is missing, importing the library
+raises immediately (build it with ``python -m test_sequence_layers_07_b300.build``).
+
+The lower-case helpers (``linear_prefill`` ...) allocate the outputs with
+torch and call the entry points above.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libttt.so")
+
+TTT_OK, TTT_ERR_INVALID_ARG, TTT_ERR_UNSUPPORTED, TTT_ERR_CUDA, TTT_ERR_TIMEOUT = range(5)
+TTT_F32, TTT_BF16 = 0, 1
+
+EXPORTED = ("ttt_linear_prefill", "ttt_mlp_prefill", "ttt_linear_decode_step", "ttt_get_device_status",
+            "ttt_status_string", "ttt_last_error", "ttt_version")
+
+
+class TTTError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"{msg} (status {status})")
+        self.status = status
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Loads libttt.so once; raises FileNotFoundError if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(path):
+                raise FileNotFoundError(
+                    f"{path} not found: build the CUDA library with "
+                    "`python -m test_sequence_layers_07_b300.build` (there is no fallback)")
+            lib = ctypes.CDLL(path)
+            vp, fp, i = ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int
+            lib.ttt_linear_prefill.argtypes = [vp, vp, vp, fp, fp, vp, fp, i, i, i, i, i, i, vp]
+            lib.ttt_mlp_prefill.argtypes = [vp, vp, vp, fp, fp, fp, vp, fp, fp, i, i, i, i, i, i, i, vp]
+            lib.ttt_linear_decode_step.argtypes = [vp, vp, vp, fp, fp, vp, i, i, i, i, vp]
+            lib.ttt_get_device_status.argtypes = [vp]
+            for f in (lib.ttt_linear_prefill, lib.ttt_mlp_prefill, lib.ttt_linear_decode_step,
+                      lib.ttt_get_device_status):
+                f.restype = i
+            lib.ttt_status_string.argtypes = [i]
+            lib.ttt_status_string.restype = ctypes.c_char_p
+            lib.ttt_last_error.argtypes = []
+            lib.ttt_last_error.restype = ctypes.c_char_p
+            lib.ttt_version.argtypes = []
+            lib.ttt_version.restype = i
+            _lib = lib
+    return _lib
+
+
+def _check(status: int):
+    if status != TTT_OK:
+        lib = load_library()
+        msg = lib.ttt_last_error().decode() or lib.ttt_status_string(status).decode()
+        raise TTTError(status, msg)
+
+
+def _stream(stream):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _ptr(t: torch.Tensor | None, name: str, dtype=None):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    return t.data_ptr()
+
+
+def _io_dtype(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return TTT_F32
+    if t.dtype == torch.bfloat16:
+        return TTT_BF16
+    raise TypeError(f"Q/K/V must be float32 or bfloat16, got {t.dtype}")
+
+
+def ttt_linear_prefill(Q, K, V, eta, W0, Z, W_out, chunk: int, stream=None) -> None:
+    """TTT-Linear prefill into caller-allocated Z [B,H,T,d] and W_out [B,H,d,d] (may be W0)."""
+    B, H, T, d = Q.shape
+    dt = _io_dtype(Q)
+    for name, t in (("K", K), ("V", V), ("Z", Z)):
+        if t.shape != Q.shape or t.dtype != Q.dtype:
+            raise ValueError(f"{name} must match Q in shape and dtype")
+    if eta.shape != (B, H, T) or W0.shape != (B, H, d, d) or W_out.shape != (B, H, d, d):
+        raise ValueError("eta must be [B,H,T] and W0/W_out [B,H,d,d]")
+    st = load_library().ttt_linear_prefill(
+        _ptr(Q, "Q"), _ptr(K, "K"), _ptr(V, "V"), _ptr(eta, "eta", torch.float32), _ptr(W0, "W0", torch.float32),
+        _ptr(Z, "Z"), _ptr(W_out, "W_out", torch.float32), B, H, T, d, int(chunk), dt, _stream(stream))
+    _check(st)
+
+
+def ttt_mlp_prefill(Q, K, V, eta, W1_0, W2_0, Z, W1_out, W2_out, chunk: int, stream=None) -> None:
+    """TTT-MLP prefill into caller-allocated Z, W1_out [B,H,d,hidden], W2_out [B,H,hidden,d]."""
+    B, H, T, d = Q.shape
+    hidden = W1_0.shape[-1]
+    dt = _io_dtype(Q)
+    for name, t in (("K", K), ("V", V), ("Z", Z)):
+        if t.shape != Q.shape or t.dtype != Q.dtype:
+            raise ValueError(f"{name} must match Q in shape and dtype")
+    if eta.shape != (B, H, T) or W1_0.shape != (B, H, d, hidden) or W2_0.shape != (B, H, hidden, d):
+        raise ValueError("eta must be [B,H,T], W1 [B,H,d,hidden], W2 [B,H,hidden,d]")
+    if W1_out.shape != W1_0.shape or W2_out.shape != W2_0.shape:
+        raise ValueError("output weights must match the input weights' shapes")
+    st = load_library().ttt_mlp_prefill(
+        _ptr(Q, "Q"), _ptr(K, "K"), _ptr(V, "V"), _ptr(eta, "eta", torch.float32),
+        _ptr(W1_0, "W1_0", torch.float32), _ptr(W2_0, "W2_0", torch.float32), _ptr(Z, "Z"),
+        _ptr(W1_out, "W1_out", torch.float32), _ptr(W2_out, "W2_out", torch.float32),
+        B, H, T, d, hidden, int(chunk), dt, _stream(stream))
+    _check(st)
+
+
+def ttt_linear_decode_step(q, k, v, eta, W, z, stream=None) -> None:
+    """One online TTT-Linear step; W [B,H,d,d] fp32 is updated in place, z written."""
+    B, H, d = q.shape
+    dt = _io_dtype(q)
+    for name, t in (("k", k), ("v", v), ("z", z)):
+        if t.shape != q.shape or t.dtype != q.dtype:
+            raise ValueError(f"{name} must match q in shape and dtype")
+    if eta.shape != (B, H) or W.shape != (B, H, d, d):
+        raise ValueError("eta must be [B,H] and W [B,H,d,d]")
+    st = load_library().ttt_linear_decode_step(
+        _ptr(q, "q"), _ptr(k, "k"), _ptr(v, "v"), _ptr(eta, "eta", torch.float32), _ptr(W, "W", torch.float32),
+        _ptr(z, "z"), B, H, d, dt, _stream(stream))
+    _check(st)
+
+
+def ttt_get_device_status(stream=None) -> int:
+    """Reads and clears the device status word (synchronises the stream); returns the status code."""
+    return load_library().ttt_get_device_status(_stream(stream))
+
+
+# ---------------------------------------------------------------- helpers
+
+def linear_prefill(Q, K, V, eta, W0, chunk: int, stream=None):
+    """Returns (Z, W_final) for a TTT-Linear prefill, outputs allocated by torch."""
+    Z = torch.empty_like(Q)
+    W = torch.empty_like(W0)
+    ttt_linear_prefill(Q, K, V, eta, W0, Z, W, chunk, stream)
+    return Z, W
+
+
+def mlp_prefill(Q, K, V, eta, W1, W2, chunk: int, stream=None):
+    """Returns (Z, W1_final, W2_final) for a TTT-MLP prefill."""
+    Z = torch.empty_like(Q)
+    W1o = torch.empty_like(W1)
+    W2o = torch.empty_like(W2)
+    ttt_mlp_prefill(Q, K, V, eta, W1, W2, Z, W1o, W2o, chunk, stream)
+    return Z, W1o, W2o
+
+
+def linear_decode_step(q, k, v, eta, W, stream=None):
+    """Returns z; W is updated in place."""
+    z = torch.empty_like(q)
+    ttt_linear_decode_step(q, k, v, eta, W, z, stream)
+    return z

@@ -1,0 +1,141 @@
+"""Host-side checks of the C ABI (no GPU needed).
+
+* libttt.so loads and exports every function include/ttt.h declares;
+* argument validation returns the documented status before any CUDA call
+  (null or misaligned pointers, negative sizes, bad chunk, unsupported d);
+* empty problems (B*H == 0) return TTT_OK without touching the device.
+"""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from test_sequence_layers_07_b300 import build as B
+from test_sequence_layers_07_b300 import ttt as T
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "ttt.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(T.LIB_PATH):
+        B.build()
+    return T.load_library()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(ttt_[a-z_0-9]+)\s*\(", src)))
+
+
+def test_header_declares_the_documented_entry_points():
+    names = declared_functions()
+    for n in ("ttt_linear_prefill", "ttt_mlp_prefill", "ttt_linear_decode_step", "ttt_get_device_status"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", T.LIB_PATH], capture_output=True, text=True,
+                         check=True).stdout
+    exported = set(re.findall(r"\bT (ttt_\w+)", out))
+    missing = [n for n in declared_functions() if n not in exported]
+    assert not missing, missing
+    for n in declared_functions():
+        assert hasattr(lib, n)
+    assert set(T.EXPORTED) == set(declared_functions())
+
+
+def test_header_compiles_as_c():
+    r = subprocess.run(["gcc", "-x", "c", "-std=c99", "-fsyntax-only", "-Wall", "-Werror", HEADER],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+
+
+def test_status_strings(lib):
+    assert lib.ttt_status_string(0) == b"ok"
+    assert lib.ttt_status_string(1) == b"invalid argument"
+    assert lib.ttt_status_string(4) == b"device-side wait timed out"
+    assert lib.ttt_version() >= 100
+
+
+# fake 16-byte-aligned addresses: validation must reject the call before using them
+A = 0x10000
+MIS = 0x10008
+NULL = None
+
+
+def lp(lib, Q=A, K=A, V=A, eta=A, W0=A, Z=A, Wo=A, B_=1, H=1, T_=16, d=64, chunk=16, dt=1):
+    return lib.ttt_linear_prefill(Q, K, V, eta, W0, Z, Wo, B_, H, T_, d, chunk, dt, None)
+
+
+def test_linear_prefill_validation(lib):
+    assert lp(lib, Q=NULL) == T.TTT_ERR_INVALID_ARG
+    assert b"Q" in lib.ttt_last_error()
+    assert lp(lib, W0=NULL) == T.TTT_ERR_INVALID_ARG
+    assert lp(lib, Z=MIS) == T.TTT_ERR_INVALID_ARG
+    assert b"aligned" in lib.ttt_last_error()
+    assert lp(lib, B_=-1) == T.TTT_ERR_INVALID_ARG
+    assert lp(lib, T_=-3) == T.TTT_ERR_INVALID_ARG
+    assert lp(lib, chunk=0) == T.TTT_ERR_INVALID_ARG
+    assert lp(lib, chunk=513) == T.TTT_ERR_INVALID_ARG
+    assert lp(lib, dt=7) == T.TTT_ERR_INVALID_ARG
+    assert lp(lib, d=0) == T.TTT_ERR_INVALID_ARG
+    assert lp(lib, d=48) == T.TTT_ERR_UNSUPPORTED
+    assert lp(lib, d=256) == T.TTT_ERR_UNSUPPORTED
+    # empty batch: nothing to do, no device access even with null pointers
+    assert lp(lib, Q=NULL, K=NULL, V=NULL, eta=NULL, W0=NULL, Z=NULL, Wo=NULL, B_=0) == T.TTT_OK
+    assert lp(lib, Q=NULL, K=NULL, V=NULL, eta=NULL, W0=NULL, Z=NULL, Wo=NULL, H=0) == T.TTT_OK
+
+
+def test_mlp_prefill_validation(lib):
+    def mp(**kw):
+        a = dict(Q=A, K=A, V=A, eta=A, W1=A, W2=A, Z=A, W1o=A, W2o=A, B_=1, H=1, T_=16, d=64, hd=256, chunk=16,
+                 dt=1)
+        a.update(kw)
+        return lib.ttt_mlp_prefill(a["Q"], a["K"], a["V"], a["eta"], a["W1"], a["W2"], a["Z"], a["W1o"], a["W2o"],
+                                   a["B_"], a["H"], a["T_"], a["d"], a["hd"], a["chunk"], a["dt"], None)
+    assert mp(W2=NULL) == T.TTT_ERR_INVALID_ARG
+    assert mp(W1o=MIS) == T.TTT_ERR_INVALID_ARG
+    assert mp(chunk=0) == T.TTT_ERR_INVALID_ARG
+    assert mp(d=128, hd=512) == T.TTT_ERR_UNSUPPORTED
+    assert mp(hd=250) == T.TTT_ERR_UNSUPPORTED
+    assert mp(chunk=32) == T.TTT_ERR_UNSUPPORTED  # chunk*hidden > 4096
+    assert mp(hd=0) == T.TTT_ERR_INVALID_ARG
+    assert mp(B_=0, Q=NULL, W1=NULL) == T.TTT_OK
+
+
+def test_decode_validation(lib):
+    def dp(**kw):
+        a = dict(q=A, k=A, v=A, eta=A, W=A, z=A, B_=2, H=3, d=64, dt=1)
+        a.update(kw)
+        return lib.ttt_linear_decode_step(a["q"], a["k"], a["v"], a["eta"], a["W"], a["z"], a["B_"], a["H"], a["d"],
+                                          a["dt"], None)
+    assert dp(W=NULL) == T.TTT_ERR_INVALID_ARG
+    assert dp(eta=MIS) == T.TTT_ERR_INVALID_ARG
+    assert dp(d=40) == T.TTT_ERR_UNSUPPORTED
+    assert dp(H=-1) == T.TTT_ERR_INVALID_ARG
+    assert dp(B_=0, W=NULL) == T.TTT_OK
+
+
+def test_binding_rejects_cpu_tensors(lib):
+    import torch
+    x = torch.zeros(1, 1, 16, 16)
+    with pytest.raises((TypeError, ValueError)):
+        T.ttt_linear_prefill(x, x, x, torch.zeros(1, 1, 16), torch.zeros(1, 1, 16, 16), x, torch.zeros(1, 1, 16, 16), 16)
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    with pytest.raises(FileNotFoundError):
+        # a fresh loader pointed at a path with no library must raise, not fall back
+        import importlib
+        mod = importlib.import_module("test_sequence_layers_07_b300.ttt")
+        saved = mod._lib
+        try:
+            mod._lib = None
+            mod.load_library(str(tmp_path / "libttt.so"))
+        finally:
+            mod._lib = saved

@@ -1,0 +1,200 @@
+"""GPU parity: the CUDA library (through its C ABI) against the fp64 oracle.
+
+Error metric: max|delta| / ||ref||_inf per output; bar 1e-4 for fp32 inputs and
+2e-2 for bf16 inputs, applied to Z and to every final weight matrix.  Inputs
+are the seeded workloads of test_sequence_layers_07_b300.workloads; the oracle
+reads exactly the rounded values the GPU reads.
+"""
+import numpy as np
+import pytest
+import torch
+
+from oracle import oracle as O
+from test_sequence_layers_07_b300 import ttt as T
+from test_sequence_layers_07_b300 import workloads as WL
+from tests._parity import TOL, cuda, f64, heads, rel_err
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    T.load_library()
+    yield
+    assert T.ttt_get_device_status() == T.TTT_OK
+
+
+def run_linear(x, chunk):
+    g = cuda(x)
+    Z, W = T.linear_prefill(g["Q"], g["K"], g["V"], g["eta"], g["W0"], chunk)
+    torch.cuda.synchronize()
+    return Z, W
+
+
+def run_mlp(x, chunk):
+    g = cuda(x)
+    Z, W1, W2 = T.mlp_prefill(g["Q"], g["K"], g["V"], g["eta"], g["W1"], g["W2"], chunk)
+    torch.cuda.synchronize()
+    return Z, W1, W2
+
+
+# ------------------------------------------------------------------ TTT-Linear
+
+def test_oracle_check_workload_fp32():
+    w = WL.WORKLOADS["oracle_check"]
+    x = WL.workload_inputs(w)
+    Z, W = run_linear(x, w.chunk)
+    r = f64(x)
+    for fn in (O.linear_dual, O.linear_primal):
+        Zr, Wr = fn(r["Q"], r["K"], r["V"], r["eta"], r["W0"], w.chunk)
+        assert rel_err(Z, Zr) <= TOL["f32"]
+        assert rel_err(W, Wr) <= TOL["f32"]
+
+
+LIN_CASES = [(200, 16), (200, 37), (64, 1), (96, 64), (300, 512), (13, 16)]
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("d", [16, 32, 64, 128])
+@pytest.mark.parametrize("T_,chunk", LIN_CASES)
+def test_linear_small_shapes(dtype, d, T_, chunk):
+    x = WL.linear_inputs(2, 3, T_, d, seed=100 + d + T_ + chunk, dtype=dtype)
+    Z, W = run_linear(x, chunk)
+    r = f64(x)
+    Zr, Wr = O.linear_dual(r["Q"], r["K"], r["V"], r["eta"], r["W0"], chunk)
+    assert rel_err(Z, Zr) <= TOL[dtype]
+    assert rel_err(W, Wr) <= TOL[dtype]
+
+
+def test_linear_prefill_workload_sampled_heads():
+    w = WL.WORKLOADS["linear_prefill"]
+    x = WL.workload_inputs(w)
+    Z, W = run_linear(x, w.chunk)
+    assert torch.isfinite(Z.float()).all() and torch.isfinite(W).all()
+    idx = [(0, 0), (3, 7), (7, 11), (5, 2), (1, 9), (6, 5)]
+    r = heads(f64(x), idx)
+    Zr, Wr = O.linear_dual(r["Q"], r["K"], r["V"], r["eta"], r["W0"], w.chunk)
+    Zs = torch.stack([Z[b, h] for b, h in idx])[None]
+    Ws = torch.stack([W[b, h] for b, h in idx])[None]
+    assert rel_err(Zs, Zr) <= TOL["bf16"]
+    assert rel_err(Ws, Wr) <= TOL["bf16"]
+
+
+@pytest.mark.parametrize("chunk", [16, 64, 512])
+def test_long_context_workload_sampled_heads(chunk):
+    w = WL.WORKLOADS["long_context"]
+    x = WL.workload_inputs(w)
+    Z, W = run_linear(x, chunk)
+    assert torch.isfinite(Z.float()).all() and torch.isfinite(W).all()
+    idx = [(0, 3), (0, 14)]
+    r = heads(f64(x), idx)
+    Zr, Wr = O.linear_dual(r["Q"], r["K"], r["V"], r["eta"], r["W0"], chunk)
+    Zs = torch.stack([Z[b, h] for b, h in idx])[None]
+    Ws = torch.stack([W[b, h] for b, h in idx])[None]
+    assert rel_err(Zs, Zr) <= TOL["bf16"]
+    assert rel_err(Ws, Wr) <= TOL["bf16"]
+
+
+def test_linear_in_place_state_and_split_resume():
+    x = WL.linear_inputs(2, 2, 128, 64, seed=7, dtype="bf16")
+    g = cuda(x)
+    Z_full, W_full = T.linear_prefill(g["Q"], g["K"], g["V"], g["eta"], g["W0"], 16)
+    # two calls split at a block boundary, the second resuming from the first's state, in place
+    W = g["W0"].clone()
+    Za = torch.empty_like(g["Q"][:, :, :48].contiguous())
+    T.ttt_linear_prefill(g["Q"][:, :, :48].contiguous(), g["K"][:, :, :48].contiguous(),
+                         g["V"][:, :, :48].contiguous(), g["eta"][:, :, :48].contiguous(), W, Za, W, 16)
+    Zb = torch.empty_like(g["Q"][:, :, 48:].contiguous())
+    T.ttt_linear_prefill(g["Q"][:, :, 48:].contiguous(), g["K"][:, :, 48:].contiguous(),
+                         g["V"][:, :, 48:].contiguous(), g["eta"][:, :, 48:].contiguous(), W, Zb, W, 16)
+    torch.cuda.synchronize()
+    r = f64(x)
+    Zr, Wr = O.linear_dual(r["Q"], r["K"], r["V"], r["eta"], r["W0"], 16)
+    assert rel_err(torch.cat([Za, Zb], 2), Zr) <= TOL["bf16"]
+    assert rel_err(W, Wr) <= TOL["bf16"]
+    assert rel_err(W_full, Wr) <= TOL["bf16"]
+
+
+def test_linear_empty_sequence_copies_state():
+    x = cuda(WL.linear_inputs(1, 2, 16, 32, seed=3, dtype="f32"))
+    Wo = torch.full_like(x["W0"], 7.0)
+    Z = torch.empty(1, 2, 0, 32, device="cuda")
+    T.ttt_linear_prefill(Z, Z, Z, torch.empty(1, 2, 0, device="cuda"), x["W0"], Z, Wo, 16)
+    torch.cuda.synchronize()
+    assert torch.equal(Wo, x["W0"])
+
+
+def test_linear_deterministic():
+    x = WL.linear_inputs(2, 3, 256, 64, seed=11, dtype="bf16")
+    Z1, W1 = run_linear(x, 16)
+    Z2, W2 = run_linear(x, 16)
+    assert torch.equal(Z1, Z2) and torch.equal(W1, W2)
+
+
+# -------------------------------------------------------------------- TTT-MLP
+
+MLP_CASES = [(48, 16), (50, 16), (20, 1), (40, 8)]
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("d", [16, 32, 64])
+@pytest.mark.parametrize("T_,chunk", MLP_CASES)
+def test_mlp_small_shapes(dtype, d, T_, chunk):
+    x = WL.mlp_inputs(2, 2, T_, d, 4 * d, seed=200 + d + T_ + chunk, dtype=dtype, w_std=0.1)
+    Z, W1, W2 = run_mlp(x, chunk)
+    r = f64(x)
+    Zr, W1r, W2r = O.mlp_dual(r["Q"], r["K"], r["V"], r["eta"], r["W1"], r["W2"], chunk)
+    assert rel_err(Z, Zr) <= TOL[dtype]
+    assert rel_err(W1, W1r) <= TOL[dtype]
+    assert rel_err(W2, W2r) <= TOL[dtype]
+
+
+def test_mlp_prefill_workload_sampled_heads():
+    w = WL.WORKLOADS["mlp_prefill"]
+    x = WL.workload_inputs(w)
+    Z, W1, W2 = run_mlp(x, w.chunk)
+    assert torch.isfinite(Z.float()).all()
+    idx = [(0, 0), (4, 6), (7, 11), (2, 3)]
+    r = heads(f64(x), idx)
+    Zr, W1r, W2r = O.mlp_dual(r["Q"], r["K"], r["V"], r["eta"], r["W1"], r["W2"], w.chunk)
+    pick = lambda t: torch.stack([t[b, h] for b, h in idx])[None]
+    assert rel_err(pick(Z), Zr) <= TOL["bf16"]
+    assert rel_err(pick(W1), W1r) <= TOL["bf16"]
+    assert rel_err(pick(W2), W2r) <= TOL["bf16"]
+
+
+# ------------------------------------------------------------------- decode
+
+def test_decode_workload_steps():
+    w = WL.WORKLOADS["decode"]
+    steps = 4
+    x = WL.decode_inputs(w.B, w.H, w.d, steps, w.seed)
+    W = x["W"].cuda()
+    Wr = WL.to_f64(x["W"])
+    for s in range(steps):
+        q, k, v, e = (x[n][s].cuda() for n in ("q", "k", "v", "eta"))
+        z = T.linear_decode_step(q, k, v, e, W)
+        torch.cuda.synchronize()
+        zr, Wr = O.linear_decode(WL.to_f64(x["q"][s]), WL.to_f64(x["k"][s]), WL.to_f64(x["v"][s]),
+                                 WL.to_f64(x["eta"][s]), Wr)
+        assert rel_err(z, zr) <= TOL["bf16"]
+        assert rel_err(W, Wr) <= TOL["bf16"]
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("d", [16, 32, 64, 128])
+def test_decode_matches_online_prefill(dtype, d):
+    # T decode steps equal a prefill with one-token blocks
+    x = WL.linear_inputs(3, 2, 12, d, seed=300 + d, dtype=dtype)
+    g = cuda(x)
+    W = g["W0"].clone()
+    zs = []
+    for t in range(12):
+        zs.append(T.linear_decode_step(g["Q"][:, :, t].contiguous(), g["K"][:, :, t].contiguous(),
+                                       g["V"][:, :, t].contiguous(), g["eta"][:, :, t].contiguous(), W))
+    torch.cuda.synchronize()
+    r = f64(x)
+    Zr, Wr = O.linear_primal(r["Q"], r["K"], r["V"], r["eta"], r["W0"], 1)
+    assert rel_err(torch.stack(zs, 2), Zr) <= TOL[dtype]
+    assert rel_err(W, Wr) <= TOL[dtype]
