@@ -90,38 +90,68 @@ def ncu_traffic(kernel_key, src_files):
     return d.get("dram_bytes_per_launch")
 
 
+class _Nvml:
+    """Minimal ctypes binding of libnvidia-ml (clock and clock-event-reason queries only)."""
+
+    def __init__(self):
+        import ctypes
+        self.c = ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit_v2 failed")
+
+    def handle(self, pci_bus_id: str):
+        h = self.c.c_void_p()
+        r = self.lib.nvmlDeviceGetHandleByPciBusId_v2(pci_bus_id.encode(), self.c.byref(h))
+        if r != 0:
+            r = self.lib.nvmlDeviceGetHandleByIndex_v2(0, self.c.byref(h))
+        if r != 0:
+            raise RuntimeError(f"nvml handle lookup failed ({r})")
+        return h
+
+    def clock(self, h, max_=False):
+        v = self.c.c_uint()
+        f = self.lib.nvmlDeviceGetMaxClockInfo if max_ else self.lib.nvmlDeviceGetClockInfo
+        if f(h, 1, self.c.byref(v)) != 0:  # 1 = NVML_CLOCK_SM
+            raise RuntimeError("clock query failed")
+        return v.value
+
+    def reasons(self, h):
+        v = self.c.c_ulonglong()
+        if self.lib.nvmlDeviceGetCurrentClocksEventReasons(h, self.c.byref(v)) != 0:
+            raise RuntimeError("reason query failed")
+        return v.value
+
+
 class ClockSampler:
-    """Samples SM clock and clock-event reasons with NVML while the timed region runs."""
+    """Samples SM clock and clock-event reasons (NVML through ctypes) while the timed region runs."""
 
     REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
                0x80: "hw_power_brake_slowdown", 0x2: "applications_clocks_setting", 0x1: "gpu_idle",
                0x10: "sync_boost"}
 
-    def __init__(self, device=0, interval=0.005):
+    def __init__(self, device=0, interval=0.002):
         self.interval = interval
         self.samples, self.reasons = [], set()
         self.max_mhz = None
         self._stop = threading.Event()
-        self._h = None
+        self._err = None
+        self._nv = None
         try:
-            import pynvml
-            pynvml.nvmlInit()
-            self._nv = pynvml
-            uuid = str(torch.cuda.get_device_properties(device).uuid)
-            try:
-                self._h = pynvml.nvmlDeviceGetHandleByUUID(("GPU-" + uuid) if not uuid.startswith("GPU-") else uuid)
-            except Exception:
-                self._h = pynvml.nvmlDeviceGetHandleByIndex(device)
-            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self._h, pynvml.NVML_CLOCK_SM)
-        except Exception as e:  # no NVML: report nothing rather than guess
-            self._err = str(e)
+            self._nv = _Nvml()
+            props = torch.cuda.get_device_properties(device)
+            bus = "%08X:%02X:%02X.0" % (props.pci_domain_id, props.pci_bus_id, props.pci_device_id)
+            self._h = self._nv.handle(bus)
+            self.max_mhz = self._nv.clock(self._h, max_=True)
+        except Exception as e:
+            self._nv = None
+            self._err = f"nvml: {e!r}"
 
     def _run(self):
-        nv = self._nv
         while not self._stop.is_set():
             try:
-                self.samples.append(nv.nvmlDeviceGetClockInfo(self._h, nv.NVML_CLOCK_SM))
-                r = nv.nvmlDeviceGetCurrentClocksEventReasons(self._h)
+                self.samples.append(self._nv.clock(self._h))
+                r = self._nv.reasons(self._h)
                 for bit, name in self.REASONS.items():
                     if r & bit:
                         self.reasons.add(name)
@@ -130,22 +160,23 @@ class ClockSampler:
             time.sleep(self.interval)
 
     def __enter__(self):
-        if self._h is not None:
+        if self._nv is not None:
             self._t = threading.Thread(target=self._run, daemon=True)
             self._t.start()
         return self
 
     def __exit__(self, *a):
-        if self._h is not None:
+        if self._nv is not None:
             self._stop.set()
             self._t.join()
 
     def summary(self):
-        if self._h is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvml unavailable"], "samples": 0}
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": [], "samples": 0,
+                    "note": self._err or "no samples in the timed region"}
         reasons = sorted(self.reasons - {"gpu_idle"})
-        return {"sm_mhz": statistics.median(self.samples) if self.samples else None, "sm_max_mhz": self.max_mhz,
-                "reasons": reasons, "samples": len(self.samples)}
+        return {"sm_mhz": statistics.median(self.samples), "sm_max_mhz": self.max_mhz, "reasons": reasons,
+                "samples": len(self.samples)}
 
 
 def dist_setup(gpus):
@@ -180,16 +211,23 @@ def max_over_ranks(x: float, world: int) -> float:
     return float(t.item())
 
 
-def timed_loop(fn, steps, warmup, world, stream=None, sampler=None):
+def timed_loop(fn, steps, warmup, world, stream=None, sampler=None, min_warm_s=0.3):
     """Runs `fn(i)` warmup times untimed, then `steps` times between two barriers + syncs.
 
-    Returns (ms_per_step over the whole region, max over ranks; mean per-launch ms from
-    per-call CUDA events on the launching stream).
+    Warm-up runs at least `warmup` steps and at least `min_warm_s` seconds (so the
+    clocks have ramped up).  Returns (ms_per_step over the whole region, max over
+    ranks; mean per-launch ms from per-call CUDA events on the launching stream).
     """
     stream = stream or torch.cuda.current_stream()
-    for i in range(warmup):
+    t_start = time.perf_counter()
+    i = 0
+    while i < warmup or time.perf_counter() - t_start < min_warm_s:
         fn(i)
+        i += 1
+        if i % 16 == 0:
+            torch.cuda.synchronize()
     torch.cuda.synchronize()
+    warmup = i
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
@@ -370,18 +408,18 @@ def run_ours(args):
         "gpu_launches": args.steps,
     }
     if not args.no_e2e:
-        line["e2e"] = bench_e2e(T_mod, w, max(3, args.steps // 4), args.warmup, world)
+        line["e2e"] = bench_e2e(T_mod, w, max(5, min(200, args.steps // 10)), args.warmup, world)
     if args.rows == "all":
         rows = {}
         rows["linear_prefill"] = head
         wm = WL.WORKLOADS["mlp_prefill"]
-        rows["mlp_prefill"] = bench_mlp(T_mod, wm, max(3, args.steps // 4), args.warmup, world, peaks)
+        rsteps = max(5, min(50, args.steps // 20))
+        rows["mlp_prefill"] = bench_mlp(T_mod, wm, rsteps, args.warmup, world, peaks)
         wl = WL.WORKLOADS["long_context"]
         for b in wl.chunks:
-            rows[f"long_context_b{b}"] = bench_linear(T_mod, wl, b, max(3, args.steps // 8), args.warmup, world,
-                                                      peaks, nrot=1)
+            rows[f"long_context_b{b}"] = bench_linear(T_mod, wl, b, rsteps, args.warmup, world, peaks, nrot=1)
         wd = WL.WORKLOADS["decode"]
-        rows["decode"] = bench_decode(T_mod, wd, max(3, args.steps // 20), args.warmup, world, peaks)
+        rows["decode"] = bench_decode(T_mod, wd, max(3, rsteps // 5), args.warmup, world, peaks)
         line["rows"] = rows
     if rank == 0 and world == 1 and not args.no_cpu:
         line["cpu_baseline"] = cpu_baseline(w)
@@ -424,13 +462,13 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
-LINEAR_SRC = ["linear_prefill_generic.cu"]
+LINEAR_SRC = ["linear_prefill_mma.cu", "ptx.cuh"]
 
 
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--rows", choices=["all", "none"], default="all")

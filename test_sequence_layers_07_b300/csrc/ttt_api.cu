@@ -93,7 +93,12 @@ ttt_status ttt_linear_prefill(const void* Q, const void* K, const void* V, const
     CHECK_PTR(eta);
     CHECK_PTR(Z);
     ttt::LinearArgs a{Q, K, V, eta, W0, Z, W_out, B, H, T, d, chunk, dtype == TTT_BF16 ? 1 : 0};
-    cudaError_t e = ttt::launch_linear_prefill_generic(a, s);
+    int* status = nullptr;
+    cudaError_t e = status_ptr(&status);
+    if (e != cudaSuccess) return cuda_fail(e, "ttt_linear_prefill status word");
+    // tensor-core kernel for bf16, d in {64, 128}, 16 | chunk, chunk | T; generic kernel otherwise
+    e = ttt::launch_linear_prefill_mma(a, s, status);
+    if (e == cudaErrorNotSupported) e = ttt::launch_linear_prefill_generic(a, s);
     if (e != cudaSuccess) return cuda_fail(e, "ttt_linear_prefill launch");
     return TTT_OK;
 }
