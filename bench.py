@@ -409,17 +409,19 @@ def run_ours(args):
     }
     if not args.no_e2e:
         line["e2e"] = bench_e2e(T_mod, w, max(5, min(200, args.steps // 10)), args.warmup, world)
-    if args.rows == "all":
-        rows = {}
-        rows["linear_prefill"] = head
-        wm = WL.WORKLOADS["mlp_prefill"]
+    if args.rows != "none":
+        want = lambda name: args.rows in ("all", name)
+        rows = {"linear_prefill": head}
         rsteps = max(5, min(50, args.steps // 20))
-        rows["mlp_prefill"] = bench_mlp(T_mod, wm, rsteps, args.warmup, world, peaks)
-        wl = WL.WORKLOADS["long_context"]
-        for b in wl.chunks:
-            rows[f"long_context_b{b}"] = bench_linear(T_mod, wl, b, rsteps, args.warmup, world, peaks, nrot=1)
-        wd = WL.WORKLOADS["decode"]
-        rows["decode"] = bench_decode(T_mod, wd, max(3, rsteps // 5), args.warmup, world, peaks)
+        if want("mlp_prefill"):
+            rows["mlp_prefill"] = bench_mlp(T_mod, WL.WORKLOADS["mlp_prefill"], rsteps, args.warmup, world, peaks)
+        if want("long_context"):
+            wl = WL.WORKLOADS["long_context"]
+            for b in wl.chunks:
+                rows[f"long_context_b{b}"] = bench_linear(T_mod, wl, b, rsteps, args.warmup, world, peaks, nrot=1)
+        if want("decode"):
+            wd = WL.WORKLOADS["decode"]
+            rows["decode"] = bench_decode(T_mod, wd, max(3, rsteps // 5), args.warmup, world, peaks)
         line["rows"] = rows
     if rank == 0 and world == 1 and not args.no_cpu:
         line["cpu_baseline"] = cpu_baseline(w)
@@ -471,7 +473,8 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--rows", choices=["all", "none"], default="all")
+    ap.add_argument("--rows", choices=["all", "none", "mlp_prefill", "long_context", "decode"], default="all",
+                    help="workload rows timed after the headline (default: all)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     args = ap.parse_args(argv)
