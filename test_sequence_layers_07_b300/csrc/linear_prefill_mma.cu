@@ -304,48 +304,15 @@ linear_prefill_mma_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_
 
 // ---------------------------------------------------------------- host side
 
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-cudaError_t get_encoder(EncodeTiledFn* fn) {
-    static EncodeTiledFn cached = nullptr;
-    if (!cached) {
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q);
-        if (e != cudaSuccess) return e;
-        if (q != cudaDriverEntryPointSuccess || !p) return cudaErrorSymbolNotFound;
-        cached = reinterpret_cast<EncodeTiledFn>(p);
-    }
-    *fn = cached;
-    return cudaSuccess;
-}
-
-// [rows][D] bf16 viewed as a 2D tensor; box = 16 rows x 64 columns, 128-byte swizzle.
-cudaError_t make_map(CUtensorMap* m, const void* base, uint64_t rows, int D) {
-    EncodeTiledFn enc;
-    cudaError_t e = get_encoder(&enc);
-    if (e != cudaSuccess) return e;
-    cuuint64_t dims[2] = {cuuint64_t(D), cuuint64_t(rows)};
-    cuuint64_t strides[1] = {cuuint64_t(D) * 2};
-    cuuint32_t box[2] = {64, 16};
-    cuuint32_t estr[2] = {1, 1};
-    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
-}
-
 template <int D, int CG, int NST, bool SINGLE>
 cudaError_t launch_cfg(const LinearArgs& a, cudaStream_t s, int* status) {
     using C = MmaCfg<D, CG, NST>;
     const uint64_t rows = uint64_t(a.B) * a.H * a.T;
     CUtensorMap mq, mk, mv;
     cudaError_t e;
-    if ((e = make_map(&mq, a.Q, rows, D)) != cudaSuccess) return e;
-    if ((e = make_map(&mk, a.K, rows, D)) != cudaSuccess) return e;
-    if ((e = make_map(&mv, a.V, rows, D)) != cudaSuccess) return e;
+    if ((e = make_tma_map_bf16(&mq, a.Q, rows, D)) != cudaSuccess) return e;
+    if ((e = make_tma_map_bf16(&mk, a.K, rows, D)) != cudaSuccess) return e;
+    if ((e = make_tma_map_bf16(&mv, a.V, rows, D)) != cudaSuccess) return e;
     auto kern = linear_prefill_mma_kernel<D, CG, NST, SINGLE>;
     const int bytes = C::BYTES + 1024;  // + alignment slack
     if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) != cudaSuccess) return e;
@@ -370,6 +337,39 @@ int pick_cg(int d, long long bh, int sms) {
 }
 
 }  // namespace
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static cudaError_t get_encoder(EncodeTiledFn* fn) {
+    static EncodeTiledFn cached = nullptr;
+    if (!cached) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q);
+        if (e != cudaSuccess) return e;
+        if (q != cudaDriverEntryPointSuccess || !p) return cudaErrorSymbolNotFound;
+        cached = reinterpret_cast<EncodeTiledFn>(p);
+    }
+    *fn = cached;
+    return cudaSuccess;
+}
+
+// [rows][D] bf16 viewed as a 2D tensor; box = 16 rows x 64 columns, 128-byte swizzle.
+cudaError_t make_tma_map_bf16(CUtensorMap* m, const void* base, uint64_t rows, int D) {
+    EncodeTiledFn enc;
+    cudaError_t e = get_encoder(&enc);
+    if (e != cudaSuccess) return e;
+    cuuint64_t dims[2] = {cuuint64_t(D), cuuint64_t(rows)};
+    cuuint64_t strides[1] = {cuuint64_t(D) * 2};
+    cuuint32_t box[2] = {64, 16};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
 
 cudaError_t launch_linear_prefill_mma(const LinearArgs& a, cudaStream_t s, int* status) {
     if (!a.bf16 || (a.d != 64 && a.d != 128) || a.chunk % 16 != 0 || a.T % a.chunk != 0) return cudaErrorNotSupported;

@@ -136,7 +136,12 @@ ttt_status ttt_mlp_prefill(const void* Q, const void* K, const void* V, const fl
     CHECK_PTR(eta);
     CHECK_PTR(Z);
     ttt::MlpArgs a{Q, K, V, eta, W1_0, W2_0, Z, W1_out, W2_out, B, H, T, d, hidden, chunk, dtype == TTT_BF16 ? 1 : 0};
-    cudaError_t e = ttt::launch_mlp_prefill_generic(a, s);
+    int* status = nullptr;
+    cudaError_t e = status_ptr(&status);
+    if (e != cudaSuccess) return cuda_fail(e, "ttt_mlp_prefill status word");
+    // tensor-core kernel for bf16, d = 64, hidden = 256, chunk = 16, 16 | T; generic kernel otherwise
+    e = ttt::launch_mlp_prefill_tc(a, s, status);
+    if (e == cudaErrorNotSupported) e = ttt::launch_mlp_prefill_generic(a, s);
     if (e != cudaSuccess) return cuda_fail(e, "ttt_mlp_prefill launch");
     return TTT_OK;
 }

@@ -2,6 +2,7 @@
 // kernel translation units.  Not part of the public ABI (see include/ttt.h).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -54,6 +55,14 @@ size_t mlp_generic_smem_bytes(int d, int hidden, int chunk);
 // cudaErrorNotSupported when the shape is not covered, so the caller can use
 // the generic kernel instead.
 cudaError_t launch_linear_prefill_mma(const LinearArgs& a, cudaStream_t s, int* status);
+
+// Tensor-core (tcgen05) TTT-MLP prefill for bf16, d = 64, hidden = 256, chunk = 16.
+bool mlp_prefill_tc_supported(const MlpArgs& a);
+cudaError_t launch_mlp_prefill_tc(const MlpArgs& a, cudaStream_t s, int* status);
+
+// TMA descriptor of a [rows][D] bf16 row-major tensor: boxes of 16 rows x 64
+// columns with the 128-byte swizzle (D a multiple of 64).
+cudaError_t make_tma_map_bf16(CUtensorMap* m, const void* base, uint64_t rows, int D);
 
 // Bandwidth-bound single-token step.
 cudaError_t launch_linear_decode(const DecodeArgs& a, cudaStream_t s);

@@ -150,6 +150,41 @@ def test_mlp_small_shapes(dtype, d, T_, chunk):
     assert rel_err(W2, W2r) <= TOL[dtype]
 
 
+@pytest.mark.parametrize("T_,w_std,seed", [(16, 0.1, 1), (64, 0.02, 2), (400, 0.1, 3), (1024, 0.05, 4)])
+def test_mlp_tensor_core_shape(T_, w_std, seed):
+    # d = 64, hidden = 256, blocks of 16, bf16: the tcgen05 kernel
+    x = WL.mlp_inputs(2, 3, T_, 64, 256, seed=500 + seed, dtype="bf16", w_std=w_std)
+    Z, W1, W2 = run_mlp(x, 16)
+    r = f64(x)
+    Zr, W1r, W2r = O.mlp_dual(r["Q"], r["K"], r["V"], r["eta"], r["W1"], r["W2"], 16)
+    assert rel_err(Z, Zr) <= TOL["bf16"]
+    assert rel_err(W1, W1r) <= TOL["bf16"]
+    assert rel_err(W2, W2r) <= TOL["bf16"]
+
+
+def test_mlp_tensor_core_in_place_split_and_deterministic():
+    x = WL.mlp_inputs(1, 4, 128, 64, 256, seed=77, dtype="bf16", w_std=0.1)
+    g = cuda(x)
+    Z1, A1, B1 = T.mlp_prefill(g["Q"], g["K"], g["V"], g["eta"], g["W1"], g["W2"], 16)
+    Z2, A2, B2 = T.mlp_prefill(g["Q"], g["K"], g["V"], g["eta"], g["W1"], g["W2"], 16)
+    torch.cuda.synchronize()
+    assert torch.equal(Z1, Z2) and torch.equal(A1, A2) and torch.equal(B1, B2)
+    # two calls split at a block boundary, chained through the state, updated in place
+    W1, W2 = g["W1"].clone(), g["W2"].clone()
+    parts = []
+    for lo, hi in ((0, 48), (48, 128)):
+        sl = lambda t: t[:, :, lo:hi].contiguous()
+        Zp = torch.empty_like(sl(g["Q"]))
+        T.ttt_mlp_prefill(sl(g["Q"]), sl(g["K"]), sl(g["V"]), sl(g["eta"]), W1, W2, Zp, W1, W2, 16)
+        parts.append(Zp)
+    torch.cuda.synchronize()
+    r = f64(x)
+    Zr, W1r, W2r = O.mlp_dual(r["Q"], r["K"], r["V"], r["eta"], r["W1"], r["W2"], 16)
+    assert rel_err(torch.cat(parts, 2), Zr) <= TOL["bf16"]
+    assert rel_err(W1, W1r) <= TOL["bf16"] and rel_err(W2, W2r) <= TOL["bf16"]
+    assert rel_err(Z1, Zr) <= TOL["bf16"]
+
+
 def test_mlp_prefill_workload_sampled_heads():
     w = WL.WORKLOADS["mlp_prefill"]
     x = WL.workload_inputs(w)
