@@ -29,7 +29,8 @@
 //    W1 as soon as its update has landed (overlapping the Z half of the block),
 //    W2 after its last reader.
 //  * Eight compute warps: warp w reads TMEM lanes 32(w%4)..+31 of half w/4.
-//    Thread 0 issues the MMAs and commits them to one mbarrier; a ninth warp
+//    Lane 0 of warps 0..3 issue the MMAs (split four ways: one thread issues a
+//    tcgen05.mma only every ~85 cycles) and commit to one mbarrier; a ninth warp
 //    streams Q/K/V tiles by TMA and eta by a bulk copy into a 4-stage ring.
 //  * All waits are bounded; on expiry the kernel records TTT_ERR_TIMEOUT,
 //    leaves the loop on every thread at the next barrier, drains its copies
@@ -76,15 +77,16 @@ static_assert((NST - 1) * STAGE + 128 * 128 <= SMEM_BYTES, "score operand overru
 // tensor-memory columns
 constexpr uint32_t TM_W1T = 0;   // W1^T, half h at +64h (lane = hidden % 128, column = d)
 constexpr uint32_t TM_W2 = 128;  // W2,   half h at +64h
-constexpr uint32_t TM_ZK = 256;  // (K W1)^T, half h at +16h
-constexpr uint32_t TM_ZQ = 288;  // (Q W1)^T, then the layer-1 pre-activation of the read-out
+constexpr uint32_t TM_ZKQ = 256;  // half h at +32h: (K W1)^T in columns 0..15, (Q W1)^T in 16..31 (then the
+                                  // layer-1 pre-activation of the read-out)
 constexpr uint32_t TM_S1 = 320;  // rows 0..15: K Q^T
-constexpr uint32_t TM_P = 336;   // rows 0..63: (Hk W2)^T
-constexpr uint32_t TM_G = 352;   // (E2 W2^T)^T, half h at +16h
-constexpr uint32_t TM_ZO = 384;  // rows 0..63: Z^T; rows 64..79: Hk Hq^T
+constexpr uint32_t TM_P = 336;   // rows 0..63: (Hk W2)^T as four partial sums at +16j
+constexpr uint32_t TM_G = 400;   // (E2 W2^T)^T, half h at +16h
+constexpr uint32_t TM_ZO = 432;  // rows 0..63: Z^T; rows 64..79: Hk Hq^T; four partial sums at +16j
 constexpr uint32_t TM_COLS = 512;
 
 constexpr uint32_t ID_KK16 = tc::make_idesc(128, 16, 0, 0);         // A, B K-major
+constexpr uint32_t ID_KK32 = tc::make_idesc(128, 32, 0, 0);         // A, B K-major, N = 32
 constexpr uint32_t ID_MK16 = tc::make_idesc(128, 16, 1, 0);         // A MN-major, B K-major
 constexpr uint32_t ID_MM64N = tc::make_idesc(128, 64, 1, 1, 0, 1);  // both MN-major, -B
 constexpr uint32_t ID_MM16N = tc::make_idesc(128, 16, 1, 1, 0, 1);  // both MN-major, -B
@@ -169,7 +171,7 @@ mlp_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_cons
             mbar_init(smem_u32(&full_bar[s]), 1);
             mbar_init(smem_u32(&empty_bar[s]), 1);
         }
-        mbar_init(smem_u32(&mma_bar), 1);
+        mbar_init(smem_u32(&mma_bar), 4);  // one commit per MMA issuer
         s_err = 0;
         s_zero = 0;
         fence_mbar_init();
@@ -282,6 +284,26 @@ mlp_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_cons
         };
 
         const uint32_t w2s = sb + OFF_W2S, w1t = sb + OFF_W1T;
+        // Four MMA issuers (lane 0 of warps 0..3, one per SM sub-partition): one thread
+        // issues a tcgen05.mma only every ~85 cycles, so each stage's products are split
+        // over four threads, with the long contractions (K = 256) cut into four partial
+        // accumulators that the epilogue adds in a fixed order (deterministic).
+        const bool issuer = lane == 0 && warp < 4;
+        const int r = warp;  // issuer index
+
+        // per-thread 16-byte chunk offsets of the swizzled layout for this thread's column
+        // (hidden unit hc of a 64-wide block): element (row, hc) lives at row*128 + xo[row & 7]
+        uint32_t xo[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) xo[i] = uint32_t((((hc >> 3) ^ i) << 4) + ((hc & 7) << 1));
+        // the head-dimension column of the epilogues over d (warps 0,1 of either half)
+        const int dd = 32 * (q & 1) + lane;
+        uint32_t xd[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) xd[i] = uint32_t((((dd >> 3) ^ i) << 4) + ((dd & 7) << 1));
+        const bool dwarp = q < 2;  // warps 0, 1, 4, 5 read TMEM lanes 0..63 (the head dimension)
+        const int t0 = 8 * h;      // ...and split the 16 token columns between the halves
+
         for (int n = 0; n < nblk; ++n) {
             const int s = n % NST;
             const uint32_t st = sb + OFF_RING + s * STAGE;
@@ -294,110 +316,125 @@ mlp_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_cons
                 et[i] = f.x; et[i + 1] = f.y; et[i + 2] = f.z; et[i + 3] = f.w;
             }
 
-            // ---- S1: (K W1)^T, (Q W1)^T, K Q^T
-            if (tid == 0 && !err) {
+            // ---- S1: (K W1)^T | (Q W1)^T per half (the K and Q tiles are adjacent: N = 32), K Q^T
+            if (issuer && !err) {
                 tc::fence_after_sync();
+                if (r < 2) {
 #pragma unroll
-                for (int hh = 0; hh < 2; ++hh)
+                    for (int ks = 0; ks < 4; ++ks)
+                        tc::mma(tm + TM_ZKQ + 32 * r, sw_desc(w1t + r * 128 * 128 + ks * 32, 16),
+                                sw_desc(st + ks * 32, 16), ID_KK32, ks > 0);
+                } else if (r == 2) {
 #pragma unroll
-                    for (int ks = 0; ks < 4; ++ks) {
-                        const uint64_t a = sw_desc(w1t + hh * 128 * 128 + ks * 32, 16);
-                        tc::mma(tm + TM_ZK + 16 * hh, a, sw_desc(st + ks * 32, 16), ID_KK16, ks > 0);
-                        tc::mma(tm + TM_ZQ + 16 * hh, a, sw_desc(st + TILE + ks * 32, 16), ID_KK16, ks > 0);
-                    }
-#pragma unroll
-                for (int ks = 0; ks < 4; ++ks)
-                    tc::mma(tm + TM_S1, sw_desc(st + ks * 32, 16), sw_desc(st + TILE + ks * 32, 16), ID_KK16, ks > 0);
+                    for (int ks = 0; ks < 4; ++ks)
+                        tc::mma(tm + TM_S1, sw_desc(st + ks * 32, 16), sw_desc(st + TILE + ks * 32, 16), ID_KK16,
+                                ks > 0);
+                }
                 tc::commit(smem_u32(&mma_bar));
             }
+            __syncwarp();
             float gp[16];
             if (wait_mma()) {
                 float zk[16], s1[16];
-                tc::ld16(tl + TM_ZK + 16 * h, zk);
+                tc::ld16(tl + TM_ZKQ + 32 * h, zk);
                 if (warp == 0) tc::ld16(tl + TM_S1, s1);
                 tc::ld_wait();
+                uint8_t* hk = smem + OFF_W2S + hb * W2S_BLK + 64 * 128;
 #pragma unroll
-                for (int t = 0; t < 16; ++t) {
-                    const float hk = gelu_and_prime(zk[t], gp[t]);
-                    st_bf16(smem + OFF_W2S + hb * W2S_BLK + tc::sw128(64 + t, hc), hk);
-                }
+                for (int t = 0; t < 16; ++t) st_bf16(hk + t * 128 + xo[t & 7], gelu_and_prime(zk[t], gp[t]));
                 if (warp == 0 && lane < 16) {
-                    float r[16];
+                    float rr[16];
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) r[i] = i >= lane ? s1[i] : 0.f;
-                    st_core_row(smem + OFF_B1, lane, r);
+                    for (int i = 0; i < 16; ++i) rr[i] = i >= lane ? s1[i] : 0.f;
+                    st_core_row(smem + OFF_B1, lane, rr);
                 }
             }
             if (end_stage()) break;
 
-            // ---- S2: (Hk W2)^T
-            if (tid == 0) {
+            // ---- S2: (Hk W2)^T, K = 256 split into four partial accumulators
+            if (issuer) {
                 tc::fence_after_sync();
 #pragma unroll
-                for (int ks = 0; ks < 16; ++ks) {
-                    const uint32_t o = (ks >> 2) * W2S_BLK + (ks & 3) * 32;
-                    tc::mma(tm + TM_P, sw_desc(w2s + o, 16), sw_desc(w2s + o + 64 * 128, 16), ID_KK16, ks > 0);
+                for (int kk = 0; kk < 4; ++kk) {
+                    const uint32_t o = r * W2S_BLK + kk * 32;
+                    tc::mma(tm + TM_P + 16 * r, sw_desc(w2s + o, 16), sw_desc(w2s + o + 64 * 128, 16), ID_KK16, kk > 0);
                 }
                 tc::commit(smem_u32(&mma_bar));
             }
-            if (wait_mma() && warp < 2) {
-                const int dd = 32 * q + lane;
-                float p[16];
-                tc::ld16(tl + TM_P, p);
-                tc::ld_wait();
+            __syncwarp();
+            if (wait_mma() && dwarp) {
+                float p[8], pp[8];
+                tc::ld8(tl + TM_P + t0, p);
 #pragma unroll
-                for (int t = 0; t < 16; ++t) {
-                    const float v = __bfloat162float(
-                        *reinterpret_cast<const __nv_bfloat16*>(stp + 2 * TILE + tc::sw128(t, dd)));
-                    const float e = p[t] - v;
-                    st_bf16(smem + OFF_E2 + tc::sw128(t, dd), e);
-                    st_bf16(smem + OFF_E2P + tc::sw128(t, dd), et[t] * e);
+                for (int j = 1; j < 4; ++j) {
+                    tc::ld8(tl + TM_P + 16 * j + t0, pp);
+                    tc::ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) p[i] += pp[i];
+                }
+                float v[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    v[i] = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(stp + 2 * TILE + (t0 + i) * 128 +
+                                                                                    xd[(t0 + i) & 7]));
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int t = t0 + i;
+                    const float e = p[i] - v[i];
+                    st_bf16(smem + OFF_E2 + t * 128 + xd[t & 7], e);
+                    st_bf16(smem + OFF_E2P + t * 128 + xd[t & 7], et[t] * e);
                 }
             }
             if (end_stage()) break;
 
-            // ---- S3: (E2 W2^T)^T and the W2 update  W2 += Hk^T (-eta.E2)
-            if (tid == 0) {
+            // ---- S3: (E2 W2^T)^T per half (issuers 0, 1) and the W2 update W2 += Hk^T (-eta.E2) (issuers 2, 3)
+            if (issuer) {
                 tc::fence_after_sync();
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
+                if (r < 2) {
 #pragma unroll
                     for (int ks = 0; ks < 4; ++ks)
-                        tc::mma(tm + TM_G + 16 * hh, sw_desc(w2s + 2 * hh * W2S_BLK + ks * 2048, W2S_BLK),
+                        tc::mma(tm + TM_G + 16 * r, sw_desc(w2s + 2 * r * W2S_BLK + ks * 2048, W2S_BLK),
                                 sw_desc(sb + OFF_E2 + ks * 32, 16), ID_MK16, ks > 0);
+                } else {
+                    const int hh = r - 2;
                     tc::mma(tm + TM_W2 + 64 * hh, sw_desc(w2s + 2 * hh * W2S_BLK + 64 * 128, W2S_BLK),
                             sw_desc(sb + OFF_E2P, TILE), ID_MM64N, 1);
                 }
                 tc::commit(smem_u32(&mma_bar));
             }
+            __syncwarp();
             if (wait_mma()) {
                 float g[16];
                 tc::ld16(tl + TM_G + 16 * h, g);
                 tc::ld_wait();
+                uint8_t* e1 = smem + OFF_E1P + hb * TILE;
 #pragma unroll
-                for (int t = 0; t < 16; ++t)
-                    st_bf16(smem + OFF_E1P + hb * TILE + tc::sw128(t, hc), et[t] * g[t] * gp[t]);
+                for (int t = 0; t < 16; ++t) st_bf16(e1 + t * 128 + xo[t & 7], et[t] * g[t] * gp[t]);
             }
             if (end_stage()) break;
 
-            // ---- S4: read-out layer 1 with the causal delta, and the W1 update  W1^T += (eta.E1)^T (-K)
-            if (tid == 0) {
+            // ---- S4: read-out layer 1 with the causal delta (issuers 0, 1) and the W1 update
+            //      W1^T += (eta.E1)^T (-K) (issuers 2, 3)
+            if (issuer) {
                 tc::fence_after_sync();
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    const uint64_t a = sw_desc(sb + OFF_E1P + 2 * hh * TILE, TILE);
-                    tc::mma(tm + TM_ZQ + 16 * hh, a, core16_desc(sb + OFF_B1), ID_MM16N, 1);
+                const int hh = r & 1;
+                const uint64_t a = sw_desc(sb + OFF_E1P + 2 * hh * TILE, TILE);
+                if (r < 2)
+                    tc::mma(tm + TM_ZKQ + 32 * hh + 16, a, core16_desc(sb + OFF_B1), ID_MM16N, 1);
+                else
                     tc::mma(tm + TM_W1T + 64 * hh, a, sw_desc(st, TILE), ID_MM64N, 1);
-                }
                 tc::commit(smem_u32(&mma_bar));
             }
+            __syncwarp();
             if (wait_mma()) {
                 float zq[16];
-                tc::ld16(tl + TM_ZQ + 16 * h, zq);
+                tc::ld16(tl + TM_ZKQ + 32 * h + 16, zq);
                 tc::ld_wait();
+                uint8_t* hq = smem + OFF_HQ + hb * TILE;
 #pragma unroll
-                for (int t = 0; t < 16; ++t) st_bf16(smem + OFF_HQ + hb * TILE + tc::sw128(t, hc), gelu(zq[t]));
-                // the W1 update has landed: refresh its bf16 copy for the next block
+                for (int t = 0; t < 16; ++t) st_bf16(hq + t * 128 + xo[t & 7], gelu(zq[t]));
+                // the W1 update has landed: refresh its bf16 copy (row hid) for the next block
+                uint8_t* w1row = smem + OFF_W1T + hid * 128;
 #pragma unroll
                 for (int c0 = 0; c0 < D; c0 += 16) {
                     float w[16];
@@ -408,62 +445,73 @@ mlp_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_cons
                     a.z = pack_bf16(w[4], w[5]); a.w = pack_bf16(w[6], w[7]);
                     b.x = pack_bf16(w[8], w[9]); b.y = pack_bf16(w[10], w[11]);
                     b.z = pack_bf16(w[12], w[13]); b.w = pack_bf16(w[14], w[15]);
-                    *reinterpret_cast<uint4*>(smem + OFF_W1T + tc::sw128(hid, c0)) = a;
-                    *reinterpret_cast<uint4*>(smem + OFF_W1T + tc::sw128(hid, c0 + 8)) = b;
+                    *reinterpret_cast<uint4*>(w1row + ((((c0 >> 3) ^ hid) & 7) << 4)) = a;
+                    *reinterpret_cast<uint4*>(w1row + (((((c0 >> 3) + 1) ^ hid) & 7) << 4)) = b;
                 }
             }
             if (end_stage()) break;
 
-            // ---- S5: (Hq W2)^T in rows 0..63, Hk Hq^T in rows 64..79
-            if (tid == 0) {
+            // ---- S5: (Hq W2)^T in rows 0..63 and Hk Hq^T in rows 64..79, K = 256 in four partials
+            if (issuer) {
                 tc::fence_after_sync();
 #pragma unroll
-                for (int ks = 0; ks < 16; ++ks) {
-                    const uint32_t o = (ks >> 2) * W2S_BLK + (ks & 3) * 32;
-                    tc::mma(tm + TM_ZO, sw_desc(w2s + o, 16), sw_desc(sb + OFF_HQ + (ks >> 2) * TILE + (ks & 3) * 32, 16),
-                            ID_KK16, ks > 0);
-                }
+                for (int kk = 0; kk < 4; ++kk)
+                    tc::mma(tm + TM_ZO + 16 * r, sw_desc(w2s + r * W2S_BLK + kk * 32, 16),
+                            sw_desc(sb + OFF_HQ + r * TILE + kk * 32, 16), ID_KK16, kk > 0);
                 tc::commit(smem_u32(&mma_bar));
             }
+            __syncwarp();
             if (wait_mma()) {
                 if (warp == 2) {
-                    float s2[16];
+                    float s2[16], sp[16];
                     tc::ld16(tl + TM_ZO, s2);
-                    tc::ld_wait();
-                    if (lane < 16) {
-                        float r[16];
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) r[i] = i >= lane ? s2[i] : 0.f;
-                        st_core_row(smem + OFF_B2, lane, r);
+                    for (int j = 1; j < 4; ++j) {
+                        tc::ld16(tl + TM_ZO + 16 * j, sp);
+                        tc::ld_wait();
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) s2[i] += sp[i];
+                    }
+                    if (lane < 16) {
+                        float rr[16];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) rr[i] = i >= lane ? s2[i] : 0.f;
+                        st_core_row(smem + OFF_B2, lane, rr);
                     }
                 }
-                // W2's last reader of this block has finished: refresh its bf16 copy
+                // W2's last reader of this block has finished: refresh its bf16 copy (column hc of W2^T)
+                uint8_t* w2c = smem + OFF_W2S + hb * W2S_BLK;
 #pragma unroll
                 for (int c0 = 0; c0 < D; c0 += 16) {
                     float w[16];
                     tc::ld16(tl + TM_W2 + 64 * h + c0, w);
                     tc::ld_wait();
 #pragma unroll
-                    for (int i = 0; i < 16; ++i)
-                        st_bf16(smem + OFF_W2S + hb * W2S_BLK + tc::sw128(c0 + i, hc), w[i]);
+                    for (int i = 0; i < 16; ++i) st_bf16(w2c + (c0 + i) * 128 + xo[i & 7], w[i]);
                 }
             }
             if (end_stage()) break;
 
-            // ---- S6: Z^T += (eta.E2)^T (-tril(Hq Hk^T)^T)
-            if (tid == 0) {
+            // ---- S6: Z^T += (eta.E2)^T (-tril(Hq Hk^T)^T), into partial 0
+            if (issuer) {
                 tc::fence_after_sync();
-                tc::mma(tm + TM_ZO, sw_desc(sb + OFF_E2P, TILE), core16_desc(sb + OFF_B2), ID_MM16N, 1);
+                if (r == 0) tc::mma(tm + TM_ZO, sw_desc(sb + OFF_E2P, TILE), core16_desc(sb + OFF_B2), ID_MM16N, 1);
                 tc::commit(smem_u32(&mma_bar));
             }
-            if (wait_mma() && warp < 2) {
-                const int dd = 32 * q + lane;
-                float z[16];
-                tc::ld16(tl + TM_ZO, z);
-                tc::ld_wait();
-                __nv_bfloat16* zp = Z + (bh * T + size_t(BT) * n) * D + dd;
+            __syncwarp();
+            if (wait_mma() && dwarp) {
+                float z[8], zp[8];
+                tc::ld8(tl + TM_ZO + t0, z);
 #pragma unroll
-                for (int t = 0; t < 16; ++t) zp[t * D] = __float2bfloat16_rn(z[t]);
+                for (int j = 1; j < 4; ++j) {
+                    tc::ld8(tl + TM_ZO + 16 * j + t0, zp);
+                    tc::ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) z[i] += zp[i];
+                }
+                __nv_bfloat16* zo = Z + (bh * T + size_t(BT) * n + t0) * D + dd;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) zo[i * D] = __float2bfloat16_rn(z[i]);
             }
             const bool stop = end_stage();
             if (tid == 0) mbar_arrive(smem_u32(&empty_bar[s]));
@@ -471,10 +519,10 @@ mlp_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_cons
         }
 
         // every MMA this CTA issued has completed before the state is read and TMEM freed
-        if (tid == 0) {
+        if (issuer) {
             tc::commit(smem_u32(&mma_bar));
-            mbar_wait_bounded(smem_u32(&mma_bar), mph, &s_zero, kWaitLimitNs);
         }
+        if (tid == 0) mbar_wait_bounded(smem_u32(&mma_bar), mph, &s_zero, kWaitLimitNs);
         bar_compute();
         tc::fence_after_sync();
 
