@@ -11,7 +11,8 @@ The JSON line printed by rank 0 carries the headline value (tokens/s over all
 ranks), its roofline fraction, the clocks seen during the timed region, the
 end-to-end number through the public API with host buffers, the oracle's CPU
 baseline, and under "rows" the other workloads (TTT-MLP prefill, the
-long-context chunk sweep and the decode step), each timed the same way.
+long-context chunk sweep, the TTT-Linear and TTT-MLP decode steps), each timed
+the same way.
 
 --impl reference times the fp64 CPU oracle (test infrastructure) on the host
 cores on a bounded sample of the same workload.
@@ -332,6 +333,39 @@ def bench_decode(T_mod, w, steps, warmup, world, peaks, graph_steps=1024, nrot=N
             "frac": t_roof / (per_step * 1e-3), "bound": "hbm", "state_copies": nrot}
 
 
+def mlp_decode_bytes(B, H, d, hd, elt=2):
+    """Per step: W1 and W2 read + written once, q,k,v read, z written, eta read."""
+    return 2 * 2 * B * H * d * hd * 4 + 4 * B * H * d * elt + 4 * B * H
+
+
+def bench_mlp_decode(T_mod, w, steps, warmup, world, peaks, graph_steps=256, nrot=2):
+    """A CUDA graph of `graph_steps` TTT-MLP decode steps; `nrot` state copies rotate (2 x 100.7 MB > L2)."""
+    x = WL.mlp_decode_inputs(w.B, w.H, w.d, w.hidden, graph_steps, w.seed)
+    q, k, v, e = (x[n].cuda() for n in ("q", "k", "v", "eta"))
+    states = [(x["W1"].cuda(), x["W2"].cuda()) for _ in range(nrot)]
+    z = torch.empty_like(q)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        for i in range(2):
+            W1, W2 = states[i % nrot]
+            T_mod.ttt_mlp_decode_step(q[i], k[i], v[i], e[i], W1, W2, z[i])
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for i in range(graph_steps):
+            W1, W2 = states[i % nrot]
+            T_mod.ttt_mlp_decode_step(q[i], k[i], v[i], e[i], W1, W2, z[i])
+    ms, ms_launch = timed_loop(lambda i: g.replay(), steps, warmup, world)
+    per_step = ms_launch / graph_steps
+    nbytes = mlp_decode_bytes(w.B, w.H, w.d, w.hidden)
+    t_roof = nbytes / (peaks["hbm_gbs"] * 1e9)
+    return {"tokens_per_s": w.B / (per_step * 1e-3), "us_per_step": per_step * 1e3, "graph_steps": graph_steps,
+            "bytes_per_step": nbytes, "achieved_gbs": nbytes / (per_step * 1e-3) / 1e9,
+            "roofline_us": t_roof * 1e6, "frac": t_roof / (per_step * 1e-3), "bound": "hbm", "state_copies": nrot}
+
+
 def bench_e2e(T_mod, w, steps, warmup, world):
     """Public API with pinned host buffers: H2D of the inputs, the prefill, D2H of Z and W, every step."""
     x = WL.workload_inputs(w)
@@ -422,6 +456,9 @@ def run_ours(args):
         if want("decode"):
             wd = WL.WORKLOADS["decode"]
             rows["decode"] = bench_decode(T_mod, wd, max(3, rsteps // 5), args.warmup, world, peaks)
+        if want("mlp_decode"):
+            wd = WL.WORKLOADS["mlp_decode"]
+            rows["mlp_decode"] = bench_mlp_decode(T_mod, wd, max(3, rsteps // 5), args.warmup, world, peaks)
         line["rows"] = rows
     if rank == 0 and world == 1 and not args.no_cpu:
         line["cpu_baseline"] = cpu_baseline(w)
@@ -473,7 +510,8 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--rows", choices=["all", "none", "mlp_prefill", "long_context", "decode"], default="all",
+    ap.add_argument("--rows", choices=["all", "none", "mlp_prefill", "long_context", "decode", "mlp_decode"],
+                    default="all",
                     help="workload rows timed after the headline (default: all)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")

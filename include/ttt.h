@@ -105,7 +105,7 @@ ttt_status ttt_linear_prefill(const void* Q, const void* K, const void* V, const
  *   W1_0, W1_out  [B][H][d][hidden]  fp32  (W1_out may equal W1_0)
  *   W2_0, W2_out  [B][H][hidden][d]  fp32  (W2_out may equal W2_0)
  *   d in {16, 32, 64}; hidden a multiple of 16 with d*hidden <= 16384;
- *   chunk 1..512 with chunk*hidden <= 8192 (last block may be shorter).
+ *   chunk 1..64 with chunk*hidden <= 4096 (last block may be shorter).
  *
  * Source: "Test-Time Training (TTT) Layers for Sequence Modeling", section
  * "Variants: TTT-Linear vs. TTT-MLP" (two-layer MLP inner model); loss, step
@@ -134,6 +134,30 @@ ttt_status ttt_mlp_prefill(const void* Q, const void* K, const void* V, const fl
 ttt_status ttt_linear_decode_step(const void* q, const void* k, const void* v, const float* eta,
                                   float* W, void* z, int B, int H, int d, ttt_dtype dtype,
                                   void* stream);
+
+/*
+ * TTT-MLP decode: one online step (a block of one token) for every
+ * (batch, head), updating W1 and W2 in place; the output is read through the
+ * updated weights:
+ *
+ *   u = k W1, a = GELU(u), e2 = a W2 - v, e1 = (e2 W2^T) . GELU'(u)
+ *   W1 <- W1 - eta k^T e1,   W2 <- W2 - eta a^T e2
+ *   z  = GELU(q W1) W2        (new W1, W2)
+ *
+ *   q, k, v, z  [B][H][d]         dtype
+ *   eta         [B][H]            fp32
+ *   W1          [B][H][d][hidden] fp32, read and written in place
+ *   W2          [B][H][hidden][d] fp32, read and written in place
+ *   d in {16, 32, 64}; hidden in {64, 128, 256} (else TTT_ERR_UNSUPPORTED)
+ *
+ * Source: "Test-Time Training (TTT) Layers for Sequence Modeling", section
+ * "Variants: TTT-Linear vs. TTT-MLP" (two-layer MLP inner model);
+ * "Test-Time Training Layers ...", section "The Core Mechanism" (loss, step,
+ * read-out after the step).  The same step as ttt_mlp_prefill with chunk 1.
+ */
+ttt_status ttt_mlp_decode_step(const void* q, const void* k, const void* v, const float* eta, float* W1,
+                               float* W2, void* z, int B, int H, int d, int hidden, ttt_dtype dtype,
+                               void* stream);
 
 /*
  * Reads and clears the device status word for the current device.

@@ -148,6 +148,14 @@ def linear_decode(q, k, v, eta, W):
     return z, Wn
 
 
+def mlp_decode(q, k, v, eta, W1, W2):
+    """One online TTT-MLP step for every (batch, head): the token-level scan on a
+    single token (block of one).  q,k,v [B,H,d], eta [B,H]; returns (z, W1_new, W2_new)."""
+    q, k, v, eta = (_f64(a) for a in (q, k, v, eta))
+    Z, A, Bm = mlp_primal(q[:, :, None], k[:, :, None], v[:, :, None], eta[:, :, None], W1, W2, 1)
+    return Z[:, :, 0], A, Bm
+
+
 def mlp_token_grad(k, v, W1, W2):
     """Loss and chain-rule pieces (a, e1, e2) of 1/2||GELU(kW1)W2 - v||^2 for one token.
 

@@ -167,6 +167,30 @@ ttt_status ttt_linear_decode_step(const void* q, const void* k, const void* v, c
     return TTT_OK;
 }
 
+ttt_status ttt_mlp_decode_step(const void* q, const void* k, const void* v, const float* eta, float* W1, float* W2,
+                               void* z, int B, int H, int d, int hidden, ttt_dtype dtype, void* stream) {
+    g_last_error[0] = 0;
+    if (B < 0 || H < 0) return fail(TTT_ERR_INVALID_ARG, "negative size%s");
+    if (dtype != TTT_F32 && dtype != TTT_BF16) return fail(TTT_ERR_INVALID_ARG, "unknown dtype%s");
+    if (d <= 0 || hidden <= 0) return fail(TTT_ERR_INVALID_ARG, "dimensions must be positive%s");
+    if (!(d == 16 || d == 32 || d == 64)) return fail(TTT_ERR_UNSUPPORTED, "MLP head dim must be 16, 32 or 64%s");
+    if (!(hidden == 64 || hidden == 128 || hidden == 256))
+        return fail(TTT_ERR_UNSUPPORTED, "MLP decode hidden must be 64, 128 or 256%s");
+    if (size_t(B) * H == 0) return TTT_OK;
+    if (size_t(B) * H > 0x7fffffffu) return fail(TTT_ERR_UNSUPPORTED, "B*H too large%s");
+    CHECK_PTR(q);
+    CHECK_PTR(k);
+    CHECK_PTR(v);
+    CHECK_PTR(eta);
+    CHECK_PTR(W1);
+    CHECK_PTR(W2);
+    CHECK_PTR(z);
+    ttt::MlpDecodeArgs a{q, k, v, eta, W1, W2, z, B, H, d, hidden, dtype == TTT_BF16 ? 1 : 0};
+    cudaError_t e = ttt::launch_mlp_decode(a, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "ttt_mlp_decode_step launch");
+    return TTT_OK;
+}
+
 ttt_status ttt_get_device_status(void* stream) {
     int* p = nullptr;
     cudaError_t e = status_ptr(&p);
@@ -195,6 +219,6 @@ const char* ttt_status_string(ttt_status s) {
 
 const char* ttt_last_error(void) { return g_last_error; }
 
-int ttt_version(void) { return 100; }
+int ttt_version(void) { return 10100; }
 
 }  // extern "C"

@@ -46,6 +46,18 @@ struct DecodeArgs {
     int bf16;
 };
 
+struct MlpDecodeArgs {
+    const void* q;
+    const void* k;
+    const void* v;
+    const float* eta;
+    float* W1;
+    float* W2;
+    void* z;
+    int B, H, d, hidden;
+    int bf16;
+};
+
 // Generic SIMT kernels: every supported shape, fp32 accumulation.
 cudaError_t launch_linear_prefill_generic(const LinearArgs& a, cudaStream_t s);
 cudaError_t launch_mlp_prefill_generic(const MlpArgs& a, cudaStream_t s);
@@ -64,7 +76,8 @@ cudaError_t launch_mlp_prefill_tc(const MlpArgs& a, cudaStream_t s, int* status)
 // columns with the 128-byte swizzle (D a multiple of 64).
 cudaError_t make_tma_map_bf16(CUtensorMap* m, const void* base, uint64_t rows, int D);
 
-// Bandwidth-bound single-token step.
+// Bandwidth-bound single-token steps.
 cudaError_t launch_linear_decode(const DecodeArgs& a, cudaStream_t s);
+cudaError_t launch_mlp_decode(const MlpDecodeArgs& a, cudaStream_t s);
 
 }  // namespace ttt

@@ -25,8 +25,8 @@ LIB_PATH = os.path.join(_PKG, "libttt.so")
 TTT_OK, TTT_ERR_INVALID_ARG, TTT_ERR_UNSUPPORTED, TTT_ERR_CUDA, TTT_ERR_TIMEOUT = range(5)
 TTT_F32, TTT_BF16 = 0, 1
 
-EXPORTED = ("ttt_linear_prefill", "ttt_mlp_prefill", "ttt_linear_decode_step", "ttt_get_device_status",
-            "ttt_status_string", "ttt_last_error", "ttt_version")
+EXPORTED = ("ttt_linear_prefill", "ttt_mlp_prefill", "ttt_linear_decode_step", "ttt_mlp_decode_step",
+            "ttt_get_device_status", "ttt_status_string", "ttt_last_error", "ttt_version")
 
 
 class TTTError(RuntimeError):
@@ -53,9 +53,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
             lib.ttt_linear_prefill.argtypes = [vp, vp, vp, fp, fp, vp, fp, i, i, i, i, i, i, vp]
             lib.ttt_mlp_prefill.argtypes = [vp, vp, vp, fp, fp, fp, vp, fp, fp, i, i, i, i, i, i, i, vp]
             lib.ttt_linear_decode_step.argtypes = [vp, vp, vp, fp, fp, vp, i, i, i, i, vp]
+            lib.ttt_mlp_decode_step.argtypes = [vp, vp, vp, fp, fp, fp, vp, i, i, i, i, i, vp]
             lib.ttt_get_device_status.argtypes = [vp]
             for f in (lib.ttt_linear_prefill, lib.ttt_mlp_prefill, lib.ttt_linear_decode_step,
-                      lib.ttt_get_device_status):
+                      lib.ttt_mlp_decode_step, lib.ttt_get_device_status):
                 f.restype = i
             lib.ttt_status_string.argtypes = [i]
             lib.ttt_status_string.restype = ctypes.c_char_p
@@ -152,6 +153,22 @@ def ttt_linear_decode_step(q, k, v, eta, W, z, stream=None) -> None:
     _check(st)
 
 
+def ttt_mlp_decode_step(q, k, v, eta, W1, W2, z, stream=None) -> None:
+    """One online TTT-MLP step; W1 [B,H,d,hidden] and W2 [B,H,hidden,d] (fp32) updated in place, z written."""
+    B, H, d = q.shape
+    hidden = W1.shape[-1]
+    dt = _io_dtype(q)
+    for name, t in (("k", k), ("v", v), ("z", z)):
+        if t.shape != q.shape or t.dtype != q.dtype:
+            raise ValueError(f"{name} must match q in shape and dtype")
+    if eta.shape != (B, H) or W1.shape != (B, H, d, hidden) or W2.shape != (B, H, hidden, d):
+        raise ValueError("eta must be [B,H], W1 [B,H,d,hidden] and W2 [B,H,hidden,d]")
+    st = load_library().ttt_mlp_decode_step(
+        _ptr(q, "q"), _ptr(k, "k"), _ptr(v, "v"), _ptr(eta, "eta", torch.float32), _ptr(W1, "W1", torch.float32),
+        _ptr(W2, "W2", torch.float32), _ptr(z, "z"), B, H, d, hidden, dt, _stream(stream))
+    _check(st)
+
+
 def ttt_get_device_status(stream=None) -> int:
     """Reads and clears the device status word (synchronises the stream); returns the status code."""
     return load_library().ttt_get_device_status(_stream(stream))
@@ -174,6 +191,13 @@ def mlp_prefill(Q, K, V, eta, W1, W2, chunk: int, stream=None):
     W2o = torch.empty_like(W2)
     ttt_mlp_prefill(Q, K, V, eta, W1, W2, Z, W1o, W2o, chunk, stream)
     return Z, W1o, W2o
+
+
+def mlp_decode_step(q, k, v, eta, W1, W2, stream=None):
+    """Returns z; W1 and W2 are updated in place."""
+    z = torch.empty_like(q)
+    ttt_mlp_decode_step(q, k, v, eta, W1, W2, z, stream)
+    return z
 
 
 def linear_decode_step(q, k, v, eta, W, stream=None):

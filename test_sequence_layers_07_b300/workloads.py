@@ -22,11 +22,12 @@ float32 -> bfloat16 (round to nearest even, done by torch on the CPU).  eta and
 the weights are always fp32.  The oracle reads exactly these rounded values,
 widened to float64.
 
-The five named workloads are those the library is measured and checked on:
+The named workloads are those the library is measured and checked on:
 ``oracle_check`` (d=16, fp32), ``linear_prefill`` (B=8, H=12, d=64, T=2048,
 b=16, bf16), ``mlp_prefill`` (same tokens, hidden 256), ``long_context``
-(B=1, H=16, d=128, T=32768, b in {16, 64, 512}) and ``decode`` (B=256, H=12,
-d=64, 1024 single-token steps, per-sequence initial state).
+(B=1, H=16, d=128, T=32768, b in {16, 64, 512}), ``decode`` (B=256, H=12,
+d=64, 1024 single-token steps, per-sequence initial state) and ``mlp_decode``
+(B=64, H=12, d=64, hidden 256, 256 single-token steps).
 """
 from __future__ import annotations
 
@@ -68,6 +69,8 @@ WORKLOADS = {
                              chunks=(16, 64, 512)),
     # decode: T is the number of successive single-token steps
     "decode": Workload("decode", B=256, H=12, T=1024, d=64, chunk=1, dtype="bf16", seed=1005),
+    # TTT-MLP decode: 768 heads x 128 KB of fp32 state (the same 100.7 MB of state as the Linear decode)
+    "mlp_decode": Workload("mlp_decode", B=64, H=12, T=256, d=64, chunk=1, dtype="bf16", seed=1006, hidden=256),
 }
 
 
@@ -147,6 +150,24 @@ def decode_inputs(B, H, d, steps, seed, dtype="bf16", w_std=0.02, block=64):
         q, k, v, e = draw_qkv_eta(rng, (n, B, H), d, dtype)
         qs.append(q); ks.append(k); vs.append(v); es.append(e)
     return {"W": W, "q": torch.cat(qs), "k": torch.cat(ks), "v": torch.cat(vs), "eta": torch.cat(es)}
+
+
+def mlp_decode_inputs(B, H, d, hidden, steps, seed, dtype="bf16", w_std=0.02, block=64):
+    """Inputs of `steps` successive TTT-MLP decode steps.
+
+    W1 [B, H, d, hidden] then W2 [B, H, hidden, d] fp32 (one draw per sequence
+    and head), then the steps in blocks of `block` (Q, K, V, u per block):
+    q, k, v [steps, B, H, d] in `dtype`, eta [steps, B, H].
+    """
+    rng = np.random.default_rng(seed)
+    W1 = round_to(rng.standard_normal((B, H, d, hidden)) * w_std, "f32")
+    W2 = round_to(rng.standard_normal((B, H, hidden, d)) * w_std, "f32")
+    qs, ks, vs, es = [], [], [], []
+    for s0 in range(0, steps, block):
+        n = min(block, steps - s0)
+        q, k, v, e = draw_qkv_eta(rng, (n, B, H), d, dtype)
+        qs.append(q); ks.append(k); vs.append(v); es.append(e)
+    return {"W1": W1, "W2": W2, "q": torch.cat(qs), "k": torch.cat(ks), "v": torch.cat(vs), "eta": torch.cat(es)}
 
 
 def workload_inputs(w: Workload, chunk: int | None = None, seed_offset: int = 0):

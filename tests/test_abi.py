@@ -121,6 +121,23 @@ def test_decode_validation(lib):
     assert dp(B_=0, W=NULL) == T.TTT_OK
 
 
+def test_mlp_decode_validation(lib):
+    def md(**kw):
+        a = dict(q=A, k=A, v=A, eta=A, W1=A, W2=A, z=A, B_=2, H=3, d=64, hd=256, dt=1)
+        a.update(kw)
+        return lib.ttt_mlp_decode_step(a["q"], a["k"], a["v"], a["eta"], a["W1"], a["W2"], a["z"], a["B_"], a["H"],
+                                       a["d"], a["hd"], a["dt"], None)
+    assert md(W2=NULL) == T.TTT_ERR_INVALID_ARG
+    assert b"W2" in lib.ttt_last_error()
+    assert md(z=MIS) == T.TTT_ERR_INVALID_ARG
+    assert md(d=128) == T.TTT_ERR_UNSUPPORTED
+    assert md(hd=192) == T.TTT_ERR_UNSUPPORTED
+    assert md(hd=0) == T.TTT_ERR_INVALID_ARG
+    assert md(dt=3) == T.TTT_ERR_INVALID_ARG
+    assert md(B_=-2) == T.TTT_ERR_INVALID_ARG
+    assert md(H=0, W1=NULL, W2=NULL) == T.TTT_OK
+
+
 def test_binding_rejects_cpu_tensors(lib):
     import torch
     x = torch.zeros(1, 1, 16, 16)

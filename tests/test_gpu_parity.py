@@ -233,3 +233,51 @@ def test_decode_matches_online_prefill(dtype, d):
     Zr, Wr = O.linear_primal(r["Q"], r["K"], r["V"], r["eta"], r["W0"], 1)
     assert rel_err(torch.stack(zs, 2), Zr) <= TOL[dtype]
     assert rel_err(W, Wr) <= TOL[dtype]
+
+
+# --------------------------------------------------------------- MLP decode
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("d,hidden", [(16, 64), (32, 128), (64, 256), (16, 256), (64, 64)])
+def test_mlp_decode_steps(dtype, d, hidden):
+    steps = 3
+    x = WL.mlp_decode_inputs(3, 2, d, hidden, steps, seed=600 + d + hidden, dtype=dtype, w_std=0.1)
+    W1, W2 = x["W1"].cuda(), x["W2"].cuda()
+    A, Bm = WL.to_f64(x["W1"]), WL.to_f64(x["W2"])
+    for s in range(steps):
+        q, k, v, e = (x[n][s].cuda() for n in ("q", "k", "v", "eta"))
+        z = T.mlp_decode_step(q, k, v, e, W1, W2)
+        torch.cuda.synchronize()
+        zr, A, Bm = O.mlp_decode(WL.to_f64(x["q"][s]), WL.to_f64(x["k"][s]), WL.to_f64(x["v"][s]),
+                                 WL.to_f64(x["eta"][s]), A, Bm)
+        assert rel_err(z, zr) <= TOL[dtype]
+        assert rel_err(W1, A) <= TOL[dtype]
+        assert rel_err(W2, Bm) <= TOL[dtype]
+
+
+def test_mlp_decode_workload_steps():
+    w = WL.WORKLOADS["mlp_decode"]
+    x = WL.mlp_decode_inputs(w.B, w.H, w.d, w.hidden, 2, w.seed)
+    W1, W2 = x["W1"].cuda(), x["W2"].cuda()
+    A, Bm = WL.to_f64(x["W1"]), WL.to_f64(x["W2"])
+    for s in range(2):
+        z = T.mlp_decode_step(*(x[n][s].cuda() for n in ("q", "k", "v", "eta")), W1, W2)
+        torch.cuda.synchronize()
+        zr, A, Bm = O.mlp_decode(*(WL.to_f64(x[n][s]) for n in ("q", "k", "v", "eta")), A, Bm)
+        assert rel_err(z, zr) <= TOL["bf16"]
+        assert rel_err(W1, A) <= TOL["bf16"] and rel_err(W2, Bm) <= TOL["bf16"]
+
+
+def test_mlp_decode_matches_online_prefill():
+    # T decode steps equal a TTT-MLP prefill with one-token blocks (both on the GPU)
+    x = WL.mlp_inputs(2, 3, 10, 32, 128, seed=610, dtype="f32", w_std=0.1)
+    g = cuda(x)
+    Zp, W1p, W2p = T.mlp_prefill(g["Q"], g["K"], g["V"], g["eta"], g["W1"], g["W2"], 1)
+    W1, W2 = g["W1"].clone(), g["W2"].clone()
+    zs = [T.mlp_decode_step(g["Q"][:, :, t].contiguous(), g["K"][:, :, t].contiguous(), g["V"][:, :, t].contiguous(),
+                            g["eta"][:, :, t].contiguous(), W1, W2) for t in range(10)]
+    torch.cuda.synchronize()
+    r = f64(x)
+    Zr, W1r, W2r = O.mlp_primal(r["Q"], r["K"], r["V"], r["eta"], r["W1"], r["W2"], 1)
+    assert rel_err(torch.stack(zs, 2), Zr) <= TOL["f32"] and rel_err(Zp, Zr) <= TOL["f32"]
+    assert rel_err(W1, W1r) <= TOL["f32"] and rel_err(W2, W2r) <= TOL["f32"]

@@ -299,6 +299,26 @@ def test_mlp_online_is_plain_gradient_descent():
     assert _rel(W1o[0, 0], A) < 1e-13 and _rel(W2o[0, 0], Bm) < 1e-13
 
 
+def test_mlp_decode_is_one_token_online_step():
+    # the decode oracle is the token-level scan on one token: plain gradient descent (autograd)
+    rng = np.random.default_rng(20)
+    B, H, d, hd = 2, 1, 4, 6
+    q, k, v = (rng.standard_normal((B, H, d)) for _ in range(3))
+    eta = rng.uniform(0.1, 0.5, (B, H))
+    W1, W2 = rng.standard_normal((B, H, d, hd)) * 0.5, rng.standard_normal((B, H, hd, d)) * 0.5
+    z, A, Bm = O.mlp_decode(q, k, v, eta, W1, W2)
+    gelu_t = lambda x: torch.nn.functional.gelu(x, approximate="tanh")
+    for b in range(B):
+        At, Bt = torch.tensor(W1[b, 0], requires_grad=True), torch.tensor(W2[b, 0], requires_grad=True)
+        loss = 0.5 * ((gelu_t(torch.tensor(k[b, 0]) @ At) @ Bt - torch.tensor(v[b, 0])) ** 2).sum()
+        loss.backward()
+        A1 = W1[b, 0] - eta[b, 0] * At.grad.numpy()
+        B1 = W2[b, 0] - eta[b, 0] * Bt.grad.numpy()
+        assert _rel(A[b, 0], A1) < 1e-12 and _rel(Bm[b, 0], B1) < 1e-12
+        zr = (gelu_t(torch.tensor(q[b, 0]) @ torch.tensor(A1)) @ torch.tensor(B1)).numpy()
+        assert _rel(z[b, 0], zr) < 1e-12
+
+
 # ------------------------------------------------------------- workloads
 
 def test_workload_inputs_are_seeded_and_rounded():
