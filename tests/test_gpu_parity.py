@@ -281,3 +281,44 @@ def test_mlp_decode_matches_online_prefill():
     Zr, W1r, W2r = O.mlp_primal(r["Q"], r["K"], r["V"], r["eta"], r["W1"], r["W2"], 1)
     assert rel_err(torch.stack(zs, 2), Zr) <= TOL["f32"] and rel_err(Zp, Zr) <= TOL["f32"]
     assert rel_err(W1, W1r) <= TOL["f32"] and rel_err(W2, W2r) <= TOL["f32"]
+
+
+# ------------------------------------------------- prefill -> decode hand-off
+
+@pytest.mark.parametrize("kind", ["linear", "mlp"])
+def test_prefill_then_decode_hand_off(kind):
+    # a prompt of P tokens in blocks of 16 (last block ragged), then D single-token decode steps
+    # from the prefill's final state: the oracle runs the same schedule (block scan, then b = 1)
+    P, Dn, d = 40, 5, 64
+    if kind == "linear":
+        x = WL.linear_inputs(2, 3, P + Dn, d, seed=700, dtype="bf16")
+    else:
+        x = WL.mlp_inputs(2, 3, P + Dn, d, 256, seed=701, dtype="bf16", w_std=0.1)
+    g = cuda(x)
+    sl = lambda t, a, b: t[:, :, a:b].contiguous()
+    r = f64(x)
+    rs = lambda t, a, b: t[:, :, a:b]
+    if kind == "linear":
+        Zp, W = T.linear_prefill(sl(g["Q"], 0, P), sl(g["K"], 0, P), sl(g["V"], 0, P), sl(g["eta"], 0, P), g["W0"], 16)
+        zs = [T.linear_decode_step(g["Q"][:, :, t].contiguous(), g["K"][:, :, t].contiguous(),
+                                   g["V"][:, :, t].contiguous(), g["eta"][:, :, t].contiguous(), W)
+              for t in range(P, P + Dn)]
+        torch.cuda.synchronize()
+        Zr1, Wr1 = O.linear_primal(rs(r["Q"], 0, P), rs(r["K"], 0, P), rs(r["V"], 0, P), rs(r["eta"], 0, P), r["W0"], 16)
+        Zr2, Wr2 = O.linear_primal(rs(r["Q"], P, P + Dn), rs(r["K"], P, P + Dn), rs(r["V"], P, P + Dn),
+                                   rs(r["eta"], P, P + Dn), Wr1, 1)
+        assert rel_err(W, Wr2) <= TOL["bf16"]
+    else:
+        Zp, W1, W2 = T.mlp_prefill(sl(g["Q"], 0, P), sl(g["K"], 0, P), sl(g["V"], 0, P), sl(g["eta"], 0, P),
+                                   g["W1"], g["W2"], 16)
+        zs = [T.mlp_decode_step(g["Q"][:, :, t].contiguous(), g["K"][:, :, t].contiguous(),
+                                g["V"][:, :, t].contiguous(), g["eta"][:, :, t].contiguous(), W1, W2)
+              for t in range(P, P + Dn)]
+        torch.cuda.synchronize()
+        Zr1, A1, B1 = O.mlp_primal(rs(r["Q"], 0, P), rs(r["K"], 0, P), rs(r["V"], 0, P), rs(r["eta"], 0, P),
+                                   r["W1"], r["W2"], 16)
+        Zr2, A2, B2 = O.mlp_primal(rs(r["Q"], P, P + Dn), rs(r["K"], P, P + Dn), rs(r["V"], P, P + Dn),
+                                   rs(r["eta"], P, P + Dn), A1, B1, 1)
+        assert rel_err(W1, A2) <= TOL["bf16"] and rel_err(W2, B2) <= TOL["bf16"]
+    assert rel_err(Zp, Zr1) <= TOL["bf16"]
+    assert rel_err(torch.stack(zs, 2), Zr2) <= TOL["bf16"]
