@@ -167,6 +167,16 @@ ttt_status ttt_mlp_decode_step(const void* q, const void* k, const void* v, cons
  */
 ttt_status ttt_get_device_status(void* stream);
 
+/*
+ * Diagnostic: exercises the device-side failure path without faulting the GPU.
+ * Launches one CTA that waits, with the bounded wait the prefill kernels use,
+ * on a barrier nothing ever completes; after `limit_ns` nanoseconds (1 ns .. 2 s,
+ * else TTT_ERR_INVALID_ARG) it records TTT_ERR_TIMEOUT in the device status
+ * word and returns.  Asynchronous on `stream`; read the outcome with
+ * ttt_get_device_status().  Not part of the computation; no page counterpart.
+ */
+ttt_status ttt_selftest_wait_timeout(uint64_t limit_ns, void* stream);
+
 /* Static English text for a status code. */
 const char* ttt_status_string(ttt_status s);
 

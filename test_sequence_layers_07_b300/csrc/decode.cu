@@ -10,6 +10,15 @@
 // use), the partial products k W and q W are reduced across the 8 row groups
 // through shared memory, and the same registers are updated and stored back,
 // so W is read once and written once.
+//
+// For d in {64, 128} a streaming kernel is used instead: each CTA runs GPC
+// groups of d threads (thread c owns column c of W, so k W and q W need no
+// reduction across threads), and each group works through a fixed, equal
+// share of the heads.  The 16 or 64 KB state of a head arrives by one bulk
+// copy (cp.async.bulk, with q, k, v) into an NSTG-stage shared-memory ring,
+// is updated in place, and leaves by one bulk store; the next heads' copies
+// are in flight meanwhile.
+#include "ptx.cuh"
 #include "ttt_common.cuh"
 #include "ttt_internal.h"
 
@@ -17,6 +26,7 @@ namespace ttt {
 namespace {
 
 constexpr int kThreads = 256;
+constexpr uint64_t kWaitLimitNs = 4000000000ull;
 
 template <typename TI, int D>
 __global__ void __launch_bounds__(kThreads)
@@ -97,6 +107,166 @@ linear_decode_kernel(const TI* __restrict__ q, const TI* __restrict__ k, const T
     }
 }
 
+template <typename TI, int D, int GPC, int NSTG>
+struct StreamCfg {
+    static constexpr int WB = D * D * 4;              // fp32 state of a head
+    static constexpr int IO = D * int(sizeof(TI));    // one of q, k, v
+    static constexpr int STG = (WB + 3 * IO + 127) / 128 * 128;
+    static constexpr int BYTES = GPC * NSTG * STG;
+    static constexpr int THREADS = GPC * D;
+};
+
+__device__ __forceinline__ void group_bar(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
+
+__device__ __forceinline__ bool group_any(int id, int n, bool c) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"(uint32_t(c)), "r"(id), "r"(n)
+        : "memory");
+    return r != 0;
+}
+
+// 8 consecutive elements of q, k or v in shared memory, as fp32
+__device__ __forceinline__ void ld8(const float* p, float (&o)[8]) {
+    const float4 a = reinterpret_cast<const float4*>(p)[0], b = reinterpret_cast<const float4*>(p)[1];
+    o[0] = a.x; o[1] = a.y; o[2] = a.z; o[3] = a.w; o[4] = b.x; o[5] = b.y; o[6] = b.z; o[7] = b.w;
+}
+__device__ __forceinline__ void ld8(const __nv_bfloat16* p, float (&o)[8]) {
+    const uint4 u = *reinterpret_cast<const uint4*>(p);
+    o[0] = ptx::bf16_lo(u.x); o[1] = ptx::bf16_hi(u.x); o[2] = ptx::bf16_lo(u.y); o[3] = ptx::bf16_hi(u.y);
+    o[4] = ptx::bf16_lo(u.z); o[5] = ptx::bf16_hi(u.z); o[6] = ptx::bf16_lo(u.w); o[7] = ptx::bf16_hi(u.w);
+}
+
+template <typename TI, int D, int GPC, int NSTG>
+__global__ void __launch_bounds__(GPC * D, 1)
+linear_decode_stream_kernel(const TI* __restrict__ q, const TI* __restrict__ k, const TI* __restrict__ v,
+                            const float* __restrict__ eta, float* W, TI* __restrict__ z, int BH, int per,
+                            int* status) {
+    using C = StreamCfg<TI, D, GPC, NSTG>;
+    extern __shared__ __align__(128) uint8_t smem_s[];
+    __shared__ __align__(8) uint64_t full[GPC][NSTG];
+    __shared__ volatile int s_err;
+    __shared__ volatile int s_zero;
+    const int g = threadIdx.x / D, c = threadIdx.x % D;  // group, column
+    const int h0 = (blockIdx.x * GPC + g) * per;         // first head of this group
+    const int nh = BH - h0 < per ? (BH - h0 > 0 ? BH - h0 : 0) : per;
+    const int bar_id = 1 + g;
+    if (threadIdx.x == 0) {
+        for (int gg = 0; gg < GPC; ++gg)
+            for (int st = 0; st < NSTG; ++st) ptx::mbar_init(ptx::smem_u32(&full[gg][st]), 1);
+        s_err = 0;
+        s_zero = 0;
+        ptx::fence_mbar_init();
+    }
+    __syncthreads();
+    uint8_t* gbase = smem_s + g * NSTG * C::STG;
+    const uint32_t gb = ptx::smem_u32(gbase);
+    const bool prod = c == 0;
+    auto issue = [&](int i) {  // the group's i-th head into stage i % NSTG
+        const int st = i % NSTG;
+        const size_t h = size_t(h0) + i;
+        const uint32_t dst = gb + st * C::STG;
+        const uint32_t fb = ptx::smem_u32(&full[g][st]);
+        ptx::mbar_arrive_expect_tx(fb, C::WB + 3 * C::IO);
+        ptx::bulk_load(dst, W + h * D * D, C::WB, fb);
+        ptx::bulk_load(dst + C::WB, q + h * D, C::IO, fb);
+        ptx::bulk_load(dst + C::WB + C::IO, k + h * D, C::IO, fb);
+        ptx::bulk_load(dst + C::WB + 2 * C::IO, v + h * D, C::IO, fb);
+    };
+    // NSTG - 1 heads are in flight ahead of the one being updated; the last stage is refilled
+    // one head late, so that the refill never waits for a store that was just issued
+    int issued = 0;
+    if (prod)
+        for (; issued < NSTG && issued < nh; ++issued) issue(issued);
+    int done = 0;
+    for (int i = 0; i < nh; ++i) {
+        const int st = i % NSTG;
+        const size_t h = size_t(h0) + i;
+        const bool ok = ptx::mbar_wait_bounded(ptx::smem_u32(&full[g][st]), (i / NSTG) & 1, &s_err, kWaitLimitNs);
+        if (group_any(bar_id, D, !ok)) {
+            if (!s_err) record_status(status, kStatusTimeout);
+            s_err = 1;
+            break;
+        }
+        float* Ws = reinterpret_cast<float*>(gbase + st * C::STG);
+        const TI* qs = reinterpret_cast<const TI*>(gbase + st * C::STG + C::WB);
+        const TI* ks = qs + D;
+        const TI* vs = ks + D;
+        const float et = eta[h];
+        float w[D <= 64 ? D : 1];
+        float kw = 0.f, qw = 0.f, qk = 0.f;
+#pragma unroll(D <= 64 ? D / 8 : 2)
+        for (int r0 = 0; r0 < D; r0 += 8) {
+            float kr[8], qr[8];
+            ld8(ks + r0, kr);
+            ld8(qs + r0, qr);
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const float wv = Ws[(r0 + u) * D + c];
+                if constexpr (D <= 64) w[r0 + u] = wv;
+                kw = fmaf(kr[u], wv, kw);
+                qw = fmaf(qr[u], wv, qw);
+                qk = fmaf(qr[u], kr[u], qk);
+            }
+        }
+        const float e = kw - to_f32(vs[c]);
+        z[h * D + c] = from_f32<TI>(fmaf(-et * qk, e, qw));  // q W_new = q W - eta (q.k) e
+        const float ne = -et * e;
+#pragma unroll(D <= 64 ? D / 8 : 2)
+        for (int r0 = 0; r0 < D; r0 += 8) {
+            float kr[8];
+            ld8(ks + r0, kr);
+#pragma unroll
+            for (int u = 0; u < 8; ++u)  // registers hold the column at d = 64; re-read it at d = 128
+                Ws[(r0 + u) * D + c] = fmaf(ne, kr[u], D <= 64 ? w[r0 + u] : Ws[(r0 + u) * D + c]);
+        }
+        ptx::fence_proxy_async_smem();  // the stage's new state is visible to the bulk store
+        group_bar(bar_id, D);
+        if (prod) {
+            ptx::bulk_store(W + h * D * D, ptx::smem_u32(Ws), C::WB);
+            ptx::bulk_commit();
+            // refill the previous head's stage, whose store was issued one head ago
+            if (i >= 1 && issued < nh) {
+                ptx::bulk_wait_read_1();
+                issue(issued);
+                ++issued;
+            }
+        }
+        done = i + 1;
+    }
+    if (prod) {
+        ptx::bulk_wait_all();
+        // never retire with copies in flight (after an expired wait only)
+        for (int i = done; i < issued; ++i)
+            ptx::mbar_wait_bounded(ptx::smem_u32(&full[g][i % NSTG]), (i / NSTG) & 1, &s_zero, kWaitLimitNs);
+    }
+}
+
+template <typename TI, int D, int GPC, int NSTG>
+cudaError_t launch_stream(const DecodeArgs& a, cudaStream_t s, int* status) {
+    using C = StreamCfg<TI, D, GPC, NSTG>;
+    const int BH = a.B * a.H;
+    int dev = 0, sms = 148;
+    if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    // an equal share of heads per group, one CTA per SM at most
+    const int groups0 = sms * GPC;
+    const int per = (BH + groups0 - 1) / groups0;
+    const int groups = (BH + per - 1) / per;
+    const unsigned grid = unsigned((groups + GPC - 1) / GPC);
+    auto kern = linear_decode_stream_kernel<TI, D, GPC, NSTG>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::BYTES);
+    if (e != cudaSuccess) return e;
+    kern<<<grid, C::THREADS, C::BYTES, s>>>(static_cast<const TI*>(a.q), static_cast<const TI*>(a.k),
+                                           static_cast<const TI*>(a.v), a.eta, a.W, static_cast<TI*>(a.z), BH, per,
+                                           status);
+    return cudaGetLastError();
+}
+
 template <typename TI, int D>
 cudaError_t launch_d(const DecodeArgs& a, cudaStream_t s) {
     constexpr int HPC = kThreads / (2 * D);
@@ -109,20 +279,20 @@ cudaError_t launch_d(const DecodeArgs& a, cudaStream_t s) {
 }
 
 template <typename TI>
-cudaError_t launch_t(const DecodeArgs& a, cudaStream_t s) {
+cudaError_t launch_t(const DecodeArgs& a, cudaStream_t s, int* status) {
     switch (a.d) {
         case 16: return launch_d<TI, 16>(a, s);
         case 32: return launch_d<TI, 32>(a, s);
-        case 64: return launch_d<TI, 64>(a, s);
-        case 128: return launch_d<TI, 128>(a, s);
+        case 64: return launch_stream<TI, 64, 4, 3>(a, s, status);
+        case 128: return launch_stream<TI, 128, 1, 3>(a, s, status);
         default: return cudaErrorNotSupported;
     }
 }
 
 }  // namespace
 
-cudaError_t launch_linear_decode(const DecodeArgs& a, cudaStream_t s) {
-    return a.bf16 ? launch_t<__nv_bfloat16>(a, s) : launch_t<float>(a, s);
+cudaError_t launch_linear_decode(const DecodeArgs& a, cudaStream_t s, int* status) {
+    return a.bf16 ? launch_t<__nv_bfloat16>(a, s, status) : launch_t<float>(a, s, status);
 }
 
 }  // namespace ttt

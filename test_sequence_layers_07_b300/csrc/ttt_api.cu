@@ -162,7 +162,10 @@ ttt_status ttt_linear_decode_step(const void* q, const void* k, const void* v, c
     CHECK_PTR(W);
     CHECK_PTR(z);
     ttt::DecodeArgs a{q, k, v, eta, W, z, B, H, d, dtype == TTT_BF16 ? 1 : 0};
-    cudaError_t e = ttt::launch_linear_decode(a, static_cast<cudaStream_t>(stream));
+    int* status = nullptr;
+    cudaError_t e = status_ptr(&status);
+    if (e != cudaSuccess) return cuda_fail(e, "ttt_linear_decode_step status word");
+    e = ttt::launch_linear_decode(a, static_cast<cudaStream_t>(stream), status);
     if (e != cudaSuccess) return cuda_fail(e, "ttt_linear_decode_step launch");
     return TTT_OK;
 }
@@ -188,6 +191,18 @@ ttt_status ttt_mlp_decode_step(const void* q, const void* k, const void* v, cons
     ttt::MlpDecodeArgs a{q, k, v, eta, W1, W2, z, B, H, d, hidden, dtype == TTT_BF16 ? 1 : 0};
     cudaError_t e = ttt::launch_mlp_decode(a, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "ttt_mlp_decode_step launch");
+    return TTT_OK;
+}
+
+ttt_status ttt_selftest_wait_timeout(uint64_t limit_ns, void* stream) {
+    g_last_error[0] = 0;
+    if (limit_ns == 0 || limit_ns > 2000000000ull)
+        return fail(TTT_ERR_INVALID_ARG, "limit must be in 1 ns .. 2 s%s");
+    int* status = nullptr;
+    cudaError_t e = status_ptr(&status);
+    if (e != cudaSuccess) return cuda_fail(e, "ttt_selftest_wait_timeout status word");
+    e = ttt::launch_wait_timeout_selftest(limit_ns, static_cast<cudaStream_t>(stream), status);
+    if (e != cudaSuccess) return cuda_fail(e, "ttt_selftest_wait_timeout launch");
     return TTT_OK;
 }
 

@@ -76,8 +76,11 @@ cudaError_t launch_mlp_prefill_tc(const MlpArgs& a, cudaStream_t s, int* status)
 // columns with the 128-byte swizzle (D a multiple of 64).
 cudaError_t make_tma_map_bf16(CUtensorMap* m, const void* base, uint64_t rows, int D);
 
+// Device-side failure path: a bounded wait that nothing satisfies (see selftest.cu).
+cudaError_t launch_wait_timeout_selftest(unsigned long long limit_ns, cudaStream_t s, int* status);
+
 // Bandwidth-bound single-token steps.
-cudaError_t launch_linear_decode(const DecodeArgs& a, cudaStream_t s);
+cudaError_t launch_linear_decode(const DecodeArgs& a, cudaStream_t s, int* status);
 cudaError_t launch_mlp_decode(const MlpDecodeArgs& a, cudaStream_t s);
 
 }  // namespace ttt

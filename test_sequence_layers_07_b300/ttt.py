@@ -26,7 +26,7 @@ TTT_OK, TTT_ERR_INVALID_ARG, TTT_ERR_UNSUPPORTED, TTT_ERR_CUDA, TTT_ERR_TIMEOUT 
 TTT_F32, TTT_BF16 = 0, 1
 
 EXPORTED = ("ttt_linear_prefill", "ttt_mlp_prefill", "ttt_linear_decode_step", "ttt_mlp_decode_step",
-            "ttt_get_device_status", "ttt_status_string", "ttt_last_error", "ttt_version")
+            "ttt_get_device_status", "ttt_selftest_wait_timeout", "ttt_status_string", "ttt_last_error", "ttt_version")
 
 
 class TTTError(RuntimeError):
@@ -55,6 +55,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
             lib.ttt_linear_decode_step.argtypes = [vp, vp, vp, fp, fp, vp, i, i, i, i, vp]
             lib.ttt_mlp_decode_step.argtypes = [vp, vp, vp, fp, fp, fp, vp, i, i, i, i, i, vp]
             lib.ttt_get_device_status.argtypes = [vp]
+            lib.ttt_selftest_wait_timeout.argtypes = [ctypes.c_uint64, vp]
+            lib.ttt_selftest_wait_timeout.restype = i
             for f in (lib.ttt_linear_prefill, lib.ttt_mlp_prefill, lib.ttt_linear_decode_step,
                       lib.ttt_mlp_decode_step, lib.ttt_get_device_status):
                 f.restype = i
@@ -167,6 +169,11 @@ def ttt_mlp_decode_step(q, k, v, eta, W1, W2, z, stream=None) -> None:
         _ptr(q, "q"), _ptr(k, "k"), _ptr(v, "v"), _ptr(eta, "eta", torch.float32), _ptr(W1, "W1", torch.float32),
         _ptr(W2, "W2", torch.float32), _ptr(z, "z"), B, H, d, hidden, dt, _stream(stream))
     _check(st)
+
+
+def ttt_selftest_wait_timeout(limit_ns: int, stream=None) -> None:
+    """Launches the device-side bounded-wait self-test (records TTT_ERR_TIMEOUT after `limit_ns`)."""
+    _check(load_library().ttt_selftest_wait_timeout(int(limit_ns), _stream(stream)))
 
 
 def ttt_get_device_status(stream=None) -> int:

@@ -138,6 +138,11 @@ def test_mlp_decode_validation(lib):
     assert md(H=0, W1=NULL, W2=NULL) == T.TTT_OK
 
 
+def test_selftest_limit_validation(lib):
+    assert lib.ttt_selftest_wait_timeout(0, None) == T.TTT_ERR_INVALID_ARG
+    assert lib.ttt_selftest_wait_timeout(3 * 10**9, None) == T.TTT_ERR_INVALID_ARG
+
+
 def test_binding_rejects_cpu_tensors(lib):
     import torch
     x = torch.zeros(1, 1, 16, 16)
