@@ -261,7 +261,8 @@ linear_prefill_mma_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_
                 const int s = si % NST, n = subs_in(si), x = si % NX;
                 const uint32_t st = sbase + s * C::STAGE;
                 uint8_t* gout = gslots + x * SPS * 512;
-                for (int i = 0; i < n; ++i) {
+                // one 16-token sub-block of the recurrence
+                auto step = [&](int i) {
                     const int sb = si * SPS + i;
                     if (SINGLE || sb % nsub == 0) pack_state<KS>(w, wa0);
                     float pa[4][2][4] = {};
@@ -288,7 +289,18 @@ linear_prefill_mma_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_
                         mma_bf16_16816(w[2 * kk + 1], ga, kt[kk][2], kt[kk][3]);
                     }
                     *reinterpret_cast<uint4*>(gout + i * 512 + lane * 16) = make_uint4(ga[0], ga[1], ga[2], ga[3]);
-                    if (i + 1 < n) load(st, i + 1);
+                };
+                if (n == SPS) {  // full stage: unrolled, so the compiler schedules across sub-blocks
+#pragma unroll
+                    for (int i = 0; i < SPS; ++i) {
+                        step(i);
+                        if (i + 1 < SPS) load(st, i + 1);
+                    }
+                } else {
+                    for (int i = 0; i < n; ++i) {
+                        step(i);
+                        if (i + 1 < n) load(st, i + 1);
+                    }
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&xf_bar[cg][x]));
