@@ -333,7 +333,7 @@ linear_prefill_mma_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_
                 if (!wait(full_bar[s], par) || !wait(sc_bar[s], par) || !wait(xf_bar[cg][x], (si / NX) & 1)) break;
                 const uint32_t st = sbase + s * C::STAGE;
                 const uint8_t* gin = gslots + x * SPS * 512;
-                for (int i = 0; i < n; ++i) {
+                auto step = [&](int i) {
                     uint32_t qb[KS][4], kt[NT / 2][4], wr[KS][4];
 #pragma unroll
                     for (int ks = 0; ks < KS; ++ks) ldsm_x4(st + C::QOFF + i * C::TILE + off_nk[ks], qb[ks]);
@@ -373,6 +373,12 @@ linear_prefill_mma_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_
                     *reinterpret_cast<uint4*>(zp) = v;
                     zp += 16 * D;
                     __syncwarp();
+                                };
+                if (n == SPS) {
+#pragma unroll
+                    for (int i = 0; i < SPS; ++i) step(i);
+                } else {
+                    for (int i = 0; i < n; ++i) step(i);
                 }
                 __syncwarp();
                 // Q, K, the scores and the error operands of this stage are consumed; the chain
