@@ -86,6 +86,13 @@ typedef enum ttt_dtype {
  *   chunk    1..512; the last block may be shorter when chunk does not divide T
  *   d        16, 32, 64 or 128 (else TTT_ERR_UNSUPPORTED)
  *
+ * Kernels: bf16 with 16 | chunk and chunk | T runs on the tensor cores (at
+ * d = 64 and 32 <= chunk <= 128 with the read-out as tcgen05 products, else
+ * on warp-level MMAs); other shapes on a generic SIMT kernel.  The environment
+ * variable TTT_LINEAR_PREFILL_KERNEL = "tc", "mma" or "generic" starts the
+ * choice at that kernel (a kernel that does not cover the shape passes it on).
+ * All give the same result up to rounding.
+ *
  * Source: "Test-Time Training Layers ...", sections "The Core Mechanism" and
  * "Hardware Parallelization"; TTT essay, paragraph on the dual form.
  */

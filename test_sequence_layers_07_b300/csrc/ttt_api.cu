@@ -8,6 +8,7 @@
 
 #include <mutex>
 #include <stdio.h>
+#include <stdlib.h>
 #include <string.h>
 
 #include "../../include/ttt.h"
@@ -66,6 +67,17 @@ cudaError_t status_ptr(int** out) {
 
 extern "C" {
 
+// First kernel of the TTT-Linear prefill dispatch from the environment: 0 tc, 1 mma, 2 generic,
+// -1 (unset or unknown) the default choice by shape.
+static int linear_kernel_choice() {
+    const char* v = getenv("TTT_LINEAR_PREFILL_KERNEL");
+    if (!v) return -1;
+    if (!strcmp(v, "tc")) return 0;
+    if (!strcmp(v, "mma")) return 1;
+    if (!strcmp(v, "generic")) return 2;
+    return -1;
+}
+
 ttt_status ttt_linear_prefill(const void* Q, const void* K, const void* V, const float* eta, const float* W0,
                               void* Z, float* W_out, int B, int H, int T, int d, int chunk, ttt_dtype dtype,
                               void* stream) {
@@ -96,8 +108,15 @@ ttt_status ttt_linear_prefill(const void* Q, const void* K, const void* V, const
     int* status = nullptr;
     cudaError_t e = status_ptr(&status);
     if (e != cudaSuccess) return cuda_fail(e, "ttt_linear_prefill status word");
-    // tensor-core kernel for bf16, d in {64, 128}, 16 | chunk, chunk | T; generic kernel otherwise
-    e = ttt::launch_linear_prefill_mma(a, s, status);
+    // bf16, 16 | chunk, chunk | T: the tcgen05 read-out kernel at d = 64 where it is the faster one,
+    // the warp-MMA kernel at d in {64, 128}; the generic kernel otherwise.
+    // TTT_LINEAR_PREFILL_KERNEL = "tc", "mma" or "generic" makes the dispatch start at that kernel
+    // (the next one takes the shapes it does not cover).
+    const int first = linear_kernel_choice();
+    e = cudaErrorNotSupported;
+    if (first == 0 || (first < 0 && ttt::linear_prefill_tc_preferred(a)))
+        e = ttt::launch_linear_prefill_tc(a, s, status);
+    if (e == cudaErrorNotSupported && first <= 1) e = ttt::launch_linear_prefill_mma(a, s, status);
     if (e == cudaErrorNotSupported) e = ttt::launch_linear_prefill_generic(a, s);
     if (e != cudaSuccess) return cuda_fail(e, "ttt_linear_prefill launch");
     return TTT_OK;

@@ -68,6 +68,12 @@ size_t mlp_generic_smem_bytes(int d, int hidden, int chunk);
 // the generic kernel instead.
 cudaError_t launch_linear_prefill_mma(const LinearArgs& a, cudaStream_t s, int* status);
 
+// TTT-Linear prefill at d = 64 (bf16, 16 | chunk, chunk | T): the recurrence on
+// warp-level MMAs, the read-out as per-stage tcgen05 products.
+bool linear_prefill_tc_supported(const LinearArgs& a);
+bool linear_prefill_tc_preferred(const LinearArgs& a);  // the faster of the two at this shape
+cudaError_t launch_linear_prefill_tc(const LinearArgs& a, cudaStream_t s, int* status);
+
 // Tensor-core (tcgen05) TTT-MLP prefill for bf16, d = 64, hidden = 256, chunk = 16.
 bool mlp_prefill_tc_supported(const MlpArgs& a);
 cudaError_t launch_mlp_prefill_tc(const MlpArgs& a, cudaStream_t s, int* status);

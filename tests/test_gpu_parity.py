@@ -5,6 +5,9 @@ Error metric: max|delta| / ||ref||_inf per output; bar 1e-4 for fp32 inputs and
 are the seeded workloads of test_sequence_layers_07_b300.workloads; the oracle
 reads exactly the rounded values the GPU reads.
 """
+import contextlib
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -67,6 +70,39 @@ def test_linear_small_shapes(dtype, d, T_, chunk):
     assert rel_err(W, Wr) <= TOL[dtype]
 
 
+@contextlib.contextmanager
+def linear_kernel(name):
+    """Start the TTT-Linear prefill dispatch at kernel `name` ("tc", "mma" or "generic")."""
+    old = os.environ.get("TTT_LINEAR_PREFILL_KERNEL")
+    os.environ["TTT_LINEAR_PREFILL_KERNEL"] = name
+    try:
+        yield
+    finally:
+        if old is None:
+            del os.environ["TTT_LINEAR_PREFILL_KERNEL"]
+        else:
+            os.environ["TTT_LINEAR_PREFILL_KERNEL"] = old
+
+
+# d = 64 bf16 shapes the tensor-core kernels take: one 16-token block, stages of 128 tokens
+# with and without a short last stage, blocks longer than a stage, more CTAs than SMs
+TC_CASES = [(1, 1, 16, 16, 0.02), (2, 3, 128, 16, 0.02), (2, 3, 144, 16, 0.1), (1, 2, 1040, 16, 0.05),
+            (2, 2, 256, 32, 0.02), (1, 3, 384, 128, 0.1), (2, 2, 512, 256, 0.02), (1, 2, 1024, 512, 0.05),
+            (1, 2, 640, 64, 0.02), (4, 75, 128, 16, 0.02)]
+
+
+@pytest.mark.parametrize("kernel", ["tc", "mma", "generic"])
+@pytest.mark.parametrize("B,H,T_,chunk,w_std", TC_CASES)
+def test_linear_kernels_d64(kernel, B, H, T_, chunk, w_std):
+    x = WL.linear_inputs(B, H, T_, 64, seed=300 + T_ + chunk + H, dtype="bf16", w_std=w_std)
+    with linear_kernel(kernel):
+        Z, W = run_linear(x, chunk)
+    r = f64(x)
+    Zr, Wr = O.linear_dual(r["Q"], r["K"], r["V"], r["eta"], r["W0"], chunk)
+    assert rel_err(Z, Zr) <= TOL["bf16"]
+    assert rel_err(W, Wr) <= TOL["bf16"]
+
+
 def test_linear_prefill_workload_sampled_heads():
     w = WL.WORKLOADS["linear_prefill"]
     x = WL.workload_inputs(w)
@@ -125,10 +161,12 @@ def test_linear_empty_sequence_copies_state():
     assert torch.equal(Wo, x["W0"])
 
 
-def test_linear_deterministic():
+@pytest.mark.parametrize("kernel", ["tc", "mma"])
+def test_linear_deterministic(kernel):
     x = WL.linear_inputs(2, 3, 256, 64, seed=11, dtype="bf16")
-    Z1, W1 = run_linear(x, 16)
-    Z2, W2 = run_linear(x, 16)
+    with linear_kernel(kernel):
+        Z1, W1 = run_linear(x, 16)
+        Z2, W2 = run_linear(x, 16)
     assert torch.equal(Z1, Z2) and torch.equal(W1, W2)
 
 
