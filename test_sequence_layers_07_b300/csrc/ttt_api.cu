@@ -67,13 +67,13 @@ cudaError_t status_ptr(int** out) {
 
 extern "C" {
 
-// First kernel of the TTT-Linear prefill dispatch from the environment: 0 tc, 1 mma, 2 generic,
-// -1 (unset or unknown) the default choice by shape.
-static int linear_kernel_choice() {
-    const char* v = getenv("TTT_LINEAR_PREFILL_KERNEL");
+// First kernel of a prefill dispatch from the environment variable `var`: 0 (`k0`), 1 (`k1`),
+// 2 ("generic"), or -1 when unset or unknown (the default choice by shape).
+static int kernel_choice(const char* var, const char* k0, const char* k1) {
+    const char* v = getenv(var);
     if (!v) return -1;
-    if (!strcmp(v, "tc")) return 0;
-    if (!strcmp(v, "mma")) return 1;
+    if (!strcmp(v, k0)) return 0;
+    if (!strcmp(v, k1)) return 1;
     if (!strcmp(v, "generic")) return 2;
     return -1;
 }
@@ -112,7 +112,7 @@ ttt_status ttt_linear_prefill(const void* Q, const void* K, const void* V, const
     // the warp-MMA kernel at d in {64, 128}; the generic kernel otherwise.
     // TTT_LINEAR_PREFILL_KERNEL = "tc", "mma" or "generic" makes the dispatch start at that kernel
     // (the next one takes the shapes it does not cover).
-    const int first = linear_kernel_choice();
+    const int first = kernel_choice("TTT_LINEAR_PREFILL_KERNEL", "tc", "mma");
     e = cudaErrorNotSupported;
     if (first == 0 || (first < 0 && ttt::linear_prefill_tc_preferred(a)))
         e = ttt::launch_linear_prefill_tc(a, s, status);
@@ -158,8 +158,13 @@ ttt_status ttt_mlp_prefill(const void* Q, const void* K, const void* V, const fl
     int* status = nullptr;
     cudaError_t e = status_ptr(&status);
     if (e != cudaSuccess) return cuda_fail(e, "ttt_mlp_prefill status word");
-    // tensor-core kernel for bf16, d = 64, hidden = 256, chunk = 16, 16 | T; generic kernel otherwise
-    e = ttt::launch_mlp_prefill_tc(a, s, status);
+    // bf16, d = 64, hidden = 256, chunk = 16, 16 | T: the warp-MMA kernel (state in registers), else
+    // the tcgen05 kernel; the generic kernel otherwise.  TTT_MLP_PREFILL_KERNEL = "mma", "tc" or
+    // "generic" makes the dispatch start at that kernel.
+    const int first = kernel_choice("TTT_MLP_PREFILL_KERNEL", "mma", "tc");
+    e = cudaErrorNotSupported;
+    if (first <= 0) e = ttt::launch_mlp_prefill_mma(a, s, status);
+    if (e == cudaErrorNotSupported && first <= 1) e = ttt::launch_mlp_prefill_tc(a, s, status);
     if (e == cudaErrorNotSupported) e = ttt::launch_mlp_prefill_generic(a, s);
     if (e != cudaSuccess) return cuda_fail(e, "ttt_mlp_prefill launch");
     return TTT_OK;

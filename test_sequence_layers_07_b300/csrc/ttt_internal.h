@@ -74,6 +74,11 @@ bool linear_prefill_tc_supported(const LinearArgs& a);
 bool linear_prefill_tc_preferred(const LinearArgs& a);  // the faster of the two at this shape
 cudaError_t launch_linear_prefill_tc(const LinearArgs& a, cudaStream_t s, int* status);
 
+// TTT-MLP prefill for bf16, d = 64, hidden = 256, chunk = 16 on warp-level MMAs with the state in
+// registers.
+bool mlp_prefill_mma_supported(const MlpArgs& a);
+cudaError_t launch_mlp_prefill_mma(const MlpArgs& a, cudaStream_t s, int* status);
+
 // Tensor-core (tcgen05) TTT-MLP prefill for bf16, d = 64, hidden = 256, chunk = 16.
 bool mlp_prefill_tc_supported(const MlpArgs& a);
 cudaError_t launch_mlp_prefill_tc(const MlpArgs& a, cudaStream_t s, int* status);

@@ -188,11 +188,29 @@ def test_mlp_small_shapes(dtype, d, T_, chunk):
     assert rel_err(W2, W2r) <= TOL[dtype]
 
 
-@pytest.mark.parametrize("T_,w_std,seed", [(16, 0.1, 1), (64, 0.02, 2), (400, 0.1, 3), (1024, 0.05, 4)])
-def test_mlp_tensor_core_shape(T_, w_std, seed):
-    # d = 64, hidden = 256, blocks of 16, bf16: the tcgen05 kernel
-    x = WL.mlp_inputs(2, 3, T_, 64, 256, seed=500 + seed, dtype="bf16", w_std=w_std)
-    Z, W1, W2 = run_mlp(x, 16)
+@contextlib.contextmanager
+def mlp_kernel(name):
+    """Start the TTT-MLP prefill dispatch at kernel `name` ("mma", "tc" or "generic")."""
+    old = os.environ.get("TTT_MLP_PREFILL_KERNEL")
+    os.environ["TTT_MLP_PREFILL_KERNEL"] = name
+    try:
+        yield
+    finally:
+        if old is None:
+            del os.environ["TTT_MLP_PREFILL_KERNEL"]
+        else:
+            os.environ["TTT_MLP_PREFILL_KERNEL"] = old
+
+
+@pytest.mark.parametrize("kernel", ["mma", "tc"])
+@pytest.mark.parametrize("B,H,T_,w_std,seed", [(2, 3, 16, 0.1, 1), (2, 3, 64, 0.02, 2), (2, 3, 400, 0.1, 3),
+                                               (2, 3, 1024, 0.05, 4), (4, 50, 48, 0.05, 5)])
+def test_mlp_tensor_core_shape(kernel, B, H, T_, w_std, seed):
+    # d = 64, hidden = 256, blocks of 16, bf16: the two tensor-core kernels (the last case has
+    # more CTAs than SMs)
+    x = WL.mlp_inputs(B, H, T_, 64, 256, seed=500 + seed, dtype="bf16", w_std=w_std)
+    with mlp_kernel(kernel):
+        Z, W1, W2 = run_mlp(x, 16)
     r = f64(x)
     Zr, W1r, W2r = O.mlp_dual(r["Q"], r["K"], r["V"], r["eta"], r["W1"], r["W2"], 16)
     assert rel_err(Z, Zr) <= TOL["bf16"]
@@ -200,7 +218,9 @@ def test_mlp_tensor_core_shape(T_, w_std, seed):
     assert rel_err(W2, W2r) <= TOL["bf16"]
 
 
-def test_mlp_tensor_core_in_place_split_and_deterministic():
+@pytest.mark.parametrize("kernel", ["mma", "tc"])
+def test_mlp_tensor_core_in_place_split_and_deterministic(kernel, monkeypatch):
+    monkeypatch.setenv("TTT_MLP_PREFILL_KERNEL", kernel)
     x = WL.mlp_inputs(1, 4, 128, 64, 256, seed=77, dtype="bf16", w_std=0.1)
     g = cuda(x)
     Z1, A1, B1 = T.mlp_prefill(g["Q"], g["K"], g["V"], g["eta"], g["W1"], g["W2"], 16)
