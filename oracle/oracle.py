@@ -51,6 +51,8 @@ def _load():
                 f = getattr(lib, name)
                 f.argtypes = [dp] * 9 + [i] * 6
                 f.restype = None
+            lib.oracle_linear_backward.argtypes = [dp] * 12 + [i] * 5
+            lib.oracle_linear_backward.restype = None
             lib.oracle_linear_decode.argtypes = [dp] * 6 + [i] * 3
             lib.oracle_linear_decode.restype = None
             lib.oracle_mlp_token_grad.argtypes = [dp] * 7 + [i] * 2
@@ -112,6 +114,26 @@ def linear_primal(Q, K, V, eta, W0, chunk):
 def linear_dual(Q, K, V, eta, W0, chunk):
     """Dual (matrix) form of the same scan. Returns (Z, W_final)."""
     return _linear("oracle_linear_dual", Q, K, V, eta, W0, chunk)
+
+
+def linear_backward(Q, K, V, eta, W0, dZ, dWT, chunk):
+    """Gradient of the TTT-Linear scan with respect to (Q, K, V, eta, W0), given the gradients dZ
+    of the outputs and dWT of the final state (None: zero).  Returns (dQ, dK, dV, deta, dW0)."""
+    Q, K, V, eta, W0, dZ = (_f64(a) for a in (Q, K, V, eta, W0, dZ))
+    B, H, T, d = Q.shape
+    assert K.shape == V.shape == dZ.shape == Q.shape and eta.shape == (B, H, T) and W0.shape == (B, H, d, d)
+    assert 1 <= chunk
+    dWT_p = None
+    if dWT is not None:
+        dWT = _f64(dWT)
+        assert dWT.shape == W0.shape
+        dWT_p = _p(dWT)
+    dQ, dK, dV = np.zeros_like(Q), np.zeros_like(Q), np.zeros_like(Q)
+    deta = np.zeros_like(eta)
+    dW0 = np.zeros_like(W0)
+    _load().oracle_linear_backward(_p(Q), _p(K), _p(V), _p(eta), _p(W0), _p(dZ), dWT_p, _p(dQ), _p(dK), _p(dV),
+                                   _p(deta), _p(dW0), B, H, T, d, int(chunk))
+    return dQ, dK, dV, deta, dW0
 
 
 def _mlp(fn_name, Q, K, V, eta, W1, W2, chunk):

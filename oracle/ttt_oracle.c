@@ -243,6 +243,137 @@ void oracle_linear_dual(const double *Q, const double *K, const double *V, const
 }
 
 /*
+ * Gradient of the TTT-Linear chunked scan, for training the outer model through the inner
+ * loop.  Given the gradients of a scalar loss with respect to the outputs, dZ [B][H][T][d], and
+ * to the final state, dWT [B][H][d][d] (NULL: zero), returns the gradients with respect to the
+ * inputs Q, K, V [B][H][T][d], eta [B][H][T] and W0 [B][H][d][d].
+ *
+ * The forward definitions are those of linear_dual_head (the dual form of the mini-batch step
+ * of [HP]/[ES], readings R1-R5, R7).  Their chain rule, block by block in reverse order, with
+ * W = W_n the state at the start of block n, D = diag(eta), M the causal mask (j <= i),
+ * S = Q K^T, A = (M . S) D, E = K W - V and dWn1 the gradient of the state after the block:
+ *   from W_{n+1} = W - K^T D E:  dW += dWn1;  dE += -D K dWn1;  dK += -D E dWn1^T;
+ *                                deta_j += -sum_c E_jc (K dWn1)_jc
+ *   from Z = Q W - A E:          dW += Q^T dZ;  dQ += dZ W^T;  dE += -A^T dZ;  dA = -dZ E^T
+ *   from A = (M . S) D:          dS = M . dA D;  deta_j += sum_i M_ij dA_ij S_ij
+ *   from S = Q K^T:              dQ += dS K;  dK += dS^T Q
+ *   from E = K W - V:            dK += dE W^T;  dW += K^T dE;  dV = -dE
+ * The block-start states come from a forward pass over the whole sequence first.
+ * Pinned by central finite differences of the token-level definition (linear_primal_head).
+ */
+static void linear_backward_head(const double *Q, const double *K, const double *V,
+                                 const double *eta, const double *W0, const double *dZ,
+                                 const double *dWT, double *dQ, double *dK, double *dV,
+                                 double *deta, double *dW0, int T, int d, int chunk)
+{
+    int nblk = (T + chunk - 1) / chunk;
+    size_t dd = (size_t)d * d;
+    double *Ws = xmalloc((size_t)(nblk + 1) * dd * sizeof(double)); /* W_0 .. W_nblk */
+    double *E = xmalloc((size_t)chunk * d * sizeof(double));
+    double *dE = xmalloc((size_t)chunk * d * sizeof(double));
+    double *KdW = xmalloc((size_t)chunk * d * sizeof(double));
+    double *S = xmalloc((size_t)chunk * chunk * sizeof(double));
+    double *dA = xmalloc((size_t)chunk * chunk * sizeof(double));
+    double *dW = xmalloc(dd * sizeof(double));
+    double *dWp = xmalloc(dd * sizeof(double));
+
+    /* forward: the state at the start of every block */
+    memcpy(Ws, W0, dd * sizeof(double));
+    for (int n = 0; n < nblk; ++n) {
+        int t0 = n * chunk, b = (T - t0 < chunk) ? (T - t0) : chunk;
+        const double *Kc = K + (size_t)t0 * d, *Vc = V + (size_t)t0 * d, *ec = eta + t0;
+        const double *W = Ws + (size_t)n * dd;
+        double *Wn = Ws + (size_t)(n + 1) * dd;
+        memcpy(Wn, W, dd * sizeof(double));
+        for (int j = 0; j < b; ++j) {
+            vecmat(Kc + (size_t)j * d, W, E + (size_t)j * d, d, d);
+            for (int c = 0; c < d; ++c) E[(size_t)j * d + c] -= Vc[(size_t)j * d + c];
+        }
+        for (int j = 0; j < b; ++j) rank1_sub(Wn, ec[j], &Kc[(size_t)j * d], &E[(size_t)j * d], d, d);
+    }
+
+    /* reverse */
+    if (dWT) memcpy(dW, dWT, dd * sizeof(double));
+    else memset(dW, 0, dd * sizeof(double));
+    for (int n = nblk - 1; n >= 0; --n) {
+        int t0 = n * chunk, b = (T - t0 < chunk) ? (T - t0) : chunk;
+        const double *Qc = Q + (size_t)t0 * d, *Kc = K + (size_t)t0 * d;
+        const double *Vc = V + (size_t)t0 * d, *ec = eta + t0, *dZc = dZ + (size_t)t0 * d;
+        double *dQc = dQ + (size_t)t0 * d, *dKc = dK + (size_t)t0 * d, *dVc = dV + (size_t)t0 * d;
+        double *detac = deta + t0;
+        const double *W = Ws + (size_t)n * dd; /* the state at the start of block n */
+        /* E = K W - V, S = Q K^T, K dWn1 */
+        for (int j = 0; j < b; ++j) {
+            vecmat(Kc + (size_t)j * d, W, E + (size_t)j * d, d, d);
+            for (int c = 0; c < d; ++c) E[(size_t)j * d + c] -= Vc[(size_t)j * d + c];
+            vecmat(Kc + (size_t)j * d, dW, KdW + (size_t)j * d, d, d);
+        }
+        for (int i = 0; i < b; ++i)
+            for (int j = 0; j < b; ++j) S[(size_t)i * b + j] = dot(Qc + (size_t)i * d, Kc + (size_t)j * d, d);
+        /* dA = -dZ E^T on the mask; dE = -A^T dZ - D K dWn1 */
+        for (int i = 0; i < b; ++i)
+            for (int j = 0; j < b; ++j)
+                dA[(size_t)i * b + j] = (j <= i) ? -dot(dZc + (size_t)i * d, E + (size_t)j * d, d) : 0.0;
+        for (int j = 0; j < b; ++j)
+            for (int c = 0; c < d; ++c) {
+                double acc = -ec[j] * KdW[(size_t)j * d + c];
+                for (int i = j; i < b; ++i) acc -= S[(size_t)i * b + j] * ec[j] * dZc[(size_t)i * d + c];
+                dE[(size_t)j * d + c] = acc;
+            }
+        /* dQ = dZ W^T + dS K, with dS = M . dA D */
+        for (int i = 0; i < b; ++i)
+            for (int k = 0; k < d; ++k) {
+                double acc = dot(dZc + (size_t)i * d, W + (size_t)k * d, d);
+                for (int j = 0; j <= i; ++j) acc += dA[(size_t)i * b + j] * ec[j] * Kc[(size_t)j * d + k];
+                dQc[(size_t)i * d + k] = acc;
+            }
+        /* dK = dE W^T - D E dWn1^T + dS^T Q;  dV = -dE;  deta */
+        for (int j = 0; j < b; ++j) {
+            for (int k = 0; k < d; ++k) {
+                double acc = dot(dE + (size_t)j * d, W + (size_t)k * d, d);
+                acc -= ec[j] * dot(E + (size_t)j * d, dW + (size_t)k * d, d);
+                for (int i = j; i < b; ++i) acc += dA[(size_t)i * b + j] * ec[j] * Qc[(size_t)i * d + k];
+                dKc[(size_t)j * d + k] = acc;
+            }
+            for (int c = 0; c < d; ++c) dVc[(size_t)j * d + c] = -dE[(size_t)j * d + c];
+            double de = -dot(E + (size_t)j * d, KdW + (size_t)j * d, d);
+            for (int i = j; i < b; ++i) de += dA[(size_t)i * b + j] * S[(size_t)i * b + j];
+            detac[j] = de;
+        }
+        /* dW_n = dWn1 + Q^T dZ + K^T dE */
+        memcpy(dWp, dW, dd * sizeof(double));
+        for (int i = 0; i < b; ++i) {
+            rank1_sub(dWp, -1.0, Qc + (size_t)i * d, dZc + (size_t)i * d, d, d);
+            rank1_sub(dWp, -1.0, Kc + (size_t)i * d, dE + (size_t)i * d, d, d);
+        }
+        memcpy(dW, dWp, dd * sizeof(double));
+    }
+    memcpy(dW0, dW, dd * sizeof(double));
+    free(Ws);
+    free(E);
+    free(dE);
+    free(KdW);
+    free(S);
+    free(dA);
+    free(dW);
+    free(dWp);
+}
+
+void oracle_linear_backward(const double *Q, const double *K, const double *V, const double *eta,
+                            const double *W0, const double *dZ, const double *dWT, double *dQ,
+                            double *dK, double *dV, double *deta, double *dW0, int B, int H, int T,
+                            int d, int chunk)
+{
+    long BH = (long)B * H;
+    size_t td = (size_t)T * d, dd = (size_t)d * d;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (long bh = 0; bh < BH; ++bh)
+        linear_backward_head(Q + bh * td, K + bh * td, V + bh * td, eta + bh * (size_t)T, W0 + bh * dd,
+                             dZ + bh * td, dWT ? dWT + bh * dd : NULL, dQ + bh * td, dK + bh * td,
+                             dV + bh * td, deta + bh * (size_t)T, dW0 + bh * dd, T, d, chunk);
+}
+
+/*
  * One online step (b = 1) for every (batch, head), in place on W:
  *   e = k W - v;  W <- W - eta k^T e;  z = q W.
  * This is the per-token loop of [CM]/[MF] applied to a single token.

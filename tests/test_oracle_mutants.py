@@ -58,6 +58,20 @@ MUTANTS = [
      "for (int c = 0; c < d; ++c) e2[c] += Vc[(size_t)i * d + c];"),
     ("MLP primal W2 step uses the pre-activation", "rank1_sub(W2, eta[i], a, e2, hd, d);  /* W2 -= eta a^T e2 */",
      "rank1_sub(W2, eta[i], e1, e2, hd, d);  /* W2 -= eta a^T e2 */"),
+    ("backward dE drops the read-out term", "for (int i = j; i < b; ++i) acc -= S[(size_t)i * b + j] * ec[j]",
+     "for (int i = j; i < b; ++i) acc -= 0.0 * S[(size_t)i * b + j] * ec[j]"),
+    ("backward dK drops the state-update term", "acc -= ec[j] * dot(E + (size_t)j * d, dW + (size_t)k * d, d);",
+     "acc -= 0.0 * ec[j] * dot(E + (size_t)j * d, dW + (size_t)k * d, d);"),
+    ("backward deta update term sign", "double de = -dot(E + (size_t)j * d, KdW + (size_t)j * d, d);",
+     "double de = dot(E + (size_t)j * d, KdW + (size_t)j * d, d);"),
+    ("backward mask drops the diagonal", "dA[(size_t)i * b + j] = (j <= i) ?", "dA[(size_t)i * b + j] = (j < i) ?"),
+    ("backward dW drops K^T dE", "rank1_sub(dWp, -1.0, Kc + (size_t)i * d, dE + (size_t)i * d, d, d);",
+     "rank1_sub(dWp, -0.0, Kc + (size_t)i * d, dE + (size_t)i * d, d, d);"),
+    ("backward uses the state after the block",
+     "const double *W = Ws + (size_t)n * dd; /* the state at the start of block n */",
+     "const double *W = Ws + (size_t)(n + 1) * dd; /* the state at the start of block n */"),
+    ("backward dQ scores term uses the query's eta", "acc += dA[(size_t)i * b + j] * ec[j] * Kc[(size_t)j * d + k];",
+     "acc += dA[(size_t)i * b + j] * ec[i] * Kc[(size_t)j * d + k];"),
 ]
 
 
@@ -214,8 +228,35 @@ def pin_mlp_online_gd(M):
     return _rel(A1[0, 0], A) < 1e-12 and _rel(A2[0, 0], Bm) < 1e-12
 
 
+def pin_backward_finite_differences(M):
+    # gradient of L = sum(dZ . Z) + sum(dWT . W_T), Z and W_T from the token-level definition
+    rng = np.random.default_rng(10)
+    Q, K, V, eta, W0 = _lin(1, 1, 5, 3, 10)
+    dZ, dWT = rng.standard_normal(Q.shape), rng.standard_normal(W0.shape)
+    for chunk in (2, 5):
+        g = M.linear_backward(Q, K, V, eta, W0, dZ, dWT, chunk)
+        args = [Q, K, V, eta, W0]
+
+        def L(*a):
+            Z, W = M.linear_primal(*a, chunk)
+            return float(np.sum(dZ * Z) + np.sum(dWT * W))
+
+        for ai, a in enumerate(args):
+            fd = np.zeros_like(a)
+            for idx in np.ndindex(a.shape):
+                ap = [x.copy() for x in args]
+                am = [x.copy() for x in args]
+                ap[ai][idx] += 1e-5
+                am[ai][idx] -= 1e-5
+                fd[idx] = (L(*ap) - L(*am)) / 2e-5
+            if np.max(np.abs(g[ai] - fd)) > 1e-7 * max(1.0, np.max(np.abs(fd))):
+                return False
+    return True
+
+
 PINS = [pin_golden, pin_primal_dual, pin_linear_attention, pin_delta_rule, pin_consistent_targets,
-        pin_mlp_kernelised_attention, pin_mlp_finite_differences, pin_gelu, pin_mlp_online_gd]
+        pin_mlp_kernelised_attention, pin_mlp_finite_differences, pin_gelu, pin_mlp_online_gd,
+        pin_backward_finite_differences]
 
 
 def _bind(src_text, tmpdir, tag):
