@@ -305,6 +305,55 @@ def bench_mlp(T_mod, w, steps, warmup, world, peaks):
             "frac": max(t_tensor, t_hbm) / (ms_launch * 1e-3), "bound": "tensor" if t_tensor > t_hbm else "hbm"}
 
 
+def backward_bytes(B, H, T, d, chunk, elt=2):
+    """Backward pass: Q,K,V,dZ read and dQ,dK,dV written (elt bytes each), eta read and deta written,
+    the block-start states read once, dW_T read and dW0 written."""
+    nblk = -(-T // chunk)
+    return B * H * (T * (7 * d * elt + 8) + nblk * d * d * 4 + 2 * d * d * 4)
+
+
+def backward_flops(B, H, T, d, chunk):
+    """Per head-token: E, K dW', dQ's dZ W^T, dK's two d x d products and the two rank updates of dW
+    (2 d^2 each, 7 in all) plus the causal score products S, dA, dE, dQ, dK ((b + 1) d each, 5)."""
+    return B * H * T * (14 * d * d + 5 * (chunk + 1) * d)
+
+
+def bench_backward(T_mod, w, steps, warmup, world, peaks, nrot=2):
+    """Training step of the headline shape: the forward that records the block-start states, then
+    the backward; both timed, each on its own launches."""
+    x = WL.workload_inputs(w)
+    g = WL.backward_inputs(w.B, w.H, w.T, w.d, seed=w.seed + 100, dtype=w.dtype)
+    sets = rotating_copies({**x, "dZ": g["dZ"], "dWT": g["dWT"]}, nrot)
+    nblk = -(-w.T // w.chunk)
+    hist = [torch.empty((w.B, w.H, nblk, w.d, w.d), dtype=torch.float32, device="cuda") for _ in range(nrot)]
+    fwd_out = [(torch.empty_like(s["Q"]), torch.empty_like(s["W0"])) for s in sets]
+    bwd_out = [(torch.empty_like(s["Q"]), torch.empty_like(s["Q"]), torch.empty_like(s["Q"]),
+                torch.empty_like(s["eta"]), torch.empty_like(s["W0"])) for s in sets]
+
+    def fwd(i):
+        s, (Z, W) = sets[i % nrot], fwd_out[i % nrot]
+        T_mod.ttt_linear_prefill_hist(s["Q"], s["K"], s["V"], s["eta"], s["W0"], Z, W, hist[i % nrot], w.chunk)
+
+    def bwd(i):
+        s, o = sets[i % nrot], bwd_out[i % nrot]
+        T_mod.ttt_linear_prefill_backward(s["Q"], s["K"], s["V"], s["eta"], hist[i % nrot], s["dZ"], s["dWT"],
+                                          *o, w.chunk)
+
+    for i in range(nrot):
+        fwd(i)
+    ms_f, ms_f_launch = timed_loop(fwd, steps, warmup, world)
+    ms_b, ms_b_launch = timed_loop(bwd, steps, warmup, world)
+    nbytes = backward_bytes(w.B, w.H, w.T, w.d, w.chunk)
+    flops = backward_flops(w.B, w.H, w.T, w.d, w.chunk)
+    t_roof = max(nbytes / (peaks["hbm_gbs"] * 1e9), flops / (peaks["bf16_tflops"] * 1e12))
+    del sets, hist, fwd_out, bwd_out
+    return {"tokens_per_s": w.B * w.T / ((ms_f + ms_b) * 1e-3), "ms_per_step": ms_f + ms_b,
+            "forward_hist_ms_per_launch": ms_f_launch, "backward_ms_per_launch": ms_b_launch,
+            "backward_bytes_per_launch": nbytes, "backward_flops_per_launch": flops,
+            "backward_roofline_us": t_roof * 1e6, "backward_frac": t_roof / (ms_b_launch * 1e-3),
+            "bound": "hbm" if nbytes / (peaks["hbm_gbs"] * 1e9) > flops / (peaks["bf16_tflops"] * 1e12) else "tensor"}
+
+
 def bench_decode(T_mod, w, steps, warmup, world, peaks, graph_steps=1024, nrot=NROT):
     """A CUDA graph of `graph_steps` decode steps; `nrot` state copies rotate so the state streams from HBM."""
     x = WL.decode_inputs(w.B, w.H, w.d, graph_steps, w.seed)
@@ -459,6 +508,8 @@ def run_ours(args):
         if want("mlp_decode"):
             wd = WL.WORKLOADS["mlp_decode"]
             rows["mlp_decode"] = bench_mlp_decode(T_mod, wd, max(3, rsteps // 5), args.warmup, world, peaks)
+        if want("backward"):
+            rows["linear_backward"] = bench_backward(T_mod, w, max(3, rsteps // 5), args.warmup, world, peaks)
         line["rows"] = rows
     if rank == 0 and world == 1 and not args.no_cpu:
         line["cpu_baseline"] = cpu_baseline(w)
@@ -510,7 +561,8 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--rows", choices=["all", "none", "mlp_prefill", "long_context", "decode", "mlp_decode"],
+    ap.add_argument("--rows", choices=["all", "none", "mlp_prefill", "long_context", "decode", "mlp_decode",
+                                       "backward"],
                     default="all",
                     help="workload rows timed after the headline (default: all)")
     ap.add_argument("--no-e2e", action="store_true")

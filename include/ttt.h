@@ -101,6 +101,56 @@ ttt_status ttt_linear_prefill(const void* Q, const void* K, const void* V, const
                               int chunk, ttt_dtype dtype, void* stream);
 
 /*
+ * TTT-Linear prefill that also records the state at the start of every block
+ * (the values ttt_linear_prefill_backward needs).  Same arguments and results
+ * as ttt_linear_prefill, plus:
+ *
+ *   W_hist   [B][H][nblk][d][d]  fp32  written: W_hist[b][h][n] = the state at
+ *                                      the start of block n (n = 0: W0),
+ *                                      nblk = ceil(T / chunk)
+ *
+ * W_hist must not overlap any other argument.  Runs the SIMT fp32 kernel for
+ * every shape (slower than ttt_linear_prefill on its tensor-core shapes).
+ * Source: as ttt_linear_prefill; the saved states serve the gradient below.
+ */
+ttt_status ttt_linear_prefill_hist(const void* Q, const void* K, const void* V, const float* eta,
+                                   const float* W0, void* Z, float* W_out, float* W_hist, int B, int H,
+                                   int T, int d, int chunk, ttt_dtype dtype, void* stream);
+
+/*
+ * Gradient of the TTT-Linear prefill, for training the outer model through the
+ * inner loop (the slow weights learn the initialisation and the update rule:
+ * TTT essay, ren-xubin.github.io, paragraph on the two time scales).  Given the
+ * gradients of a scalar loss with respect to the outputs Z and to the final
+ * state, returns them with respect to Q, K, V, eta and W0:
+ *
+ *   Q, K, V     [B][H][T][d]        dtype   the forward inputs
+ *   eta         [B][H][T]           fp32
+ *   W_hist      [B][H][nblk][d][d]  fp32    block-start states from ttt_linear_prefill_hist
+ *   dZ          [B][H][T][d]        dtype   dL/dZ
+ *   dW_T        [B][H][d][d]        fp32    dL/dW_out, or NULL for zero
+ *   dQ, dK, dV  [B][H][T][d]        dtype   written: dL/dQ, dL/dK, dL/dV
+ *   deta        [B][H][T]           fp32    written: dL/deta
+ *   dW0         [B][H][d][d]        fp32    written: dL/dW0 (may be the same buffer as dW_T)
+ *   chunk       1..512 with the block tiles in shared memory: (2 d (d+1) + 7 chunk (d+1)
+ *               + 2 chunk (chunk+1) + chunk) * 4 bytes <= 227 KB (d = 64: chunk <= 64;
+ *               d = 128: chunk <= 16), else TTT_ERR_UNSUPPORTED
+ *   d           16, 32, 64 or 128
+ *
+ * Per block, reverse order (D = diag(eta), M the causal mask, S = Q K^T,
+ * A = (M . S) D, E = K W - V, dW' the gradient of the state after the block):
+ *   dE = -A^T dZ - D K dW',  dA = -dZ E^T,  dQ = dZ W^T + (M . dA D) K,
+ *   dK = dE W^T - D E dW'^T + (M . dA D)^T Q,  dV = -dE,
+ *   deta_j = -sum_c E_jc (K dW')_jc + sum_i M_ij dA_ij S_ij,
+ *   dW = dW' + Q^T dZ + K^T dE.
+ * Accumulation in fp32; outputs rounded to dtype (RN-even).
+ */
+ttt_status ttt_linear_prefill_backward(const void* Q, const void* K, const void* V, const float* eta,
+                                       const float* W_hist, const void* dZ, const float* dW_T, void* dQ,
+                                       void* dK, void* dV, float* deta, float* dW0, int B, int H, int T,
+                                       int d, int chunk, ttt_dtype dtype, void* stream);
+
+/*
  * TTT-MLP prefill: f(x; W1, W2) = GELU(x W1) W2 with the tanh form of GELU,
  * no biases.  Per block, with start state (W1, W2):
  *

@@ -122,6 +122,74 @@ ttt_status ttt_linear_prefill(const void* Q, const void* K, const void* V, const
     return TTT_OK;
 }
 
+ttt_status ttt_linear_prefill_hist(const void* Q, const void* K, const void* V, const float* eta, const float* W0,
+                                   void* Z, float* W_out, float* W_hist, int B, int H, int T, int d, int chunk,
+                                   ttt_dtype dtype, void* stream) {
+    g_last_error[0] = 0;
+    if (B < 0 || H < 0 || T < 0) return fail(TTT_ERR_INVALID_ARG, "negative size%s");
+    if (chunk < 1 || chunk > 512) return fail(TTT_ERR_INVALID_ARG, "chunk must be in 1..512%s");
+    if (dtype != TTT_F32 && dtype != TTT_BF16) return fail(TTT_ERR_INVALID_ARG, "unknown dtype%s");
+    if (d <= 0) return fail(TTT_ERR_INVALID_ARG, "head dim must be positive%s");
+    if (!supported_d(d)) return fail(TTT_ERR_UNSUPPORTED, "head dim must be 16, 32, 64 or 128%s");
+    if (size_t(B) * H == 0) return TTT_OK;
+    if (T == 0) return ttt_linear_prefill(Q, K, V, eta, W0, Z, W_out, B, H, T, d, chunk, dtype, stream);
+    CHECK_PTR(Q);
+    CHECK_PTR(K);
+    CHECK_PTR(V);
+    CHECK_PTR(eta);
+    CHECK_PTR(W0);
+    CHECK_PTR(Z);
+    CHECK_PTR(W_out);
+    CHECK_PTR(W_hist);
+    ttt::LinearArgs a{Q, K, V, eta, W0, Z, W_out, B, H, T, d, chunk, dtype == TTT_BF16 ? 1 : 0};
+    a.W_hist = W_hist;
+    // the generic kernel writes the block-start states
+    cudaError_t e = ttt::launch_linear_prefill_generic(a, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "ttt_linear_prefill_hist launch");
+    return TTT_OK;
+}
+
+ttt_status ttt_linear_prefill_backward(const void* Q, const void* K, const void* V, const float* eta,
+                                       const float* W_hist, const void* dZ, const float* dW_T, void* dQ, void* dK,
+                                       void* dV, float* deta, float* dW0, int B, int H, int T, int d, int chunk,
+                                       ttt_dtype dtype, void* stream) {
+    g_last_error[0] = 0;
+    if (B < 0 || H < 0 || T < 0) return fail(TTT_ERR_INVALID_ARG, "negative size%s");
+    if (chunk < 1 || chunk > 512) return fail(TTT_ERR_INVALID_ARG, "chunk must be in 1..512%s");
+    if (dtype != TTT_F32 && dtype != TTT_BF16) return fail(TTT_ERR_INVALID_ARG, "unknown dtype%s");
+    if (d <= 0) return fail(TTT_ERR_INVALID_ARG, "head dim must be positive%s");
+    if (!supported_d(d)) return fail(TTT_ERR_UNSUPPORTED, "head dim must be 16, 32, 64 or 128%s");
+    if (!ttt::linear_backward_supported(d, chunk))
+        return fail(TTT_ERR_UNSUPPORTED, "backward: the block tiles of this chunk and head dim exceed shared memory%s");
+    if (size_t(B) * H == 0) return TTT_OK;
+    CHECK_PTR(dW0);
+    if (dW_T && !aligned16(dW_T)) return fail(TTT_ERR_INVALID_ARG, "pointer not 16-byte aligned: %s", "dW_T");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (T == 0) {  // no tokens: the state passes through unchanged
+        const size_t bytes = size_t(B) * H * d * d * sizeof(float);
+        cudaError_t e = dW_T ? (dW_T != dW0 ? cudaMemcpyAsync(dW0, dW_T, bytes, cudaMemcpyDeviceToDevice, s)
+                                            : cudaSuccess)
+                             : cudaMemsetAsync(dW0, 0, bytes, s);
+        if (e != cudaSuccess) return cuda_fail(e, "ttt_linear_prefill_backward copy");
+        return TTT_OK;
+    }
+    CHECK_PTR(Q);
+    CHECK_PTR(K);
+    CHECK_PTR(V);
+    CHECK_PTR(eta);
+    CHECK_PTR(W_hist);
+    CHECK_PTR(dZ);
+    CHECK_PTR(dQ);
+    CHECK_PTR(dK);
+    CHECK_PTR(dV);
+    CHECK_PTR(deta);
+    ttt::LinearBwdArgs a{Q, K, V, eta, W_hist, dZ, dW_T, dQ, dK, dV, deta, dW0, B, H, T, d, chunk,
+                         dtype == TTT_BF16 ? 1 : 0};
+    cudaError_t e = ttt::launch_linear_backward(a, s);
+    if (e != cudaSuccess) return cuda_fail(e, "ttt_linear_prefill_backward launch");
+    return TTT_OK;
+}
+
 ttt_status ttt_mlp_prefill(const void* Q, const void* K, const void* V, const float* eta, const float* W1_0,
                            const float* W2_0, void* Z, float* W1_out, float* W2_out, int B, int H, int T, int d,
                            int hidden, int chunk, ttt_dtype dtype, void* stream) {
@@ -258,6 +326,6 @@ const char* ttt_status_string(ttt_status s) {
 
 const char* ttt_last_error(void) { return g_last_error; }
 
-int ttt_version(void) { return 10100; }
+int ttt_version(void) { return 10200; }
 
 }  // extern "C"

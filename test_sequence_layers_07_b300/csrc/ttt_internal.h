@@ -18,7 +18,26 @@ struct LinearArgs {
     void* Z;
     float* W_out;
     int B, H, T, d, chunk;
-    int bf16;  // 1: Q/K/V/Z are bfloat16, 0: float32
+    int bf16;                // 1: Q/K/V/Z are bfloat16, 0: float32
+    float* W_hist = nullptr;  // optional: the state at the start of every block, [B][H][nblk][d][d]
+};
+
+// Gradient of the TTT-Linear chunked scan (outer-loop training).
+struct LinearBwdArgs {
+    const void* Q;
+    const void* K;
+    const void* V;
+    const float* eta;
+    const float* W_hist;  // [B][H][nblk][d][d], the state at the start of every block
+    const void* dZ;
+    const float* dW_T;    // gradient of the final state, or nullptr (zero)
+    void* dQ;
+    void* dK;
+    void* dV;
+    float* deta;
+    float* dW0;
+    int B, H, T, d, chunk;
+    int bf16;  // 1: Q/K/V/dZ/dQ/dK/dV are bfloat16, 0: float32
 };
 
 struct MlpArgs {
@@ -57,6 +76,11 @@ struct MlpDecodeArgs {
     int B, H, d, hidden;
     int bf16;
 };
+
+// Backward of the TTT-Linear scan (SIMT, fp32, one CTA per head).  bwd_supported says whether the
+// block tiles of (d, chunk) fit in shared memory.
+bool linear_backward_supported(int d, int chunk);
+cudaError_t launch_linear_backward(const LinearBwdArgs& a, cudaStream_t s);
 
 // Generic SIMT kernels: every supported shape, fp32 accumulation.
 cudaError_t launch_linear_prefill_generic(const LinearArgs& a, cudaStream_t s);

@@ -25,7 +25,8 @@ LIB_PATH = os.path.join(_PKG, "libttt.so")
 TTT_OK, TTT_ERR_INVALID_ARG, TTT_ERR_UNSUPPORTED, TTT_ERR_CUDA, TTT_ERR_TIMEOUT = range(5)
 TTT_F32, TTT_BF16 = 0, 1
 
-EXPORTED = ("ttt_linear_prefill", "ttt_mlp_prefill", "ttt_linear_decode_step", "ttt_mlp_decode_step",
+EXPORTED = ("ttt_linear_prefill", "ttt_linear_prefill_hist", "ttt_linear_prefill_backward", "ttt_mlp_prefill",
+            "ttt_linear_decode_step", "ttt_mlp_decode_step",
             "ttt_get_device_status", "ttt_selftest_wait_timeout", "ttt_status_string", "ttt_last_error", "ttt_version")
 
 
@@ -51,13 +52,17 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
             lib = ctypes.CDLL(path)
             vp, fp, i = ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int
             lib.ttt_linear_prefill.argtypes = [vp, vp, vp, fp, fp, vp, fp, i, i, i, i, i, i, vp]
+            lib.ttt_linear_prefill_hist.argtypes = [vp, vp, vp, fp, fp, vp, fp, fp, i, i, i, i, i, i, vp]
+            lib.ttt_linear_prefill_backward.argtypes = [vp, vp, vp, fp, fp, vp, fp, vp, vp, vp, fp, fp,
+                                                        i, i, i, i, i, i, vp]
             lib.ttt_mlp_prefill.argtypes = [vp, vp, vp, fp, fp, fp, vp, fp, fp, i, i, i, i, i, i, i, vp]
             lib.ttt_linear_decode_step.argtypes = [vp, vp, vp, fp, fp, vp, i, i, i, i, vp]
             lib.ttt_mlp_decode_step.argtypes = [vp, vp, vp, fp, fp, fp, vp, i, i, i, i, i, vp]
             lib.ttt_get_device_status.argtypes = [vp]
             lib.ttt_selftest_wait_timeout.argtypes = [ctypes.c_uint64, vp]
             lib.ttt_selftest_wait_timeout.restype = i
-            for f in (lib.ttt_linear_prefill, lib.ttt_mlp_prefill, lib.ttt_linear_decode_step,
+            for f in (lib.ttt_linear_prefill, lib.ttt_linear_prefill_hist, lib.ttt_linear_prefill_backward,
+                      lib.ttt_mlp_prefill, lib.ttt_linear_decode_step,
                       lib.ttt_mlp_decode_step, lib.ttt_get_device_status):
                 f.restype = i
             lib.ttt_status_string.argtypes = [i]
@@ -117,6 +122,48 @@ def ttt_linear_prefill(Q, K, V, eta, W0, Z, W_out, chunk: int, stream=None) -> N
     st = load_library().ttt_linear_prefill(
         _ptr(Q, "Q"), _ptr(K, "K"), _ptr(V, "V"), _ptr(eta, "eta", torch.float32), _ptr(W0, "W0", torch.float32),
         _ptr(Z, "Z"), _ptr(W_out, "W_out", torch.float32), B, H, T, d, int(chunk), dt, _stream(stream))
+    _check(st)
+
+
+def ttt_linear_prefill_hist(Q, K, V, eta, W0, Z, W_out, W_hist, chunk: int, stream=None) -> None:
+    """TTT-Linear prefill that also writes the state at the start of every block into
+    W_hist [B,H,ceil(T/chunk),d,d] fp32 (the input of the backward)."""
+    B, H, T, d = Q.shape
+    dt = _io_dtype(Q)
+    for name, t in (("K", K), ("V", V), ("Z", Z)):
+        if t.shape != Q.shape or t.dtype != Q.dtype:
+            raise ValueError(f"{name} must match Q in shape and dtype")
+    nblk = -(-T // int(chunk)) if chunk > 0 else 0
+    if eta.shape != (B, H, T) or W0.shape != (B, H, d, d) or W_out.shape != (B, H, d, d):
+        raise ValueError("eta must be [B,H,T] and W0/W_out [B,H,d,d]")
+    if W_hist.shape != (B, H, nblk, d, d):
+        raise ValueError("W_hist must be [B,H,ceil(T/chunk),d,d]")
+    st = load_library().ttt_linear_prefill_hist(
+        _ptr(Q, "Q"), _ptr(K, "K"), _ptr(V, "V"), _ptr(eta, "eta", torch.float32), _ptr(W0, "W0", torch.float32),
+        _ptr(Z, "Z"), _ptr(W_out, "W_out", torch.float32), _ptr(W_hist, "W_hist", torch.float32),
+        B, H, T, d, int(chunk), dt, _stream(stream))
+    _check(st)
+
+
+def ttt_linear_prefill_backward(Q, K, V, eta, W_hist, dZ, dW_T, dQ, dK, dV, deta, dW0, chunk: int,
+                                stream=None) -> None:
+    """Gradient of the TTT-Linear prefill: dQ, dK, dV [B,H,T,d] (dtype of Q), deta [B,H,T] and
+    dW0 [B,H,d,d] (fp32) from dZ and dW_T (None: zero)."""
+    B, H, T, d = Q.shape
+    dt = _io_dtype(Q)
+    for name, t in (("K", K), ("V", V), ("dZ", dZ), ("dQ", dQ), ("dK", dK), ("dV", dV)):
+        if t.shape != Q.shape or t.dtype != Q.dtype:
+            raise ValueError(f"{name} must match Q in shape and dtype")
+    nblk = -(-T // int(chunk)) if chunk > 0 else 0
+    if eta.shape != (B, H, T) or deta.shape != (B, H, T) or dW0.shape != (B, H, d, d):
+        raise ValueError("eta/deta must be [B,H,T] and dW0 [B,H,d,d]")
+    if W_hist.shape != (B, H, nblk, d, d) or (dW_T is not None and dW_T.shape != (B, H, d, d)):
+        raise ValueError("W_hist must be [B,H,ceil(T/chunk),d,d] and dW_T [B,H,d,d]")
+    st = load_library().ttt_linear_prefill_backward(
+        _ptr(Q, "Q"), _ptr(K, "K"), _ptr(V, "V"), _ptr(eta, "eta", torch.float32),
+        _ptr(W_hist, "W_hist", torch.float32), _ptr(dZ, "dZ"), _ptr(dW_T, "dW_T", torch.float32), _ptr(dQ, "dQ"),
+        _ptr(dK, "dK"), _ptr(dV, "dV"), _ptr(deta, "deta", torch.float32), _ptr(dW0, "dW0", torch.float32),
+        B, H, T, d, int(chunk), dt, _stream(stream))
     _check(st)
 
 
@@ -189,6 +236,25 @@ def linear_prefill(Q, K, V, eta, W0, chunk: int, stream=None):
     W = torch.empty_like(W0)
     ttt_linear_prefill(Q, K, V, eta, W0, Z, W, chunk, stream)
     return Z, W
+
+
+def linear_prefill_hist(Q, K, V, eta, W0, chunk: int, stream=None):
+    """Returns (Z, W_final, W_hist) for a TTT-Linear prefill that records the block-start states."""
+    B, H, T, d = Q.shape
+    Z = torch.empty_like(Q)
+    W = torch.empty_like(W0)
+    Wh = torch.empty((B, H, -(-T // int(chunk)), d, d), dtype=torch.float32, device=Q.device)
+    ttt_linear_prefill_hist(Q, K, V, eta, W0, Z, W, Wh, chunk, stream)
+    return Z, W, Wh
+
+
+def linear_prefill_backward(Q, K, V, eta, W_hist, dZ, dW_T, chunk: int, stream=None):
+    """Returns (dQ, dK, dV, deta, dW0) of the TTT-Linear prefill."""
+    dQ, dK, dV = torch.empty_like(Q), torch.empty_like(Q), torch.empty_like(Q)
+    deta = torch.empty_like(eta)
+    dW0 = torch.empty(W_hist.shape[:2] + W_hist.shape[3:], dtype=torch.float32, device=Q.device)
+    ttt_linear_prefill_backward(Q, K, V, eta, W_hist, dZ, dW_T, dQ, dK, dV, deta, dW0, chunk, stream)
+    return dQ, dK, dV, deta, dW0
 
 
 def mlp_prefill(Q, K, V, eta, W1, W2, chunk: int, stream=None):

@@ -170,6 +170,16 @@ def mlp_decode_inputs(B, H, d, hidden, steps, seed, dtype="bf16", w_std=0.02, bl
     return {"W1": W1, "W2": W2, "q": torch.cat(qs), "k": torch.cat(ks), "v": torch.cat(vs), "eta": torch.cat(es)}
 
 
+def backward_inputs(B, H, T, d, seed, dtype="bf16", with_dWT=True):
+    """Incoming gradients of a TTT-Linear backward: dZ [B,H,T,d] ~ N(0, 1/d) in `dtype` and
+    dW_T [B,H,d,d] ~ N(0, 1/d) fp32 (or None), from their own seed."""
+    rng = np.random.default_rng(seed)
+    s = 1.0 / np.sqrt(d)
+    dZ = round_to(rng.standard_normal((B, H, T, d)) * s, dtype)
+    dWT = round_to(rng.standard_normal((B, H, d, d)) * s, "f32") if with_dWT else None
+    return {"dZ": dZ, "dWT": dWT}
+
+
 def workload_inputs(w: Workload, chunk: int | None = None, seed_offset: int = 0):
     """Inputs of a named workload (prefill kinds)."""
     if w.hidden:

@@ -91,6 +91,43 @@ def test_linear_prefill_validation(lib):
     assert lp(lib, Q=NULL, K=NULL, V=NULL, eta=NULL, W0=NULL, Z=NULL, Wo=NULL, H=0) == T.TTT_OK
 
 
+def test_linear_prefill_hist_validation(lib):
+    def hp(Q=A, K=A, V=A, eta=A, W0=A, Z=A, Wo=A, Wh=A, B_=1, H=1, T_=16, d=64, chunk=16, dt=1):
+        return lib.ttt_linear_prefill_hist(Q, K, V, eta, W0, Z, Wo, Wh, B_, H, T_, d, chunk, dt, None)
+
+    assert hp(Wh=NULL) == T.TTT_ERR_INVALID_ARG
+    assert b"W_hist" in lib.ttt_last_error()
+    assert hp(Wh=MIS) == T.TTT_ERR_INVALID_ARG
+    assert hp(K=NULL) == T.TTT_ERR_INVALID_ARG
+    assert hp(chunk=0) == T.TTT_ERR_INVALID_ARG
+    assert hp(d=48) == T.TTT_ERR_UNSUPPORTED
+    assert hp(Q=NULL, K=NULL, V=NULL, eta=NULL, W0=NULL, Z=NULL, Wo=NULL, Wh=NULL, B_=0) == T.TTT_OK
+
+
+def test_linear_backward_validation(lib):
+    def bp(Q=A, K=A, V=A, eta=A, Wh=A, dZ=A, dWT=A, dQ=A, dK=A, dV=A, de=A, dW0=A, B_=1, H=1, T_=16, d=64,
+           chunk=16, dt=1):
+        return lib.ttt_linear_prefill_backward(Q, K, V, eta, Wh, dZ, dWT, dQ, dK, dV, de, dW0, B_, H, T_, d,
+                                               chunk, dt, None)
+
+    assert bp(dZ=NULL) == T.TTT_ERR_INVALID_ARG
+    assert b"dZ" in lib.ttt_last_error()
+    assert bp(Wh=NULL) == T.TTT_ERR_INVALID_ARG
+    assert bp(de=MIS) == T.TTT_ERR_INVALID_ARG
+    assert bp(dWT=MIS) == T.TTT_ERR_INVALID_ARG
+    assert bp(dW0=NULL) == T.TTT_ERR_INVALID_ARG
+    assert bp(B_=-1) == T.TTT_ERR_INVALID_ARG
+    assert bp(chunk=513) == T.TTT_ERR_INVALID_ARG
+    assert bp(dt=3) == T.TTT_ERR_INVALID_ARG
+    assert bp(d=96) == T.TTT_ERR_UNSUPPORTED
+    # block tiles beyond shared memory: d = 64 takes chunk <= 64, d = 128 chunk <= 16
+    assert bp(chunk=128) == T.TTT_ERR_UNSUPPORTED
+    assert bp(d=128, chunk=32) == T.TTT_ERR_UNSUPPORTED
+    assert b"shared memory" in lib.ttt_last_error()
+    assert bp(Q=NULL, K=NULL, V=NULL, eta=NULL, Wh=NULL, dZ=NULL, dWT=NULL, dQ=NULL, dK=NULL, dV=NULL, de=NULL,
+              dW0=NULL, H=0) == T.TTT_OK
+
+
 def test_mlp_prefill_validation(lib):
     def mp(**kw):
         a = dict(Q=A, K=A, V=A, eta=A, W1=A, W2=A, Z=A, W1o=A, W2o=A, B_=1, H=1, T_=16, d=64, hd=256, chunk=16,
