@@ -88,12 +88,14 @@ struct Cfg {
     static constexpr int THREADS = 32 * (2 * CG + 2);
 };
 
-template <int D, int CG, int NST, int SPS, int NX, bool SINGLE>
+// HIST: also write the state at the start of every block to W_hist [B*H][T/chunk][D][D]
+// (the values the backward needs); instantiated for blocks of 16 tokens only.
+template <int D, int CG, int NST, int SPS, int NX, bool SINGLE, bool HIST>
 __global__ void __launch_bounds__(Cfg<D, CG, NST, SPS, NX>::THREADS, 1)
 linear_prefill_mma_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                           const __grid_constant__ CUtensorMap tmV, const float* __restrict__ eta,
                           const float* W0, __nv_bfloat16* __restrict__ Z, float* W_out, int T, int chunk,
-                          int* status) {
+                          int* status, float* __restrict__ W_hist) {
     using C = Cfg<D, CG, NST, SPS, NX>;
     constexpr int KS = C::KS, NT = C::NT;
 
@@ -264,7 +266,20 @@ linear_prefill_mma_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_
                 // one 16-token sub-block of the recurrence
                 auto step = [&](int i) {
                     const int sb = si * SPS + i;
-                    if (SINGLE || sb % nsub == 0) pack_state<KS>(w, wa0);
+                    if (SINGLE || sb % nsub == 0) {
+                        if constexpr (HIST) {  // the state at the start of block sb / nsub
+                            float* wh = W_hist + (bh * size_t(nsb / nsub) + sb / nsub) * D * D;
+#pragma unroll
+                            for (int nt = 0; nt < NT; ++nt) {
+                                const int r = 8 * nt + 2 * t;
+                                wh[size_t(r) * D + cw0 + g] = w[nt][0];
+                                wh[size_t(r + 1) * D + cw0 + g] = w[nt][1];
+                                wh[size_t(r) * D + cw0 + g + 8] = w[nt][2];
+                                wh[size_t(r + 1) * D + cw0 + g + 8] = w[nt][3];
+                            }
+                        }
+                        pack_state<KS>(w, wa0);
+                    }
                     float pa[4][2][4] = {};
 #pragma unroll
                     for (int ks = 0; ks < KS; ++ks) {
@@ -392,7 +407,7 @@ linear_prefill_mma_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_
 
 // ---------------------------------------------------------------- host side
 
-template <int D, int CG, int NST, int SPS, int NX, bool SINGLE>
+template <int D, int CG, int NST, int SPS, int NX, bool SINGLE, bool HIST = false>
 cudaError_t launch_cfg(const LinearArgs& a, cudaStream_t s, int* status) {
     using C = Cfg<D, CG, NST, SPS, NX>;
     const uint64_t rows = uint64_t(a.B) * a.H * a.T;
@@ -401,12 +416,12 @@ cudaError_t launch_cfg(const LinearArgs& a, cudaStream_t s, int* status) {
     if ((e = make_tma_map_bf16(&mq, a.Q, rows, D)) != cudaSuccess) return e;
     if ((e = make_tma_map_bf16(&mk, a.K, rows, D)) != cudaSuccess) return e;
     if ((e = make_tma_map_bf16(&mv, a.V, rows, D)) != cudaSuccess) return e;
-    auto kern = linear_prefill_mma_kernel<D, CG, NST, SPS, NX, SINGLE>;
+    auto kern = linear_prefill_mma_kernel<D, CG, NST, SPS, NX, SINGLE, HIST>;
     const int bytes = C::BYTES + 1024;  // + alignment slack
     if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) != cudaSuccess) return e;
     dim3 grid(unsigned(a.B) * unsigned(a.H), D / 16 / CG);
     kern<<<grid, C::THREADS, bytes, s>>>(mq, mk, mv, a.eta, a.W0, static_cast<__nv_bfloat16*>(a.Z), a.W_out, a.T,
-                                         a.chunk, status);
+                                         a.chunk, status, a.W_hist);
     return cudaGetLastError();
 }
 
@@ -414,6 +429,10 @@ cudaError_t launch_cfg(const LinearArgs& a, cudaStream_t s, int* status) {
 // already completed, so a stage carries several 16-token sub-blocks (SPS).
 template <int D, int CG, int NST, int SPS>
 cudaError_t launch_chunk(const LinearArgs& a, cudaStream_t s, int* status) {
+    if (a.W_hist) {
+        if (a.chunk != 16) return cudaErrorNotSupported;
+        return launch_cfg<D, CG, NST, SPS, NST, true, true>(a, s, status);
+    }
     return a.chunk == 16 ? launch_cfg<D, CG, NST, SPS, NST, true>(a, s, status)
                          : launch_cfg<D, CG, NST, SPS, NST, false>(a, s, status);
 }

@@ -40,4 +40,19 @@ cudaError_t make_tma_map_bf16(CUtensorMap* m, const void* base, uint64_t rows, i
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// [rows][64] fp32 viewed as a 2D tensor; box = 64 rows x 32 columns (128 bytes), 128-byte swizzle.
+cudaError_t make_tma_map_f32x64(CUtensorMap* m, const void* base, uint64_t rows) {
+    EncodeTiledFn enc;
+    cudaError_t e = get_encoder(&enc);
+    if (e != cudaSuccess) return e;
+    cuuint64_t dims[2] = {64, cuuint64_t(rows)};
+    cuuint64_t strides[1] = {64 * 4};
+    cuuint32_t box[2] = {32, 64};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 }  // namespace ttt

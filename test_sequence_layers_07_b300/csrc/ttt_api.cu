@@ -143,8 +143,13 @@ ttt_status ttt_linear_prefill_hist(const void* Q, const void* K, const void* V, 
     CHECK_PTR(W_hist);
     ttt::LinearArgs a{Q, K, V, eta, W0, Z, W_out, B, H, T, d, chunk, dtype == TTT_BF16 ? 1 : 0};
     a.W_hist = W_hist;
-    // the generic kernel writes the block-start states
-    cudaError_t e = ttt::launch_linear_prefill_generic(a, static_cast<cudaStream_t>(stream));
+    // the warp-MMA kernel records the block-start states for bf16, d in {64, 128}, chunk 16, 16 | T;
+    // the generic kernel for every other shape
+    int* status = nullptr;
+    cudaError_t e = status_ptr(&status);
+    if (e != cudaSuccess) return cuda_fail(e, "ttt_linear_prefill_hist status word");
+    e = ttt::launch_linear_prefill_mma(a, static_cast<cudaStream_t>(stream), status);
+    if (e == cudaErrorNotSupported) e = ttt::launch_linear_prefill_generic(a, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "ttt_linear_prefill_hist launch");
     return TTT_OK;
 }
@@ -185,7 +190,17 @@ ttt_status ttt_linear_prefill_backward(const void* Q, const void* K, const void*
     CHECK_PTR(deta);
     ttt::LinearBwdArgs a{Q, K, V, eta, W_hist, dZ, dW_T, dQ, dK, dV, deta, dW0, B, H, T, d, chunk,
                          dtype == TTT_BF16 ? 1 : 0};
-    cudaError_t e = ttt::launch_linear_backward(a, s);
+    // bf16, d = 64, chunk 16, 16 | T: the tensor-core kernel; the SIMT kernel otherwise
+    // (TTT_LINEAR_BACKWARD_KERNEL = "simt" forces the SIMT kernel)
+    const char* kv = getenv("TTT_LINEAR_BACKWARD_KERNEL");
+    cudaError_t e = cudaErrorNotSupported;
+    if (!(kv && !strcmp(kv, "simt"))) {
+        int* status = nullptr;
+        e = status_ptr(&status);
+        if (e != cudaSuccess) return cuda_fail(e, "ttt_linear_prefill_backward status word");
+        e = ttt::launch_linear_backward_mma(a, s, status);
+    }
+    if (e == cudaErrorNotSupported) e = ttt::launch_linear_backward(a, s);
     if (e != cudaSuccess) return cuda_fail(e, "ttt_linear_prefill_backward launch");
     return TTT_OK;
 }

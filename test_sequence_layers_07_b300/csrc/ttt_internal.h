@@ -81,6 +81,8 @@ struct MlpDecodeArgs {
 // block tiles of (d, chunk) fit in shared memory.
 bool linear_backward_supported(int d, int chunk);
 cudaError_t launch_linear_backward(const LinearBwdArgs& a, cudaStream_t s);
+// Tensor-core backward for bf16, d = 64, chunk = 16, 16 | T (cudaErrorNotSupported otherwise).
+cudaError_t launch_linear_backward_mma(const LinearBwdArgs& a, cudaStream_t s, int* status);
 
 // Generic SIMT kernels: every supported shape, fp32 accumulation.
 cudaError_t launch_linear_prefill_generic(const LinearArgs& a, cudaStream_t s);
@@ -110,6 +112,9 @@ cudaError_t launch_mlp_prefill_tc(const MlpArgs& a, cudaStream_t s, int* status)
 // TMA descriptor of a [rows][D] bf16 row-major tensor: boxes of 16 rows x 64
 // columns with the 128-byte swizzle (D a multiple of 64).
 cudaError_t make_tma_map_bf16(CUtensorMap* m, const void* base, uint64_t rows, int D);
+// TMA descriptor of a [rows][64] fp32 row-major tensor: boxes of 64 rows x 32 columns (128 bytes),
+// 128-byte swizzle (two boxes cover a 64 x 64 block).
+cudaError_t make_tma_map_f32x64(CUtensorMap* m, const void* base, uint64_t rows);
 
 // Device-side failure path: a bounded wait that nothing satisfies (see selftest.cu).
 cudaError_t launch_wait_timeout_selftest(unsigned long long limit_ns, cudaStream_t s, int* status);

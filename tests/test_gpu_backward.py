@@ -65,6 +65,24 @@ def test_backward_matches_oracle(B, H, T_, d, chunk, dtype, with_dWT):
         assert rel_err(got, want) <= TOL[dtype], name
 
 
+@pytest.mark.parametrize("kernel", ["mma", "simt"])
+@pytest.mark.parametrize("B,H,T_,with_dWT", [(1, 1, 16, True), (2, 3, 48, False), (1, 2, 208, True),
+                                             (4, 40, 64, True), (1, 2, 1040, False)])
+def test_backward_kernels_d64_blocks_of_16(kernel, B, H, T_, with_dWT, monkeypatch):
+    # bf16, d = 64, blocks of 16: the tensor-core backward (default) and the SIMT one; stages of
+    # four blocks with and without a short last stage, and more CTAs than SMs
+    if kernel == "simt":
+        monkeypatch.setenv("TTT_LINEAR_BACKWARD_KERNEL", "simt")
+    else:
+        monkeypatch.delenv("TTT_LINEAR_BACKWARD_KERNEL", raising=False)
+    x = WL.linear_inputs(B, H, T_, 64, seed=1100 + T_ + H, dtype="bf16", w_std=0.05)
+    g = WL.backward_inputs(B, H, T_, 64, seed=1200 + T_ + H, dtype="bf16", with_dWT=with_dWT)
+    _, _, _, grads = _run(x, g, 16)
+    ref = _oracle(x, g, 16)
+    for name, got, want in zip(("dQ", "dK", "dV", "deta", "dW0"), grads, ref):
+        assert rel_err(got, want) <= TOL["bf16"], name
+
+
 def test_recorded_states_are_the_block_start_states():
     # W_hist[n] is the state after the first n blocks: the final state of a prefill over them
     x = WL.linear_inputs(2, 2, 80, 32, seed=901, dtype="f32", w_std=0.05)
@@ -76,6 +94,22 @@ def test_recorded_states_are_the_block_start_states():
         cut = {k: (v[:, :, :16 * n] if k != "W0" else v) for k, v in r.items()}
         _, Wn = O.linear_dual(cut["Q"], cut["K"], cut["V"], cut["eta"], cut["W0"], 16)
         assert rel_err(Wh[:, :, n], Wn) <= TOL["f32"]
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_recorded_states_tensor_core_forward(d):
+    # bf16, blocks of 16: the warp-MMA forward records the states; compare with prefixes in the oracle
+    x = WL.linear_inputs(1, 3, 96, d, seed=905 + d, dtype="bf16", w_std=0.05)
+    g = WL.backward_inputs(1, 3, 96, d, seed=906, dtype="bf16")
+    Z, W, Wh, _ = _run(x, g, 16)
+    r = f64(x)
+    Zr, Wr = O.linear_dual(r["Q"], r["K"], r["V"], r["eta"], r["W0"], 16)
+    assert rel_err(Z, Zr) <= TOL["bf16"] and rel_err(W, Wr) <= TOL["bf16"]
+    assert torch.equal(Wh[:, :, 0], x["W0"].cuda())
+    for n in (1, 2, 5):
+        cut = {k: (v[:, :, :16 * n] if k != "W0" else v) for k, v in r.items()}
+        _, Wn = O.linear_dual(cut["Q"], cut["K"], cut["V"], cut["eta"], cut["W0"], 16)
+        assert rel_err(Wh[:, :, n], Wn) <= TOL["bf16"]
 
 
 def test_backward_headline_shape_sampled_heads():
