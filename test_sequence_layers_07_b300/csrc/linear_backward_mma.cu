@@ -23,8 +23,9 @@
 //    The term E dW'^T needs dW' with the column index as the contraction: each read-out warp
 //    keeps its own copy of rows [16r, 16r + 16) of dW (same updates, dW = dW' + Q^T dZ + K^T dE),
 //    whose accumulator fragments are exactly those B fragments.
-//  * The block-start states (fp32, 16 KB a block) stream in by cp.async through a 3-slot ring,
-//    laid out with the 128-byte swizzle so both W and W^T fragments read without bank conflicts.
+//  * The block-start states (fp32, 16 KB a block) stream in by cp.async through a 3-slot ring;
+//    one block ahead of use they are converted to a bf16 [64][64] tile (double-buffered), from
+//    which ldmatrix reads both the W and the W^T fragments.
 //  * Q/K/V/dZ arrive by TMA in reverse token order, 4 blocks a stage, 3 stages.
 //  * All mbarrier waits are bounded; the read-out warps meet at reducing barriers (bar.red.or of
 //    the per-thread error flag), so after an expired wait every role leaves its loop.
@@ -56,7 +57,8 @@ constexpr int DAP_OFF = ET_OFF + TILE;             // dA partials [4 warps][32 l
 constexpr int DAS_OFF = DAP_OFF + 4 * 32 * 32;     // summed dA [16][17] fp32 (read-out warp 0)
 constexpr int DEP_OFF = DAS_OFF + 1152;            // deta partials [4][16] fp32, then the S-term [16]
 constexpr int STG_OFF = DEP_OFF + 5 * 64;          // per read-out warp: dQ, dK staging [16][16] bf16 each
-constexpr int BYTES = STG_OFF + 4 * 1024;
+constexpr int WB_OFF = STG_OFF + 4 * 1024;       // bf16 W tiles [2][64][64], 128-byte swizzled rows
+constexpr int BYTES = WB_OFF + 2 * 64 * 128;
 constexpr int THREADS = 32 * (2 + 2 * CG);
 static_assert(BYTES + 1024 <= 232448, "shared memory");
 static_assert(W_OFF % 1024 == 0, "swizzled W slots must be 1024-byte aligned");
@@ -93,6 +95,7 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait2() { asm volatile("cp.async.wait_group 2;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait0() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 
 // barrier over the read-out warps (named barrier 1) that also ORs a per-thread flag
@@ -267,17 +270,15 @@ linear_backward_mma_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid
         }
         const uint32_t off_z = swz(lr + 8 * (lj >> 1), cw0 + 8 * (lj & 1));  // dZ^T A fragment of the group
         const int st_row = lr + 8 * (lj >> 1), st_col = cw0 + 8 * (lj & 1);  // stmatrix.trans rows (tokens)
-        uint32_t kb[KS][4], kt[KS][4], qt[KS][4], zt[4];
+        // prefetched one block ahead: what the first products of a step read (K rows, dZ^T, A, eta);
+        // the transposed K and Q fragments of the update load inside the step
+        uint32_t kb[KS][4], zt[4];
         uint4 am;
         float e0 = 0, e1 = 0, e2 = 0, e3 = 0;  // eta of tokens 2t, 2t + 1, 8 + 2t, 9 + 2t
         auto load = [&](int s, int i, int n) {
             const uint32_t st = sbase + s * STAGE;
 #pragma unroll
             for (int ks = 0; ks < KS; ++ks) ldsm_x4(st + KOFF + i * TILE + off_nk[ks], kb[ks]);
-#pragma unroll
-            for (int kk = 0; kk < KS; ++kk) ldsm_x4_trans(st + KOFF + i * TILE + off_tk[kk], kt[kk]);
-#pragma unroll
-            for (int kk = 0; kk < KS; ++kk) ldsm_x4_trans(st + QOFF + i * TILE + off_tk[kk], qt[kk]);
             ldsm_x4_trans(st + ZOFF + i * TILE + off_z, zt);
             am = *reinterpret_cast<const uint4*>(smem + SC_OFF + (s * SPS + i) * SCSZ + lane * 16);
             const float* es = reinterpret_cast<const float*>(smem + s * STAGE + EOFF + (n - 1 - i) * 64);
@@ -291,14 +292,15 @@ linear_backward_mma_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid
             const int s = si % NST, n = subs_in(si);
             uint8_t* det = smem + DE_OFF + s * SPS * TILE;
             auto step = [&](int i) {
+                const uint32_t st = sbase + s * STAGE;
                 uint32_t wa[KS][4];
                 pack_state<KS>(w, wa);
-                // P^T = dW'^T K^T (16 columns x 16 tokens)
-                float pa[4][2][4] = {};
+                // P^T = dW'^T K^T (16 columns x 16 tokens), in two partial chains
+                float pa[2][2][4] = {};
 #pragma unroll
                 for (int ks = 0; ks < KS; ++ks) {
-                    mma_bf16_16816(pa[ks & 3][0], wa[ks], kb[ks][0], kb[ks][1]);
-                    mma_bf16_16816(pa[ks & 3][1], wa[ks], kb[ks][2], kb[ks][3]);
+                    mma_bf16_16816(pa[ks & 1][0], wa[ks], kb[ks][0], kb[ks][1]);
+                    mma_bf16_16816(pa[ks & 1][1], wa[ks], kb[ks][2], kb[ks][3]);
                 }
                 // T1^T = dZ^T A
                 float t1[2][4] = {};
@@ -308,7 +310,7 @@ linear_backward_mma_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid
 #pragma unroll
                 for (int j = 0; j < 2; ++j)
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) p[j][k] = (pa[0][j][k] + pa[1][j][k]) + (pa[2][j][k] + pa[3][j][k]);
+                    for (int k = 0; k < 4; ++k) p[j][k] = pa[0][j][k] + pa[1][j][k];
                 // dE^T = -(T1^T + P^T D), as a bf16 A fragment (rows c, K = token)
                 uint32_t ge[4];
                 ge[0] = pack_bf16(-fmaf(e0, p[0][0], t1[0][0]), -fmaf(e1, p[0][1], t1[0][1]));
@@ -318,10 +320,13 @@ linear_backward_mma_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid
                 // dW^T += dZ^T Q + dE^T K
 #pragma unroll
                 for (int kk = 0; kk < KS; ++kk) {
-                    mma_bf16_16816(w[2 * kk], zt, qt[kk][0], qt[kk][1]);
-                    mma_bf16_16816(w[2 * kk + 1], zt, qt[kk][2], qt[kk][3]);
-                    mma_bf16_16816(w[2 * kk], ge, kt[kk][0], kt[kk][1]);
-                    mma_bf16_16816(w[2 * kk + 1], ge, kt[kk][2], kt[kk][3]);
+                    uint32_t qt[4], kt[4];
+                    ldsm_x4_trans(st + QOFF + i * TILE + off_tk[kk], qt);
+                    ldsm_x4_trans(st + KOFF + i * TILE + off_tk[kk], kt);
+                    mma_bf16_16816(w[2 * kk], zt, qt[0], qt[1]);
+                    mma_bf16_16816(w[2 * kk + 1], zt, qt[2], qt[3]);
+                    mma_bf16_16816(w[2 * kk], ge, kt[0], kt[1]);
+                    mma_bf16_16816(w[2 * kk + 1], ge, kt[2], kt[3]);
                 }
                 // dE of this group's columns into the block's [16][64] tile (rows tokens)
                 stsm_x4_trans(smem_u32(det + i * TILE) + swz(st_row, st_col), ge[0], ge[1], ge[2], ge[3]);
@@ -387,9 +392,27 @@ linear_backward_mma_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid
             }
             cp_async_commit();
         };
+        // fp32 slot of block p -> bf16 tile p % 2 (this thread: 4 chunks of 8 values)
+        auto convert_w = [&](int p) {
+            if (p >= nsb) return;
+            const uint8_t* src = smem + W_OFF + (p % NW) * WSLOT;
+            uint8_t* dstt = smem + WB_OFF + (p & 1) * 8192;
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int q = rt + 128 * u;  // chunk 0..511: row q >> 3, columns 8 (q & 7) ..
+                const int din = q >> 3, c8 = (q & 7) * 8;
+                const float4 a = *reinterpret_cast<const float4*>(src + wsw(din, c8));
+                const float4 b = *reinterpret_cast<const float4*>(src + wsw(din, c8 + 4));
+                *reinterpret_cast<uint4*>(dstt + swz(din, c8)) =
+                    make_uint4(pack_bf16(a.x, a.y), pack_bf16(a.z, a.w), pack_bf16(b.x, b.y), pack_bf16(b.z, b.w));
+            }
+        };
         fetch_w(0);
         fetch_w(1);
-        bool err = false;
+        fetch_w(2);
+        cp_async_wait2();
+        bool err = bar_readout_any(false);  // every thread's chunks of block 0 are in
+        convert_w(0);
         const int st_row = lr + 8 * (lj & 1), st_col = 8 * (lj >> 1);  // stmatrix rows of an A-layout tile
         float* dep = reinterpret_cast<float*>(smem + DEP_OFF);           // [4][16] partials, then [16] S-term
         uint8_t* stg = smem + STG_OFF + r * 1024;
@@ -402,14 +425,16 @@ linear_backward_mma_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid
             const uint8_t* stp = smem + s * STAGE;
             for (int i = 0; i < n; ++i, ++p) {
                 const int sb = hi - i;
-                cp_async_wait1();  // this thread's chunks of the state of block p
-                // ---- barrier A: the state of block p is in, every warp is done with block p - 1
+                cp_async_wait1();  // this thread's chunks of the state of block p + 1
+                // ---- barrier A: the bf16 tile of block p and the fp32 state of block p + 1 are in,
+                // every warp is done with block p - 1
                 if (bar_readout_any(err)) { err = true; break; }
                 if (p >= 1 && r == 0 && lane < 16)
                     deta[bh * T + 16 * (sb + 1) + lane] =
                         dep[64 + lane] + ((dep[lane] + dep[16 + lane]) + (dep[32 + lane] + dep[48 + lane]));
-                fetch_w(p + 2);
-                const uint8_t* Wp = smem + W_OFF + (p % NW) * WSLOT;
+                convert_w(p + 1);
+                fetch_w(p + 3);  // into the slot of block p, converted one block ago
+                const uint32_t wb = sbase + WB_OFF + (p & 1) * 8192;
                 const float* es = reinterpret_cast<const float*>(stp + EOFF + (n - 1 - i) * 64);
                 const uint8_t* Kt_ = stp + KOFF + i * TILE;
                 const uint8_t* Vt_ = stp + VOFF + i * TILE;
@@ -418,17 +443,12 @@ linear_backward_mma_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid
                 float e[2][4] = {};
 #pragma unroll
                 for (int ks = 0; ks < KS; ++ks) {
-                    uint32_t ka[4];
+                    uint32_t ka[4], wk[4];
                     ldsm_x4(st + KOFF + i * TILE + off_tk[ks], ka);
-#pragma unroll
-                    for (int nt = 0; nt < 2; ++nt) {
-                        const int c = 16 * r + 8 * nt + g, d0 = 16 * ks + 2 * t;
-                        const uint32_t b0 = pack_bf16(*reinterpret_cast<const float*>(Wp + wsw(d0, c)),
-                                                      *reinterpret_cast<const float*>(Wp + wsw(d0 + 1, c)));
-                        const uint32_t b1 = pack_bf16(*reinterpret_cast<const float*>(Wp + wsw(d0 + 8, c)),
-                                                      *reinterpret_cast<const float*>(Wp + wsw(d0 + 9, c)));
-                        mma_bf16_16816(e[nt], ka, b0, b1);
-                    }
+                    // W as B (K = d_in, N = c 16r ..): transposed loads of the rows d_in
+                    ldsm_x4_trans(wb + swz(16 * ks + lr + 8 * (lj & 1), 16 * r + 8 * (lj >> 1)), wk);
+                    mma_bf16_16816(e[0], ka, wk[0], wk[1]);
+                    mma_bf16_16816(e[1], ka, wk[2], wk[3]);
                 }
 #pragma unroll
                 for (int nt = 0; nt < 2; ++nt) {
@@ -467,23 +487,32 @@ linear_backward_mma_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid
                     }
                 }
                 if (r == 0) {
-                    // deta's S-term of this block: sum over queries i >= j of dA_ij S_ij (key j = lane)
-                    float* das = reinterpret_cast<float*>(smem + DAS_OFF);
+                    // deta's S-term of this block: sum over queries i >= j of dA_ij S_ij, per key j;
+                    // this lane's products (i = g, g + 8; j = 8 nt + 2t, + 1), summed over g by shuffles
+                    const float* S = reinterpret_cast<const float*>(smem + SC_OFF + (s * SPS + i) * SCSZ + 512);
+                    float cs[2][2];
 #pragma unroll
                     for (int nt = 0; nt < 2; ++nt) {
                         const int j0 = 8 * nt + 2 * t;
-                        das[g * 17 + j0] = ds[nt][0];
-                        das[g * 17 + j0 + 1] = ds[nt][1];
-                        das[(g + 8) * 17 + j0] = ds[nt][2];
-                        das[(g + 8) * 17 + j0 + 1] = ds[nt][3];
+                        const float2 s0 = *reinterpret_cast<const float2*>(S + g * 16 + j0);
+                        const float2 s1 = *reinterpret_cast<const float2*>(S + (g + 8) * 16 + j0);
+                        cs[nt][0] = (j0 <= g ? ds[nt][0] * s0.x : 0.f) + ds[nt][2] * s1.x;
+                        cs[nt][1] = (j0 + 1 <= g ? ds[nt][1] * s0.y : 0.f) + ds[nt][3] * s1.y;
+                        if (nt == 1) {  // keys 8..15: query rows 0..7 never reach them
+                            cs[1][0] = (j0 <= g + 8 ? ds[1][2] * s1.x : 0.f);
+                            cs[1][1] = (j0 + 1 <= g + 8 ? ds[1][3] * s1.y : 0.f);
+                        }
                     }
-                    __syncwarp();
-                    if (lane < 16) {
-                        const float* S = reinterpret_cast<const float*>(smem + SC_OFF + (s * SPS + i) * SCSZ + 512);
-                        float acc = 0.f;
-                        for (int q = lane; q < 16; ++q) acc = fmaf(das[q * 17 + lane], S[q * 16 + lane], acc);
-                        dep[64 + lane] = acc;
-                    }
+#pragma unroll
+                    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            float v = cs[nt][h];
+                            v += __shfl_xor_sync(0xffffffffu, v, 4);
+                            v += __shfl_xor_sync(0xffffffffu, v, 8);
+                            v += __shfl_xor_sync(0xffffffffu, v, 16);
+                            if (g == 0) dep[64 + 8 * nt + 2 * t + h] = v;
+                        }
                 }
                 uint32_t dsa[4], dst[4];
                 {
@@ -507,17 +536,15 @@ linear_backward_mma_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid
                 const uint32_t det = sbase + DE_OFF + (s * SPS + i) * TILE;
 #pragma unroll
                 for (int kc = 0; kc < KS; ++kc) {
-                    uint32_t za[4], da_[4], ea[4];
+                    uint32_t za[4], da_[4], ea[4], wt[4];
                     ldsm_x4(st + ZOFF + i * TILE + off_tk[kc], za);
                     ldsm_x4(det + off_tk[kc], da_);
                     ldsm_x4(sbase + ET_OFF + off_tk[kc], ea);
+                    // W^T as B (K = column c, N = d_in 16r ..): plain loads of the rows d_in
+                    ldsm_x4(wb + swz(16 * r + lr + 8 * (lj >> 1), 16 * kc + 8 * (lj & 1)), wt);
 #pragma unroll
                     for (int nd = 0; nd < 2; ++nd) {
-                        // W^T as B (K = column c, N = d_in 16r + 8nd + g)
-                        const int din = 16 * r + 8 * nd + g, c0 = 16 * kc + 2 * t;
-                        const float2 wlo = *reinterpret_cast<const float2*>(Wp + wsw(din, c0));
-                        const float2 whi = *reinterpret_cast<const float2*>(Wp + wsw(din, c0 + 8));
-                        const uint32_t b0 = pack_bf16(wlo.x, wlo.y), b1 = pack_bf16(whi.x, whi.y);
+                        const uint32_t b0 = wt[2 * nd], b1 = wt[2 * nd + 1];
                         mma_bf16_16816(q[nd], za, b0, b1);
                         mma_bf16_16816(k[nd], da_, b0, b1);
                         // dW'^T as B from the replica (rows d_in, columns c)
