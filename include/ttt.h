@@ -109,8 +109,9 @@ ttt_status ttt_linear_prefill(const void* Q, const void* K, const void* V, const
  *                                      the start of block n (n = 0: W0),
  *                                      nblk = ceil(T / chunk)
  *
- * W_hist must not overlap any other argument.  Runs the SIMT fp32 kernel for
- * every shape (slower than ttt_linear_prefill on its tensor-core shapes).
+ * W_hist must not overlap any other argument.  bf16 with d in {64, 128} and
+ * chunk 16 runs the warp-MMA prefill kernel with the state writes added;
+ * every other shape the SIMT fp32 kernel.
  * Source: as ttt_linear_prefill; the saved states serve the gradient below.
  */
 ttt_status ttt_linear_prefill_hist(const void* Q, const void* K, const void* V, const float* eta,
@@ -143,7 +144,9 @@ ttt_status ttt_linear_prefill_hist(const void* Q, const void* K, const void* V, 
  *   dK = dE W^T - D E dW'^T + (M . dA D)^T Q,  dV = -dE,
  *   deta_j = -sum_c E_jc (K dW')_jc + sum_i M_ij dA_ij S_ij,
  *   dW = dW' + Q^T dZ + K^T dE.
- * Accumulation in fp32; outputs rounded to dtype (RN-even).
+ * Accumulation in fp32; outputs rounded to dtype (RN-even).  bf16 with d = 64
+ * and chunk 16 runs on the tensor cores, every other shape on a SIMT fp32
+ * kernel; TTT_LINEAR_BACKWARD_KERNEL = "simt" forces the SIMT kernel.
  */
 ttt_status ttt_linear_prefill_backward(const void* Q, const void* K, const void* V, const float* eta,
                                        const float* W_hist, const void* dZ, const float* dW_T, void* dQ,
