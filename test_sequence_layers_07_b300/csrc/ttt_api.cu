@@ -69,12 +69,13 @@ extern "C" {
 
 // First kernel of a prefill dispatch from the environment variable `var`: 0 (`k0`), 1 (`k1`),
 // 2 ("generic"), or -1 when unset or unknown (the default choice by shape).
-static int kernel_choice(const char* var, const char* k0, const char* k1) {
+static int kernel_choice(const char* var, const char* k0, const char* k1, const char* k2 = nullptr) {
     const char* v = getenv(var);
     if (!v) return -1;
     if (!strcmp(v, k0)) return 0;
     if (!strcmp(v, k1)) return 1;
-    if (!strcmp(v, "generic")) return 2;
+    if (k2 && !strcmp(v, k2)) return 2;
+    if (!strcmp(v, "generic")) return k2 ? 3 : 2;
     return -1;
 }
 
@@ -108,15 +109,15 @@ ttt_status ttt_linear_prefill(const void* Q, const void* K, const void* V, const
     int* status = nullptr;
     cudaError_t e = status_ptr(&status);
     if (e != cudaSuccess) return cuda_fail(e, "ttt_linear_prefill status word");
-    // bf16, 16 | chunk, chunk | T: the tcgen05 read-out kernel at d = 64 where it is the faster one,
-    // the warp-MMA kernel at d in {64, 128}; the generic kernel otherwise.
-    // TTT_LINEAR_PREFILL_KERNEL = "tc", "mma" or "generic" makes the dispatch start at that kernel
-    // (the next one takes the shapes it does not cover).
-    const int first = kernel_choice("TTT_LINEAR_PREFILL_KERNEL", "tc", "mma");
+    // bf16, 16 | chunk, chunk | T: the fused warp-MMA kernel at d = 64, the split warp-MMA kernel
+    // at d = 128; the generic kernel otherwise.  TTT_LINEAR_PREFILL_KERNEL = "fused", "tc", "mma"
+    // or "generic" makes the dispatch start at that kernel (the next one takes the shapes it does
+    // not cover); "tc" is the kernel with the read-out on tcgen05.
+    const int first = kernel_choice("TTT_LINEAR_PREFILL_KERNEL", "fused", "tc", "mma");
     e = cudaErrorNotSupported;
-    if (first == 0 || (first < 0 && ttt::linear_prefill_tc_preferred(a)))
-        e = ttt::launch_linear_prefill_tc(a, s, status);
-    if (e == cudaErrorNotSupported && first <= 1) e = ttt::launch_linear_prefill_mma(a, s, status);
+    if (first <= 0) e = ttt::launch_linear_prefill_fused(a, s, status);
+    if (e == cudaErrorNotSupported && first == 1) e = ttt::launch_linear_prefill_tc(a, s, status);
+    if (e == cudaErrorNotSupported && first <= 2) e = ttt::launch_linear_prefill_mma(a, s, status);
     if (e == cudaErrorNotSupported) e = ttt::launch_linear_prefill_generic(a, s);
     if (e != cudaSuccess) return cuda_fail(e, "ttt_linear_prefill launch");
     return TTT_OK;
@@ -143,12 +144,13 @@ ttt_status ttt_linear_prefill_hist(const void* Q, const void* K, const void* V, 
     CHECK_PTR(W_hist);
     ttt::LinearArgs a{Q, K, V, eta, W0, Z, W_out, B, H, T, d, chunk, dtype == TTT_BF16 ? 1 : 0};
     a.W_hist = W_hist;
-    // the warp-MMA kernel records the block-start states for bf16, d in {64, 128}, chunk 16, 16 | T;
-    // the generic kernel for every other shape
+    // the warp-MMA kernels record the block-start states for bf16, d in {64, 128}, chunk 16, 16 | T
+    // (the fused one at d = 64); the generic kernel for every other shape
     int* status = nullptr;
     cudaError_t e = status_ptr(&status);
     if (e != cudaSuccess) return cuda_fail(e, "ttt_linear_prefill_hist status word");
-    e = ttt::launch_linear_prefill_mma(a, static_cast<cudaStream_t>(stream), status);
+    e = ttt::launch_linear_prefill_fused(a, static_cast<cudaStream_t>(stream), status);
+    if (e == cudaErrorNotSupported) e = ttt::launch_linear_prefill_mma(a, static_cast<cudaStream_t>(stream), status);
     if (e == cudaErrorNotSupported) e = ttt::launch_linear_prefill_generic(a, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "ttt_linear_prefill_hist launch");
     return TTT_OK;

@@ -94,6 +94,11 @@ size_t mlp_generic_smem_bytes(int d, int hidden, int chunk);
 // the generic kernel instead.
 cudaError_t launch_linear_prefill_mma(const LinearArgs& a, cudaStream_t s, int* status);
 
+// TTT-Linear prefill at d = 64 (bf16, 16 | chunk, chunk | T): one warp per 16-column group runs
+// the recurrence and the read-out on warp-level MMAs (cudaErrorNotSupported for other shapes).
+bool linear_prefill_fused_supported(const LinearArgs& a);
+cudaError_t launch_linear_prefill_fused(const LinearArgs& a, cudaStream_t s, int* status);
+
 // TTT-Linear prefill at d = 64 (bf16, 16 | chunk, chunk | T): the recurrence on
 // warp-level MMAs, the read-out as per-stage tcgen05 products.
 bool linear_prefill_tc_supported(const LinearArgs& a);

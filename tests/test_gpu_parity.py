@@ -72,7 +72,7 @@ def test_linear_small_shapes(dtype, d, T_, chunk):
 
 @contextlib.contextmanager
 def linear_kernel(name):
-    """Start the TTT-Linear prefill dispatch at kernel `name` ("tc", "mma" or "generic")."""
+    """Start the TTT-Linear prefill dispatch at kernel `name` ("fused", "tc", "mma" or "generic")."""
     old = os.environ.get("TTT_LINEAR_PREFILL_KERNEL")
     os.environ["TTT_LINEAR_PREFILL_KERNEL"] = name
     try:
@@ -91,7 +91,7 @@ TC_CASES = [(1, 1, 16, 16, 0.02), (2, 3, 128, 16, 0.02), (2, 3, 144, 16, 0.1), (
             (1, 2, 640, 64, 0.02), (4, 75, 128, 16, 0.02)]
 
 
-@pytest.mark.parametrize("kernel", ["tc", "mma", "generic"])
+@pytest.mark.parametrize("kernel", ["fused", "tc", "mma", "generic"])
 @pytest.mark.parametrize("B,H,T_,chunk,w_std", TC_CASES)
 def test_linear_kernels_d64(kernel, B, H, T_, chunk, w_std):
     x = WL.linear_inputs(B, H, T_, 64, seed=300 + T_ + chunk + H, dtype="bf16", w_std=w_std)
@@ -161,7 +161,7 @@ def test_linear_empty_sequence_copies_state():
     assert torch.equal(Wo, x["W0"])
 
 
-@pytest.mark.parametrize("kernel", ["tc", "mma"])
+@pytest.mark.parametrize("kernel", ["fused", "tc", "mma"])
 def test_linear_deterministic(kernel):
     x = WL.linear_inputs(2, 3, 256, 64, seed=11, dtype="bf16")
     with linear_kernel(kernel):
