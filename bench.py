@@ -552,7 +552,7 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
-LINEAR_SRC = ["linear_prefill_mma.cu", "ptx.cuh"]
+LINEAR_SRC = ["linear_prefill_fused.cu", "ptx.cuh"]
 
 
 def main(argv=None):

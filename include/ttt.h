@@ -86,11 +86,12 @@ typedef enum ttt_dtype {
  *   chunk    1..512; the last block may be shorter when chunk does not divide T
  *   d        16, 32, 64 or 128 (else TTT_ERR_UNSUPPORTED)
  *
- * Kernels: bf16 with 16 | chunk and chunk | T runs on the tensor cores (at
- * d = 64 and 32 <= chunk <= 128 with the read-out as tcgen05 products, else
- * on warp-level MMAs); other shapes on a generic SIMT kernel.  The environment
- * variable TTT_LINEAR_PREFILL_KERNEL = "tc", "mma" or "generic" starts the
- * choice at that kernel (a kernel that does not cover the shape passes it on).
+ * Kernels: bf16 with 16 | chunk and chunk | T runs on warp-level tensor-core
+ * MMAs (d = 64: one warp per 16-column group; d = 128: a recurrence warp and a
+ * read-out warp per group); other shapes on a generic SIMT kernel.  The
+ * environment variable TTT_LINEAR_PREFILL_KERNEL = "fused", "tc", "mma" or
+ * "generic" starts the choice at that kernel ("tc": d = 64 with the read-out
+ * as tcgen05 products; a kernel that does not cover the shape passes it on).
  * All give the same result up to rounding.
  *
  * Source: "Test-Time Training Layers ...", sections "The Core Mechanism" and
@@ -110,7 +111,7 @@ ttt_status ttt_linear_prefill(const void* Q, const void* K, const void* V, const
  *                                      nblk = ceil(T / chunk)
  *
  * W_hist must not overlap any other argument.  bf16 with d in {64, 128} and
- * chunk 16 runs the warp-MMA prefill kernel with the state writes added;
+ * chunk 16 runs the warp-MMA prefill kernels with the state writes added;
  * every other shape the SIMT fp32 kernel.
  * Source: as ttt_linear_prefill; the saved states serve the gradient below.
  */
