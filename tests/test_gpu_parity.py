@@ -84,11 +84,12 @@ def linear_kernel(name):
             os.environ["TTT_LINEAR_PREFILL_KERNEL"] = old
 
 
-# d = 64 bf16 shapes the tensor-core kernels take: one 16-token block, stages of 128 tokens
-# with and without a short last stage, blocks longer than a stage, more CTAs than SMs
+# d = 64 bf16 shapes the tensor-core kernels take: one 16-token block, stages with and without a
+# short last stage, blocks longer than a stage, more CTAs than SMs; B*H = 1..37 runs one column
+# group per CTA, 38..74 two, from 75 four (on 148 SMs)
 TC_CASES = [(1, 1, 16, 16, 0.02), (2, 3, 128, 16, 0.02), (2, 3, 144, 16, 0.1), (1, 2, 1040, 16, 0.05),
             (2, 2, 256, 32, 0.02), (1, 3, 384, 128, 0.1), (2, 2, 512, 256, 0.02), (1, 2, 1024, 512, 0.05),
-            (1, 2, 640, 64, 0.02), (4, 75, 128, 16, 0.02)]
+            (1, 2, 640, 64, 0.02), (4, 75, 128, 16, 0.02), (2, 24, 272, 16, 0.05), (3, 16, 288, 32, 0.02)]
 
 
 @pytest.mark.parametrize("kernel", ["fused", "tc", "mma", "generic"])
