@@ -445,12 +445,11 @@ bool linear_prefill_tc_supported(const LinearArgs& a) {
            uint64_t(a.B) * a.H * a.T <= 0x7fffffffull;  // TMA row coordinate is int32
 }
 
-// Measured on B300 at B=8 H=12 T=2048: this kernel and the all-warp-MMA kernel tie at chunk 16
+// Measured on B300 at B=8 H=12 T=2048: this kernel and the split warp-MMA kernel tie at chunk 16
 // (49.7 vs 49.6 us); at chunk 64 this one is faster (53.6 vs 58.9 us), at chunk 512 slower
 // (53.5 vs 50.6 us).  Both are bound by the chain warps, which share the SM's tensor cores and
-// shared-memory path with the read-out, in either form.
-bool linear_prefill_tc_preferred(const LinearArgs& a) { return a.chunk >= 32 && a.chunk <= 128; }
-
+// shared-memory path with the read-out, in either form; the one-warp-per-group kernel
+// (linear_prefill_fused.cu) beats both at every chunk, so this one runs only on request.
 cudaError_t launch_linear_prefill_tc(const LinearArgs& a, cudaStream_t s, int* status) {
     if (!linear_prefill_tc_supported(a)) return cudaErrorNotSupported;
     return a.chunk == 16 ? launch_kernel<true>(a, s, status) : launch_kernel<false>(a, s, status);

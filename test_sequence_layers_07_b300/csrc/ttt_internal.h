@@ -102,7 +102,6 @@ cudaError_t launch_linear_prefill_fused(const LinearArgs& a, cudaStream_t s, int
 // TTT-Linear prefill at d = 64 (bf16, 16 | chunk, chunk | T): the recurrence on
 // warp-level MMAs, the read-out as per-stage tcgen05 products.
 bool linear_prefill_tc_supported(const LinearArgs& a);
-bool linear_prefill_tc_preferred(const LinearArgs& a);  // the faster of the two at this shape
 cudaError_t launch_linear_prefill_tc(const LinearArgs& a, cudaStream_t s, int* status);
 
 // TTT-MLP prefill for bf16, d = 64, hidden = 256, chunk = 16 on warp-level MMAs with the state in
