@@ -307,9 +307,10 @@ def bench_mlp(T_mod, w, steps, warmup, world, peaks):
 
 def backward_bytes(B, H, T, d, chunk, elt=2):
     """Backward pass: Q,K,V,dZ read and dQ,dK,dV written (elt bytes each), eta read and deta written,
-    the block-start states read once, dW_T read and dW0 written."""
+    the block-start states read once (elt bytes each: recorded in the dtype of Q), dW_T read and dW0
+    written (fp32)."""
     nblk = -(-T // chunk)
-    return B * H * (T * (7 * d * elt + 8) + nblk * d * d * 4 + 2 * d * d * 4)
+    return B * H * (T * (7 * d * elt + 8) + nblk * d * d * elt + 2 * d * d * 4)
 
 
 def backward_flops(B, H, T, d, chunk):
@@ -325,7 +326,7 @@ def bench_backward(T_mod, w, steps, warmup, world, peaks, nrot=2):
     g = WL.backward_inputs(w.B, w.H, w.T, w.d, seed=w.seed + 100, dtype=w.dtype)
     sets = rotating_copies({**x, "dZ": g["dZ"], "dWT": g["dWT"]}, nrot)
     nblk = -(-w.T // w.chunk)
-    hist = [torch.empty((w.B, w.H, nblk, w.d, w.d), dtype=torch.float32, device="cuda") for _ in range(nrot)]
+    hist = [torch.empty((w.B, w.H, nblk, w.d, w.d), dtype=sets[0]["Q"].dtype, device="cuda") for _ in range(nrot)]
     fwd_out = [(torch.empty_like(s["Q"]), torch.empty_like(s["W0"])) for s in sets]
     bwd_out = [(torch.empty_like(s["Q"]), torch.empty_like(s["Q"]), torch.empty_like(s["Q"]),
                 torch.empty_like(s["eta"]), torch.empty_like(s["W0"])) for s in sets]

@@ -106,17 +106,20 @@ ttt_status ttt_linear_prefill(const void* Q, const void* K, const void* V, const
  * (the values ttt_linear_prefill_backward needs).  Same arguments and results
  * as ttt_linear_prefill, plus:
  *
- *   W_hist   [B][H][nblk][d][d]  fp32  written: W_hist[b][h][n] = the state at
- *                                      the start of block n (n = 0: W0),
- *                                      nblk = ceil(T / chunk)
+ *   W_hist   [B][H][nblk][d][d]  dtype  written: W_hist[b][h][n] = the state at
+ *                                       the start of block n (n = 0: W0),
+ *                                       nblk = ceil(T / chunk)
  *
+ * W_hist has the element type of Q/K/V: fp32 for TTT_F32; for TTT_BF16 the
+ * state rounded to bf16 (RN-even), which is the operand the forward's products
+ * used and all the backward reads (half the bytes of fp32 states).
  * W_hist must not overlap any other argument.  bf16 with d in {64, 128} and
  * chunk 16 runs the warp-MMA prefill kernels with the state writes added;
- * every other shape the SIMT fp32 kernel.
+ * every other shape the SIMT kernel.
  * Source: as ttt_linear_prefill; the saved states serve the gradient below.
  */
 ttt_status ttt_linear_prefill_hist(const void* Q, const void* K, const void* V, const float* eta,
-                                   const float* W0, void* Z, float* W_out, float* W_hist, int B, int H,
+                                   const float* W0, void* Z, float* W_out, void* W_hist, int B, int H,
                                    int T, int d, int chunk, ttt_dtype dtype, void* stream);
 
 /*
@@ -128,7 +131,7 @@ ttt_status ttt_linear_prefill_hist(const void* Q, const void* K, const void* V, 
  *
  *   Q, K, V     [B][H][T][d]        dtype   the forward inputs
  *   eta         [B][H][T]           fp32
- *   W_hist      [B][H][nblk][d][d]  fp32    block-start states from ttt_linear_prefill_hist
+ *   W_hist      [B][H][nblk][d][d]  dtype   block-start states from ttt_linear_prefill_hist
  *   dZ          [B][H][T][d]        dtype   dL/dZ
  *   dW_T        [B][H][d][d]        fp32    dL/dW_out, or NULL for zero
  *   dQ, dK, dV  [B][H][T][d]        dtype   written: dL/dQ, dL/dK, dL/dV
@@ -150,7 +153,7 @@ ttt_status ttt_linear_prefill_hist(const void* Q, const void* K, const void* V, 
  * kernel; TTT_LINEAR_BACKWARD_KERNEL = "simt" forces the SIMT kernel.
  */
 ttt_status ttt_linear_prefill_backward(const void* Q, const void* K, const void* V, const float* eta,
-                                       const float* W_hist, const void* dZ, const float* dW_T, void* dQ,
+                                       const void* W_hist, const void* dZ, const float* dW_T, void* dQ,
                                        void* dK, void* dV, float* deta, float* dW0, int B, int H, int T,
                                        int d, int chunk, ttt_dtype dtype, void* stream);
 

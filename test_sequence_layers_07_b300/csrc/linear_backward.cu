@@ -15,7 +15,8 @@
 //     dQ = dZ W^T + dS K              dK = dE W^T - D E dW'^T + dS^T Q
 //     dV = -dE                        deta_j = -sum_c E_jc (K dW')_jc + sum_i M_ij dA_ij S_ij
 //     dW = dW' + Q^T dZ + K^T dE      (carried to the previous block; dW0 at the end)
-// The block-start states W come from the forward pass (ttt_linear_prefill_hist).
+// The block-start states W come from the forward pass (ttt_linear_prefill_hist), in the element
+// type of Q (bf16 runs record the state rounded to bf16, the operand the forward's products used).
 //
 // One CTA per (batch, head): dQ, dK and deta sum over every output column, so the column split
 // of the forward kernels does not apply.  The block's tiles, both states and the b x b score
@@ -47,7 +48,7 @@ __device__ __forceinline__ void load_tile(float* sh, const TI* src, int rows) {
 template <typename TI, int D>
 __global__ void __launch_bounds__(kThreads)
 linear_backward_kernel(const TI* __restrict__ Q, const TI* __restrict__ K, const TI* __restrict__ V,
-                       const float* __restrict__ eta, const float* __restrict__ W_hist, const TI* __restrict__ dZ,
+                       const float* __restrict__ eta, const TI* __restrict__ W_hist, const TI* __restrict__ dZ,
                        const float* __restrict__ dW_T, TI* __restrict__ dQ, TI* __restrict__ dK,
                        TI* __restrict__ dV, float* __restrict__ deta, float* __restrict__ dW0, int T, int chunk) {
     constexpr int LD = D + 1;
@@ -77,8 +78,8 @@ linear_backward_kernel(const TI* __restrict__ Q, const TI* __restrict__ K, const
         const int t0 = n * chunk, rows = min(chunk, T - t0);
         const size_t base = hd + size_t(t0) * D;
         __syncthreads();  // the previous (later) block is done with every tile
-        const float* Wn = W_hist + (bh * nblk + n) * size_t(D) * D;
-        for (int idx = threadIdx.x; idx < D * D; idx += kThreads) Ws[(idx / D) * LD + idx % D] = Wn[idx];
+        const TI* Wn = W_hist + (bh * nblk + n) * size_t(D) * D;
+        for (int idx = threadIdx.x; idx < D * D; idx += kThreads) Ws[(idx / D) * LD + idx % D] = to_f32(Wn[idx]);
         load_tile<TI, D>(Qs, Q + base, rows);
         load_tile<TI, D>(Ks, K + base, rows);
         load_tile<TI, D>(Vs, V + base, rows);
@@ -176,7 +177,8 @@ cudaError_t launch_d(const LinearBwdArgs& a, cudaStream_t s) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(bytes));
     if (e != cudaSuccess) return e;
     kern<<<unsigned(a.B) * unsigned(a.H), kThreads, bytes, s>>>(
-        static_cast<const TI*>(a.Q), static_cast<const TI*>(a.K), static_cast<const TI*>(a.V), a.eta, a.W_hist,
+        static_cast<const TI*>(a.Q), static_cast<const TI*>(a.K), static_cast<const TI*>(a.V), a.eta,
+        static_cast<const TI*>(a.W_hist),
         static_cast<const TI*>(a.dZ), a.dW_T, static_cast<TI*>(a.dQ), static_cast<TI*>(a.dK), static_cast<TI*>(a.dV),
         a.deta, a.dW0, a.T, a.chunk);
     return cudaGetLastError();

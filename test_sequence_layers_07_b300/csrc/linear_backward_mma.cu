@@ -23,8 +23,8 @@
 //    The term E dW'^T needs dW' with the column index as the contraction: each read-out warp
 //    keeps its own copy of rows [16r, 16r + 16) of dW (same updates, dW = dW' + Q^T dZ + K^T dE),
 //    whose accumulator fragments are exactly those B fragments.
-//  * The block-start states (fp32, 16 KB a block) stream in by cp.async through a 3-slot ring;
-//    one block ahead of use they are converted to a bf16 [64][64] tile (double-buffered), from
+//  * The block-start states (bf16, as the forward recorded them: 8 KB a block) stream in by
+//    cp.async, three blocks ahead, straight into a 4-slot ring of swizzled [64][64] tiles, from
 //    which ldmatrix reads both the W and the W^T fragments.
 //  * Q/K/V/dZ arrive by TMA in reverse token order, 4 blocks a stage, 3 stages.
 //  * All mbarrier waits are bounded; the read-out warps meet at reducing barriers (bar.red.or of
@@ -41,15 +41,15 @@ namespace {
 using namespace ptx;
 
 constexpr uint64_t kWaitLimitNs = 4000000000ull;  // 4 s: far beyond any legitimate wait
-constexpr int D = 64, CG = 4, SPS = 4, NST = 3, NW = 3;
+constexpr int D = 64, CG = 4, SPS = 4, NST = 3, NW = 4;
 constexpr int KS = D / 16, NT = D / 8;
 constexpr int TILE = 16 * D * 2;  // one [16][64] bf16 block tile (one TMA box)
 // stage slot: Q, K, V, dZ tiles of SPS blocks (processing order), then eta (SPS x 16 fp32, token order)
 constexpr int QOFF = 0, KOFF = SPS * TILE, VOFF = 2 * SPS * TILE, ZOFF = 3 * SPS * TILE, EOFF = 4 * SPS * TILE;
 constexpr int STAGE = (EOFF + SPS * 64 + 1023) / 1024 * 1024;
-constexpr int W_OFF = NST * STAGE;                 // W ring: NW x [64][64] fp32, two [64][32] swizzled boxes
-constexpr int WSLOT = D * D * 4;
-constexpr int SC_OFF = W_OFF + NW * WSLOT;         // scores ring [NST][SPS]: A fragments (512 B) + S [16][16] fp32
+constexpr int WB_OFF = NST * STAGE;                // W ring: NW x [64][64] bf16, 128-byte swizzled rows
+constexpr int WSLOT = D * D * 2;
+constexpr int SC_OFF = WB_OFF + NW * WSLOT;        // scores ring [NST][SPS]: A fragments (512 B) + S [16][16] fp32
 constexpr int SCSZ = 512 + 1024;
 constexpr int DE_OFF = SC_OFF + NST * SPS * SCSZ;  // dE ring [NST][SPS] x [16][64] bf16
 constexpr int ET_OFF = DE_OFF + NST * SPS * TILE;  // E [16][64] bf16
@@ -57,20 +57,15 @@ constexpr int DAP_OFF = ET_OFF + TILE;             // dA partials [4 warps][32 l
 constexpr int DAS_OFF = DAP_OFF + 4 * 32 * 32;     // summed dA [16][17] fp32 (read-out warp 0)
 constexpr int DEP_OFF = DAS_OFF + 1152;            // deta partials [4][16] fp32, then the S-term [16]
 constexpr int STG_OFF = DEP_OFF + 5 * 64;          // per read-out warp: dQ, dK staging [16][16] bf16 each
-constexpr int WB_OFF = STG_OFF + 4 * 1024;       // bf16 W tiles [2][64][64], 128-byte swizzled rows
-constexpr int BYTES = WB_OFF + 2 * 64 * 128;
+constexpr int BYTES = STG_OFF + 4 * 1024;
 constexpr int THREADS = 32 * (2 + 2 * CG);
 static_assert(BYTES + 1024 <= 232448, "shared memory");
-static_assert(W_OFF % 1024 == 0, "swizzled W slots must be 1024-byte aligned");
+static_assert(WB_OFF % 1024 == 0, "swizzled W slots must be 1024-byte aligned");
 
 // byte offset of (row, col) in a [rows][64] bf16 tile with 128-byte rows, 16-byte chunk XOR row % 8;
 // col % 8 == 0
 __device__ __forceinline__ uint32_t swz(int row, int col) {
     return uint32_t(row * 128 + ((((col >> 3) ^ row) & 7) << 4));
-}
-// byte offset of W[din][c] in a W slot: two [64][32] fp32 boxes with the 128-byte swizzle
-__device__ __forceinline__ uint32_t wsw(int din, int c) {
-    return uint32_t((c >> 5) * 8192 + din * 128 + (((((c & 31) >> 2) ^ din) & 7) << 4) + (c & 3) * 4);
 }
 
 template <int NK>
@@ -94,7 +89,6 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait2() { asm volatile("cp.async.wait_group 2;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait0() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 
@@ -120,7 +114,7 @@ __device__ __forceinline__ float2 bf16x2_at(const uint8_t* tile, int row, int co
 __global__ void __launch_bounds__(THREADS, 1)
 linear_backward_mma_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                            const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmZ,
-                           const float* __restrict__ eta, const float* __restrict__ W_hist,
+                           const float* __restrict__ eta, const __nv_bfloat16* __restrict__ W_hist,
                            const float* __restrict__ dW_T, __nv_bfloat16* __restrict__ dQ,
                            __nv_bfloat16* __restrict__ dK, __nv_bfloat16* __restrict__ dV, float* __restrict__ deta,
                            float* __restrict__ dW0, int T, int* status) {
@@ -377,42 +371,26 @@ linear_backward_mma_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid
             rep[nt][3] = dW_T ? src[size_t(r0 + 8) * D + c0 + 1] : 0.f;
         }
         // the block-start state of the p-th block in processing order, by cp.async: this thread's
-        // eight 16-byte chunks of the 16 KB block, placed in the swizzled layout
+        // four 16-byte chunks of the 8 KB bf16 block, placed in the swizzled layout of slot p % NW
         auto fetch_w = [&](int p) {
             if (p < nsb) {
                 const int sb = nsb - 1 - p;
-                const float* src = W_hist + (bh * nsb + sb) * size_t(D) * D;
-                const uint32_t dst = sbase + W_OFF + (p % NW) * WSLOT;
+                const __nv_bfloat16* src = W_hist + (bh * nsb + sb) * size_t(D) * D;
+                const uint32_t dst = sbase + WB_OFF + (p % NW) * WSLOT;
 #pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    const int q = rt + 128 * u;           // chunk 0..1023: row q >> 4, 4 floats at (q & 15) * 4
-                    const int din = q >> 4, c = (q & 15) * 4;
-                    cp_async16(dst + wsw(din, c), src + din * D + c);
+                for (int u = 0; u < 4; ++u) {
+                    const int q = rt + 128 * u;  // chunk 0..511: row q >> 3, columns 8 (q & 7) ..
+                    const int din = q >> 3, c8 = (q & 7) * 8;
+                    cp_async16(dst + swz(din, c8), src + din * D + c8);
                 }
             }
             cp_async_commit();
-        };
-        // fp32 slot of block p -> bf16 tile p % 2 (this thread: 4 chunks of 8 values)
-        auto convert_w = [&](int p) {
-            if (p >= nsb) return;
-            const uint8_t* src = smem + W_OFF + (p % NW) * WSLOT;
-            uint8_t* dstt = smem + WB_OFF + (p & 1) * 8192;
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int q = rt + 128 * u;  // chunk 0..511: row q >> 3, columns 8 (q & 7) ..
-                const int din = q >> 3, c8 = (q & 7) * 8;
-                const float4 a = *reinterpret_cast<const float4*>(src + wsw(din, c8));
-                const float4 b = *reinterpret_cast<const float4*>(src + wsw(din, c8 + 4));
-                *reinterpret_cast<uint4*>(dstt + swz(din, c8)) =
-                    make_uint4(pack_bf16(a.x, a.y), pack_bf16(a.z, a.w), pack_bf16(b.x, b.y), pack_bf16(b.z, b.w));
-            }
         };
         fetch_w(0);
         fetch_w(1);
         fetch_w(2);
         cp_async_wait2();
         bool err = bar_readout_any(false);  // every thread's chunks of block 0 are in
-        convert_w(0);
         const int st_row = lr + 8 * (lj & 1), st_col = 8 * (lj >> 1);  // stmatrix rows of an A-layout tile
         float* dep = reinterpret_cast<float*>(smem + DEP_OFF);           // [4][16] partials, then [16] S-term
         uint8_t* stg = smem + STG_OFF + r * 1024;
@@ -425,16 +403,14 @@ linear_backward_mma_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid
             const uint8_t* stp = smem + s * STAGE;
             for (int i = 0; i < n; ++i, ++p) {
                 const int sb = hi - i;
-                cp_async_wait1();  // this thread's chunks of the state of block p + 1
-                // ---- barrier A: the bf16 tile of block p and the fp32 state of block p + 1 are in,
-                // every warp is done with block p - 1
+                cp_async_wait2();  // this thread's chunks of the state of block p
+                // ---- barrier A: the state of block p is in, every warp is done with block p - 1
                 if (bar_readout_any(err)) { err = true; break; }
                 if (p >= 1 && r == 0 && lane < 16)
                     deta[bh * T + 16 * (sb + 1) + lane] =
                         dep[64 + lane] + ((dep[lane] + dep[16 + lane]) + (dep[32 + lane] + dep[48 + lane]));
-                convert_w(p + 1);
-                fetch_w(p + 3);  // into the slot of block p, converted one block ago
-                const uint32_t wb = sbase + WB_OFF + (p & 1) * 8192;
+                fetch_w(p + 3);  // into the slot of block p - 1
+                const uint32_t wb = sbase + WB_OFF + (p % NW) * WSLOT;
                 const float* es = reinterpret_cast<const float*>(stp + EOFF + (n - 1 - i) * 64);
                 const uint8_t* Kt_ = stp + KOFF + i * TILE;
                 const uint8_t* Vt_ = stp + VOFF + i * TILE;
@@ -655,7 +631,7 @@ cudaError_t launch_linear_backward_mma(const LinearBwdArgs& a, cudaStream_t s, i
         cudaSuccess)
         return e;
     linear_backward_mma_kernel<<<unsigned(a.B) * unsigned(a.H), THREADS, bytes, s>>>(
-        mq, mk, mv, mz, a.eta, a.W_hist, a.dW_T, static_cast<__nv_bfloat16*>(a.dQ), static_cast<__nv_bfloat16*>(a.dK),
+        mq, mk, mv, mz, a.eta, static_cast<const __nv_bfloat16*>(a.W_hist), a.dW_T, static_cast<__nv_bfloat16*>(a.dQ), static_cast<__nv_bfloat16*>(a.dK),
         static_cast<__nv_bfloat16*>(a.dV), a.deta, a.dW0, a.T, status);
     return cudaGetLastError();
 }

@@ -78,18 +78,20 @@ struct FusedCfg {
     static constexpr int QOFF = 0, KOFF = SPS * TILE, VOFF = 2 * SPS * TILE, EOFF = 3 * SPS * TILE;
     static constexpr int STAGE = (EOFF + SPS * 64 + 1023) / 1024 * 1024;
     static constexpr int SC_OFF = NST * STAGE;  // masked scores [NST][SPS][32 lanes] x 16 B
-    static constexpr int BYTES = SC_OFF + NST * SPS * 512;
+    static constexpr int HS_OFF = SC_OFF + NST * SPS * 512;  // per warp: a [D][16] bf16 state slice
+    static constexpr int BYTES = HS_OFF + CG * D * 32;
     static constexpr int THREADS = 32 * (CG + 1);
 };
 
-// HIST: also write the state at the start of every block to W_hist [B*H][T/chunk][D][D] (the
-// values the backward needs); instantiated for blocks of 16 tokens only.
+// HIST: also write the state at the start of every block to W_hist [B*H][T/chunk][D][D], as bf16
+// (the operand the products use, and what the backward reads); instantiated for blocks of 16
+// tokens only.
 template <int D, int CG, int NST, int SPS, bool SINGLE, bool HIST>
 __global__ void __launch_bounds__(FusedCfg<D, CG, NST, SPS>::THREADS, 1)
 linear_prefill_fused_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                             const __grid_constant__ CUtensorMap tmV, const float* __restrict__ eta,
                             const float* W0, __nv_bfloat16* __restrict__ Z, float* W_out, int T, int chunk,
-                            int* status, float* __restrict__ W_hist) {
+                            int* status, __nv_bfloat16* __restrict__ W_hist) {
     using C = FusedCfg<D, CG, NST, SPS>;
     constexpr int KS = C::KS, NT = C::NT;
 
@@ -273,18 +275,26 @@ linear_prefill_fused_kernel(const __grid_constant__ CUtensorMap tmQ, const __gri
                 const uint4 sf4 = *reinterpret_cast<const uint4*>(sc + i * 512 + lane * 16);
                 const bool bstart = SINGLE || sb % nsub == 0;
                 if (bstart) {
-                    if constexpr (HIST) {  // the state at the start of block sb / nsub
-                        float* wh = W_hist + (bh * size_t(nsb / nsub) + sb / nsub) * D * D;
-#pragma unroll
-                        for (int nt = 0; nt < NT; ++nt) {
-                            const int r = 8 * nt + 2 * t;
-                            wh[size_t(r) * D + cw0 + g] = w[nt][0];
-                            wh[size_t(r + 1) * D + cw0 + g] = w[nt][1];
-                            wh[size_t(r) * D + cw0 + g + 8] = w[nt][2];
-                            wh[size_t(r + 1) * D + cw0 + g + 8] = w[nt][3];
-                        }
-                    }
                     pack_state<KS>(w, wa0);
+                    if constexpr (HIST) {
+                        // the bf16 state at the start of block sb / nsub: the A fragments of W^T
+                        // stored transposed (stmatrix) into this warp's [D][16] slice, then 16-byte
+                        // rows halves to W_hist[d_in][cw0 ..]
+                        const uint32_t hs = sbase + C::HS_OFF + cg * D * 32;
+#pragma unroll
+                        for (int ks = 0; ks < KS; ++ks)
+                            stsm_x4_trans(hs + (16 * ks + 8 * (lj >> 1) + lr) * 32 + (lj & 1) * 16, wa0[ks][0],
+                                          wa0[ks][1], wa0[ks][2], wa0[ks][3]);
+                        __syncwarp();
+                        __nv_bfloat16* wh = W_hist + (bh * size_t(nsb / nsub) + sb / nsub) * D * D + cw0;
+#pragma unroll
+                        for (int u = 0; u < D / 16; ++u) {
+                            const int q = lane + 32 * u;  // chunk: row q >> 1, half q & 1
+                            const uint4 v = *reinterpret_cast<const uint4*>(smem + C::HS_OFF + cg * D * 32 + q * 16);
+                            *reinterpret_cast<uint4*>(wh + size_t(q >> 1) * D + 8 * (q & 1)) = v;
+                        }
+                        __syncwarp();
+                    }
                 }
                 if constexpr (!SINGLE) {
                     if (bstart) {
@@ -390,11 +400,12 @@ cudaError_t launch_cfg(const LinearArgs& a, cudaStream_t s, int* status) {
     if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) != cudaSuccess) return e;
     dim3 grid(unsigned(a.B) * unsigned(a.H), D / 16 / CG);
     kern<<<grid, C::THREADS, bytes, s>>>(mq, mk, mv, a.eta, a.W0, static_cast<__nv_bfloat16*>(a.Z), a.W_out, a.T,
-                                         a.chunk, status, a.W_hist);
+                                         a.chunk, status, static_cast<__nv_bfloat16*>(a.W_hist));
     return cudaGetLastError();
 }
 
-// stages of 256 tokens, double-buffered: 2 x 97 KB of Q/K/V/eta + 16 KB of scores per CTA
+// stages of 256 tokens, double-buffered: 2 x 97 KB of Q/K/V/eta + 16 KB of scores + 8 KB of state
+// staging per CTA
 constexpr int kSps = 16, kNst = 2;
 
 template <int CG>

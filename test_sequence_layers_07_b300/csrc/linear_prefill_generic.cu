@@ -54,7 +54,7 @@ __global__ void __launch_bounds__(kThreads)
 linear_prefill_generic_kernel(const TI* __restrict__ Q, const TI* __restrict__ K,
                               const TI* __restrict__ V, const float* __restrict__ eta,
                               const float* W0, TI* __restrict__ Z, float* W_out, int T, int chunk,
-                              float* __restrict__ W_hist) {
+                              TI* __restrict__ W_hist) {
     using C = GenCfg<D>;
     constexpr int NS = C::NS;
     extern __shared__ float smem[];
@@ -81,10 +81,10 @@ linear_prefill_generic_kernel(const TI* __restrict__ Q, const TI* __restrict__ K
     for (int t0 = 0; t0 < T; t0 += chunk) {
         const int n = min(chunk, T - t0);
         for (int j = threadIdx.x; j < n; j += kThreads) Et[j] = eh[t0 + j];
-        if (W_hist) {  // the state at the start of this block (this CTA's columns)
-            float* wh = W_hist + (bh * nblk + t0 / chunk) * size_t(D) * D;
+        if (W_hist) {  // the state at the start of this block (this CTA's columns), as TI
+            TI* wh = W_hist + (bh * nblk + t0 / chunk) * size_t(D) * D;
             for (int idx = threadIdx.x; idx < D * NS; idx += kThreads)
-                wh[size_t(idx / NS) * D + col0 + idx % NS] = Ws[idx];
+                wh[size_t(idx / NS) * D + col0 + idx % NS] = from_f32<TI>(Ws[idx]);
         }
 
         // E = K W0 - V  (this slice's columns)
@@ -203,7 +203,7 @@ cudaError_t launch_d(const LinearArgs& a, cudaStream_t s) {
     dim3 grid(unsigned(a.B) * unsigned(a.H), C::SLICES);
     kern<<<grid, kThreads, C::BYTES, s>>>(static_cast<const TI*>(a.Q), static_cast<const TI*>(a.K),
                                           static_cast<const TI*>(a.V), a.eta, a.W0,
-                                          static_cast<TI*>(a.Z), a.W_out, a.T, a.chunk, a.W_hist);
+                                          static_cast<TI*>(a.Z), a.W_out, a.T, a.chunk, static_cast<TI*>(a.W_hist));
     return cudaGetLastError();
 }
 

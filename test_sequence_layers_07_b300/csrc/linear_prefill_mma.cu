@@ -88,14 +88,14 @@ struct Cfg {
     static constexpr int THREADS = 32 * (2 * CG + 2);
 };
 
-// HIST: also write the state at the start of every block to W_hist [B*H][T/chunk][D][D]
-// (the values the backward needs); instantiated for blocks of 16 tokens only.
+// HIST: also write the state at the start of every block to W_hist [B*H][T/chunk][D][D], rounded
+// to bf16 (what the backward reads); instantiated for blocks of 16 tokens only.
 template <int D, int CG, int NST, int SPS, int NX, bool SINGLE, bool HIST>
 __global__ void __launch_bounds__(Cfg<D, CG, NST, SPS, NX>::THREADS, 1)
 linear_prefill_mma_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                           const __grid_constant__ CUtensorMap tmV, const float* __restrict__ eta,
                           const float* W0, __nv_bfloat16* __restrict__ Z, float* W_out, int T, int chunk,
-                          int* status, float* __restrict__ W_hist) {
+                          int* status, __nv_bfloat16* __restrict__ W_hist) {
     using C = Cfg<D, CG, NST, SPS, NX>;
     constexpr int KS = C::KS, NT = C::NT;
 
@@ -267,15 +267,15 @@ linear_prefill_mma_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_
                 auto step = [&](int i) {
                     const int sb = si * SPS + i;
                     if (SINGLE || sb % nsub == 0) {
-                        if constexpr (HIST) {  // the state at the start of block sb / nsub
-                            float* wh = W_hist + (bh * size_t(nsb / nsub) + sb / nsub) * D * D;
+                        if constexpr (HIST) {  // the state at the start of block sb / nsub, as bf16
+                            __nv_bfloat16* wh = W_hist + (bh * size_t(nsb / nsub) + sb / nsub) * D * D;
 #pragma unroll
                             for (int nt = 0; nt < NT; ++nt) {
                                 const int r = 8 * nt + 2 * t;
-                                wh[size_t(r) * D + cw0 + g] = w[nt][0];
-                                wh[size_t(r + 1) * D + cw0 + g] = w[nt][1];
-                                wh[size_t(r) * D + cw0 + g + 8] = w[nt][2];
-                                wh[size_t(r + 1) * D + cw0 + g + 8] = w[nt][3];
+                                wh[size_t(r) * D + cw0 + g] = __float2bfloat16_rn(w[nt][0]);
+                                wh[size_t(r + 1) * D + cw0 + g] = __float2bfloat16_rn(w[nt][1]);
+                                wh[size_t(r) * D + cw0 + g + 8] = __float2bfloat16_rn(w[nt][2]);
+                                wh[size_t(r + 1) * D + cw0 + g + 8] = __float2bfloat16_rn(w[nt][3]);
                             }
                         }
                         pack_state<KS>(w, wa0);
@@ -421,7 +421,7 @@ cudaError_t launch_cfg(const LinearArgs& a, cudaStream_t s, int* status) {
     if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) != cudaSuccess) return e;
     dim3 grid(unsigned(a.B) * unsigned(a.H), D / 16 / CG);
     kern<<<grid, C::THREADS, bytes, s>>>(mq, mk, mv, a.eta, a.W0, static_cast<__nv_bfloat16*>(a.Z), a.W_out, a.T,
-                                         a.chunk, status, a.W_hist);
+                                         a.chunk, status, static_cast<__nv_bfloat16*>(a.W_hist));
     return cudaGetLastError();
 }
 

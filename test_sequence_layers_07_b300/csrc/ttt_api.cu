@@ -124,7 +124,7 @@ ttt_status ttt_linear_prefill(const void* Q, const void* K, const void* V, const
 }
 
 ttt_status ttt_linear_prefill_hist(const void* Q, const void* K, const void* V, const float* eta, const float* W0,
-                                   void* Z, float* W_out, float* W_hist, int B, int H, int T, int d, int chunk,
+                                   void* Z, float* W_out, void* W_hist, int B, int H, int T, int d, int chunk,
                                    ttt_dtype dtype, void* stream) {
     g_last_error[0] = 0;
     if (B < 0 || H < 0 || T < 0) return fail(TTT_ERR_INVALID_ARG, "negative size%s");
@@ -157,7 +157,7 @@ ttt_status ttt_linear_prefill_hist(const void* Q, const void* K, const void* V, 
 }
 
 ttt_status ttt_linear_prefill_backward(const void* Q, const void* K, const void* V, const float* eta,
-                                       const float* W_hist, const void* dZ, const float* dW_T, void* dQ, void* dK,
+                                       const void* W_hist, const void* dZ, const float* dW_T, void* dQ, void* dK,
                                        void* dV, float* deta, float* dW0, int B, int H, int T, int d, int chunk,
                                        ttt_dtype dtype, void* stream) {
     g_last_error[0] = 0;
@@ -343,6 +343,6 @@ const char* ttt_status_string(ttt_status s) {
 
 const char* ttt_last_error(void) { return g_last_error; }
 
-int ttt_version(void) { return 10200; }
+int ttt_version(void) { return 10300; }
 
 }  // extern "C"

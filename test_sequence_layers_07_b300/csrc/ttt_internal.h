@@ -19,7 +19,8 @@ struct LinearArgs {
     float* W_out;
     int B, H, T, d, chunk;
     int bf16;                // 1: Q/K/V/Z are bfloat16, 0: float32
-    float* W_hist = nullptr;  // optional: the state at the start of every block, [B][H][nblk][d][d]
+    void* W_hist = nullptr;  // optional: the state at the start of every block, [B][H][nblk][d][d],
+                             // in the element type of Q (bf16: the state rounded RN-even)
 };
 
 // Gradient of the TTT-Linear chunked scan (outer-loop training).
@@ -28,7 +29,7 @@ struct LinearBwdArgs {
     const void* K;
     const void* V;
     const float* eta;
-    const float* W_hist;  // [B][H][nblk][d][d], the state at the start of every block
+    const void* W_hist;   // [B][H][nblk][d][d], the state at the start of every block (element type of Q)
     const void* dZ;
     const float* dW_T;    // gradient of the final state, or nullptr (zero)
     void* dQ;

@@ -127,7 +127,8 @@ def ttt_linear_prefill(Q, K, V, eta, W0, Z, W_out, chunk: int, stream=None) -> N
 
 def ttt_linear_prefill_hist(Q, K, V, eta, W0, Z, W_out, W_hist, chunk: int, stream=None) -> None:
     """TTT-Linear prefill that also writes the state at the start of every block into
-    W_hist [B,H,ceil(T/chunk),d,d] fp32 (the input of the backward)."""
+    W_hist [B,H,ceil(T/chunk),d,d] (the input of the backward), in the dtype of Q: fp32, or for
+    bf16 inputs the state rounded to bf16."""
     B, H, T, d = Q.shape
     dt = _io_dtype(Q)
     for name, t in (("K", K), ("V", V), ("Z", Z)):
@@ -140,7 +141,7 @@ def ttt_linear_prefill_hist(Q, K, V, eta, W0, Z, W_out, W_hist, chunk: int, stre
         raise ValueError("W_hist must be [B,H,ceil(T/chunk),d,d]")
     st = load_library().ttt_linear_prefill_hist(
         _ptr(Q, "Q"), _ptr(K, "K"), _ptr(V, "V"), _ptr(eta, "eta", torch.float32), _ptr(W0, "W0", torch.float32),
-        _ptr(Z, "Z"), _ptr(W_out, "W_out", torch.float32), _ptr(W_hist, "W_hist", torch.float32),
+        _ptr(Z, "Z"), _ptr(W_out, "W_out", torch.float32), _ptr(W_hist, "W_hist", Q.dtype),
         B, H, T, d, int(chunk), dt, _stream(stream))
     _check(st)
 
@@ -161,7 +162,7 @@ def ttt_linear_prefill_backward(Q, K, V, eta, W_hist, dZ, dW_T, dQ, dK, dV, deta
         raise ValueError("W_hist must be [B,H,ceil(T/chunk),d,d] and dW_T [B,H,d,d]")
     st = load_library().ttt_linear_prefill_backward(
         _ptr(Q, "Q"), _ptr(K, "K"), _ptr(V, "V"), _ptr(eta, "eta", torch.float32),
-        _ptr(W_hist, "W_hist", torch.float32), _ptr(dZ, "dZ"), _ptr(dW_T, "dW_T", torch.float32), _ptr(dQ, "dQ"),
+        _ptr(W_hist, "W_hist", Q.dtype), _ptr(dZ, "dZ"), _ptr(dW_T, "dW_T", torch.float32), _ptr(dQ, "dQ"),
         _ptr(dK, "dK"), _ptr(dV, "dV"), _ptr(deta, "deta", torch.float32), _ptr(dW0, "dW0", torch.float32),
         B, H, T, d, int(chunk), dt, _stream(stream))
     _check(st)
@@ -243,7 +244,7 @@ def linear_prefill_hist(Q, K, V, eta, W0, chunk: int, stream=None):
     B, H, T, d = Q.shape
     Z = torch.empty_like(Q)
     W = torch.empty_like(W0)
-    Wh = torch.empty((B, H, -(-T // int(chunk)), d, d), dtype=torch.float32, device=Q.device)
+    Wh = torch.empty((B, H, -(-T // int(chunk)), d, d), dtype=Q.dtype, device=Q.device)
     ttt_linear_prefill_hist(Q, K, V, eta, W0, Z, W, Wh, chunk, stream)
     return Z, W, Wh
 
