@@ -37,6 +37,8 @@ from test_sequence_layers_07_b300 import workloads as WL  # noqa: E402
 
 METRIC = "TTT-Linear/MLP prefill tokens/s & % roofline; decode tokens/s & HBM GB/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+# the B300's rated figures: HBM3e bandwidth and dense bf16 tensor throughput
+RATED_PEAKS = {"hbm_gbs": 7700.0, "bf16_tflops": 2250.0}
 NROT = 4  # rotating input copies for the L2-sized workloads
 
 
@@ -48,6 +50,11 @@ def load_peaks():
         d = json.load(open(p))
         return d, "measured"
     return dict(FALLBACK_PEAKS), "fallback"
+
+
+def rated_roof(nbytes, flops):
+    """Roofline time (s) against the rated peaks instead of the measured ones."""
+    return max(nbytes / (RATED_PEAKS["hbm_gbs"] * 1e9), flops / (RATED_PEAKS["bf16_tflops"] * 1e12))
 
 
 def linear_bytes(B, H, T, d, elt=2):
@@ -281,7 +288,8 @@ def bench_linear(T_mod, w, chunk, steps, warmup, world, peaks, sampler=None, nro
     return {"tokens_per_s": toks / (ms * 1e-3), "ms_per_step": ms, "ms_per_launch": ms_launch,
             "bytes_per_launch": nbytes, "flops_per_launch": flops,
             "achieved_gbs": nbytes / (ms_launch * 1e-3) / 1e9, "roofline_us": t_roof * 1e6,
-            "frac": t_roof / (ms_launch * 1e-3), "bound": "hbm"}
+            "frac": t_roof / (ms_launch * 1e-3), "bound": "hbm",
+            "frac_of_rated": rated_roof(nbytes, flops) / (ms_launch * 1e-3)}
 
 
 def bench_mlp(T_mod, w, steps, warmup, world, peaks):
@@ -302,7 +310,8 @@ def bench_mlp(T_mod, w, steps, warmup, world, peaks):
     return {"tokens_per_s": w.B * w.T / (ms * 1e-3), "ms_per_step": ms, "ms_per_launch": ms_launch,
             "flops_per_launch": flops, "bytes_per_launch": nbytes,
             "achieved_tflops": flops / (ms_launch * 1e-3) / 1e12, "roofline_us": max(t_tensor, t_hbm) * 1e6,
-            "frac": max(t_tensor, t_hbm) / (ms_launch * 1e-3), "bound": "tensor" if t_tensor > t_hbm else "hbm"}
+            "frac": max(t_tensor, t_hbm) / (ms_launch * 1e-3), "bound": "tensor" if t_tensor > t_hbm else "hbm",
+            "frac_of_rated": rated_roof(nbytes, flops) / (ms_launch * 1e-3)}
 
 
 def backward_bytes(B, H, T, d, chunk, elt=2):
@@ -352,6 +361,7 @@ def bench_backward(T_mod, w, steps, warmup, world, peaks, nrot=2):
             "forward_hist_ms_per_launch": ms_f_launch, "backward_ms_per_launch": ms_b_launch,
             "backward_bytes_per_launch": nbytes, "backward_flops_per_launch": flops,
             "backward_roofline_us": t_roof * 1e6, "backward_frac": t_roof / (ms_b_launch * 1e-3),
+            "backward_frac_of_rated": rated_roof(nbytes, flops) / (ms_b_launch * 1e-3),
             "bound": "hbm" if nbytes / (peaks["hbm_gbs"] * 1e9) > flops / (peaks["bf16_tflops"] * 1e12) else "tensor"}
 
 
@@ -380,7 +390,8 @@ def bench_decode(T_mod, w, steps, warmup, world, peaks, graph_steps=1024, nrot=N
     return {"tokens_per_s": w.B / (per_step * 1e-3), "us_per_step": per_step * 1e3, "graph_steps": graph_steps,
             "bytes_per_step": nbytes, "achieved_gbs": nbytes / (per_step * 1e-3) / 1e9,
             "state_gbs": state_bytes / (per_step * 1e-3) / 1e9, "roofline_us": t_roof * 1e6,
-            "frac": t_roof / (per_step * 1e-3), "bound": "hbm", "state_copies": nrot}
+            "frac": t_roof / (per_step * 1e-3), "bound": "hbm", "state_copies": nrot,
+            "frac_of_rated": rated_roof(nbytes, 0) / (per_step * 1e-3)}
 
 
 def mlp_decode_bytes(B, H, d, hd, elt=2):
@@ -413,7 +424,8 @@ def bench_mlp_decode(T_mod, w, steps, warmup, world, peaks, graph_steps=256, nro
     t_roof = nbytes / (peaks["hbm_gbs"] * 1e9)
     return {"tokens_per_s": w.B / (per_step * 1e-3), "us_per_step": per_step * 1e3, "graph_steps": graph_steps,
             "bytes_per_step": nbytes, "achieved_gbs": nbytes / (per_step * 1e-3) / 1e9,
-            "roofline_us": t_roof * 1e6, "frac": t_roof / (per_step * 1e-3), "bound": "hbm", "state_copies": nrot}
+            "roofline_us": t_roof * 1e6, "frac": t_roof / (per_step * 1e-3), "bound": "hbm", "state_copies": nrot,
+            "frac_of_rated": rated_roof(nbytes, 0) / (per_step * 1e-3)}
 
 
 def bench_e2e(T_mod, w, steps, warmup, world):
@@ -440,13 +452,46 @@ def bench_e2e(T_mod, w, steps, warmup, world):
             "d2h_bytes_per_step": d2h, "ms_per_step": ms}
 
 
-def cpu_baseline(w, target_s=12.0, heads=None):
-    """The fp64 oracle (dual form) on a sample of the workload's heads, scaled to tokens/s."""
-    from oracle import oracle as O
+def cpu_model() -> str:
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.processor() or "unknown"
+
+
+def oracle_single_thread(O, flat, chunk, T):
+    """tokens/s of the oracle's dual form on one sequence with one thread (restores the count)."""
+    n0 = O.num_threads()
+    O.set_num_threads(1)
+    try:
+        one = {k: v[:, :1] for k, v in flat.items()}
+        t0 = time.perf_counter()
+        O.linear_dual(one["Q"], one["K"], one["V"], one["eta"], one["W0"], chunk)
+        dt = time.perf_counter() - t0
+    finally:
+        O.set_num_threads(n0)
+    return {"value": T / dt, "unit": "tokens/s", "cores": 1, "seconds": dt,
+            "sample": f"fp64 dual form on 1 sequence ({T} tokens), 1 thread"}
+
+
+def oracle_flat(w):
     x = WL.workload_inputs(w)
     r = {k: WL.to_f64(v) for k, v in x.items()}
     BH = w.B * w.H
-    flat = {k: v.reshape((1, BH) + v.shape[2:]) for k, v in r.items()}
+    return {k: v.reshape((1, BH) + v.shape[2:]) for k, v in r.items()}
+
+
+def cpu_baseline(w, target_s=12.0, heads=None):
+    """The fp64 oracle (dual form) on a sample of the workload's heads (all of them when they fit in
+    about target_s seconds), plus the same oracle on one thread and the CPU model."""
+    from oracle import oracle as O
+    flat = oracle_flat(w)
+    BH = w.B * w.H
     n = heads or 1
     while True:
         sub = {k: v[:, :n] for k, v in flat.items()}
@@ -456,10 +501,10 @@ def cpu_baseline(w, target_s=12.0, heads=None):
         if heads or dt * 2 >= target_s or n >= BH:
             break
         n = min(BH, max(n + 1, int(n * min(8.0, target_s / max(dt, 1e-3)))))
-    full_s = dt * BH / n
-    return {"value": w.B * w.T / full_s, "unit": "tokens/s", "cores": O.num_threads(), "kind": "oracle",
+    return {"value": n * w.T / dt, "unit": "tokens/s", "cores": O.num_threads(), "kind": "oracle",
             "sample": f"fp64 dual form on {n} of {BH} (batch, head) sequences of the {w.name} workload "
-                      f"({w.T} tokens each, {dt:.2f} s), scaled to all {BH}", "seconds": dt}
+                      f"({w.T} tokens each, {dt:.2f} s)", "seconds": dt, "cpu_model": cpu_model(),
+            "single_thread": oracle_single_thread(O, flat, w.chunk, w.T)}
 
 
 def run_ours(args):
@@ -486,7 +531,9 @@ def run_ours(args):
         "roofline": {"bound": "hbm", "achieved": head["achieved_gbs"],
                      "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": head["achieved_gbs"] / peaks["hbm_gbs"],
                      "traffic": ncu_traffic("linear_prefill", LINEAR_SRC),
-                     "peak_kind": f"{peaks_kind} copy bandwidth", "bytes_per_launch": head["bytes_per_launch"],
+                     "peak_kind": f"{peaks_kind} copy bandwidth",
+                     "frac_of_rated": head["achieved_gbs"] / RATED_PEAKS["hbm_gbs"],
+                     "rated_peak": RATED_PEAKS["hbm_gbs"], "bytes_per_launch": head["bytes_per_launch"],
                      "ms_per_launch": head["ms_per_launch"]},
         "clocks": clocks,
         "gpu_launches": args.steps,
@@ -521,17 +568,26 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
-def run_reference(args):
+def run_reference(args, budget_s=150.0):
+    """The fp64 oracle's dual form on the host cores, timed per step.  A step is the whole headline
+    workload (all B*H sequences) when warm-up + steps fit in about budget_s seconds, else the largest
+    whole multiple of the thread count of its sequences that does (every core busy); the line
+    reports the measured time of those steps and the tokens they processed, not an extrapolation."""
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
     from oracle import oracle as O
     w = WL.WORKLOADS["linear_prefill"]
-    x = WL.workload_inputs(w)
-    r = {k: WL.to_f64(v) for k, v in x.items()}
+    flat = oracle_flat(w)
     BH = w.B * w.H
-    flat = {k: v.reshape((1, BH) + v.shape[2:]) for k, v in r.items()}
-    n = 2  # sequences per step: keeps the whole run within a few minutes
+    cores = O.num_threads()
+    t0 = time.perf_counter()  # calibration: one untimed pass over every sequence
+    O.linear_dual(flat["Q"], flat["K"], flat["V"], flat["eta"], flat["W0"], w.chunk)
+    per_seq = (time.perf_counter() - t0) / BH
+    n = BH
+    if (args.warmup + args.steps) * per_seq * BH > budget_s:
+        n = int(budget_s / ((args.warmup + args.steps) * per_seq))
+        n = min(BH, max(min(cores, BH), n // cores * cores))
     sub = {k: v[:, :n] for k, v in flat.items()}
     times = []
     for i in range(args.warmup + args.steps):
@@ -539,16 +595,18 @@ def run_reference(args):
         O.linear_dual(sub["Q"], sub["K"], sub["V"], sub["eta"], sub["W0"], w.chunk)
         if i >= args.warmup:
             times.append(time.perf_counter() - t0)
-    step_s = sum(times) / len(times) * BH / n  # scaled to the whole workload
-    value = w.B * w.T / step_s
-    sample = f"fp64 oracle dual form on {n} of {BH} sequences per step, scaled to all {BH}"
+    step_s = sum(times) / len(times)
+    value = n * w.T / step_s
+    sample = (f"fp64 oracle dual form on {n} of the {BH} sequences of the workload per step "
+              f"({n * w.T} tokens), {cores} threads")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": 1,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_s * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": "TTT-Linear prefill B=8 H=12 d=64 T=2048 chunk=16", "global_batch": w.B,
-                       "seq_len": w.T},
-            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": O.num_threads(), "kind": "oracle",
-                             "sample": sample},
+                       "seq_len": w.T, "sequences_per_step": n, "tokens_per_step": n * w.T},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                             "sample": sample, "cpu_model": cpu_model(),
+                             "single_thread": oracle_single_thread(O, flat, w.chunk, w.T)},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 

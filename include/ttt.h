@@ -92,7 +92,10 @@ typedef enum ttt_dtype {
  * environment variable TTT_LINEAR_PREFILL_KERNEL = "fused", "tc", "mma" or
  * "generic" starts the choice at that kernel ("tc": d = 64 with the read-out
  * as tcgen05 products; a kernel that does not cover the shape passes it on).
- * All give the same result up to rounding.
+ * All give the same result up to rounding.  TTT_WAIT_LIMIT_NS (diagnostic,
+ * 1 ns .. 4 s) bounds the barrier waits of the d = 64 fused kernel: a tiny
+ * bound makes them expire, which exercises the failure path (TTT_ERR_TIMEOUT in
+ * the device status word, every warp leaves, copies in flight are drained).
  *
  * Source: "Test-Time Training Layers ...", sections "The Core Mechanism" and
  * "Hardware Parallelization"; TTT essay, paragraph on the dual form.

@@ -159,6 +159,11 @@ linear_backward_mma_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid
         }
         return true;
     };
+    // the same wait taken by a whole warp, with a warp-uniform outcome: lanes must never part ways
+    // before the warp-wide ldmatrix / mma.sync that follow
+    auto wait_all = [&](uint64_t& bar, uint32_t parity) -> bool {
+        return __all_sync(0xffffffffu, wait(bar, parity));
+    };
 
     // ldmatrix offsets inside a [16][64] tile, k-step ks:
     //  off_nk: tiles (rows 0-7, k lo), (rows 0-7, k hi), (rows 8-15, k lo), (rows 8-15, k hi): the B
@@ -204,7 +209,7 @@ linear_backward_mma_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid
         // ------------------------------------------------------------ scores: X = K Q^T (rows key j, cols query i)
         for (int si = 0; si < nstg; ++si) {
             const int s = si % NST, n = subs_in(si);
-            if (!__all_sync(0xffffffffu, wait(full_bar[s], (si / NST) & 1))) break;
+            if (!wait_all(full_bar[s], (si / NST) & 1)) break;
             const uint32_t st = sbase + s * STAGE;
             for (int i = 0; i < n; ++i) {
                 float x0[2][4] = {}, x1[2][4] = {};
@@ -280,7 +285,7 @@ linear_backward_mma_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid
             const float2 b = *reinterpret_cast<const float2*>(es + 8 + 2 * t);
             e0 = a.x; e1 = a.y; e2 = b.x; e3 = b.y;
         };
-        bool ok = wait(full_bar[0], 0) && wait(sc_bar[0], 0);
+        bool ok = wait_all(full_bar[0], 0) && wait_all(sc_bar[0], 0);
         if (ok) load(0, 0, subs_in(0));
         for (int si = 0; ok && si < nstg; ++si) {
             const int s = si % NST, n = subs_in(si);
@@ -342,7 +347,7 @@ linear_backward_mma_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid
             if (si + 1 < nstg) {
                 const int s1 = (si + 1) % NST;
                 const uint32_t par = ((si + 1) / NST) & 1;
-                ok = wait(full_bar[s1], par) && wait(sc_bar[s1], par);
+                ok = wait_all(full_bar[s1], par) && wait_all(sc_bar[s1], par);
                 if (ok) load(s1, 0, subs_in(si + 1));
             }
         }

@@ -18,8 +18,8 @@
 //        into it in fp32.
 //    G itself, packed as the A operand of that update, is also the B operand of the read-out's
 //    correction S G^T (S the masked scores), so the error never leaves the registers either.
-//  * Measured on B300, the warp-level MMAs of all four SM sub-partitions share one rate of about
-//    one m16n8k16 per 6 cycles per SM, so the number of MMAs per SM sets the time.  Per 16-token
+//  * Measured on B300, a warp-level m16n8k16 issues at one per ~8.3 cycles per SM sub-partition
+//    (~2.1 cycles per SM over the four), so the MMAs per sub-partition bound the time.  Per 16-token
 //    sub-block a warp issues 26: 8 for K W, 8 for the update, 8 for Q W and 2 for the correction;
 //    the masked scores tril(Q K^T) (8 MMAs per sub-block, the same for every column group) are
 //    computed once per CTA: at the start of a stage each warp forms those of every CG-th
@@ -37,8 +37,9 @@
 //    eta by a bulk copy into an NST-stage mbarrier ring of SPS sub-blocks per stage.  Each mbarrier
 //    wait costs a warp ~230 cycles even when the phase has completed, hence the large stages
 //    (two waits per stage and warp: data landed, scores written).
-//  * All waits are bounded; on expiry the kernel records TTT_ERR_TIMEOUT, every warp leaves its
-//    loop, and the producer drains its copies before the CTA exits.
+//  * All waits are bounded (by `wait_ns`, normally 4 s); on expiry the kernel records
+//    TTT_ERR_TIMEOUT, every warp leaves its loop, and the producer drains its copies (with the
+//    4 s bound, whatever `wait_ns` is) before the CTA exits.
 #include <cuda.h>
 
 #include "ptx.cuh"
@@ -91,7 +92,7 @@ __global__ void __launch_bounds__(FusedCfg<D, CG, NST, SPS>::THREADS, 1)
 linear_prefill_fused_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                             const __grid_constant__ CUtensorMap tmV, const float* __restrict__ eta,
                             const float* W0, __nv_bfloat16* __restrict__ Z, float* W_out, int T, int chunk,
-                            int* status, __nv_bfloat16* __restrict__ W_hist) {
+                            int* status, __nv_bfloat16* __restrict__ W_hist, uint64_t wait_ns) {
     using C = FusedCfg<D, CG, NST, SPS>;
     constexpr int KS = C::KS, NT = C::NT;
 
@@ -125,12 +126,17 @@ linear_prefill_fused_kernel(const __grid_constant__ CUtensorMap tmQ, const __gri
     __syncthreads();
 
     auto wait = [&](uint64_t& bar, uint32_t parity) -> bool {
-        if (s_err || !mbar_wait_bounded(smem_u32(&bar), parity, &s_err, kWaitLimitNs)) {
+        if (s_err || !mbar_wait_bounded(smem_u32(&bar), parity, &s_err, wait_ns)) {
             if (!s_err) record_status(status, kStatusTimeout);
             s_err = 1;
             return false;
         }
         return true;
+    };
+    // the same wait taken by a whole warp, with a warp-uniform outcome: lanes must never part ways
+    // before the warp-wide ldmatrix / mma.sync that follow
+    auto wait_all = [&](uint64_t& bar, uint32_t parity) -> bool {
+        return __all_sync(0xffffffffu, wait(bar, parity));
     };
     auto subs_in = [&](int si) { return nsb - si * SPS < SPS ? nsb - si * SPS : SPS; };
 
@@ -236,7 +242,7 @@ linear_prefill_fused_kernel(const __grid_constant__ CUtensorMap tmQ, const __gri
             const uint32_t par = (si / NST) & 1;
             const uint32_t st = sbase + s * C::STAGE;
             uint8_t* sc = smem + C::SC_OFF + s * SPS * 512;
-            if (!(ok = wait(full_bar[s], par))) break;
+            if (!(ok = wait_all(full_bar[s], par))) break;
             // this warp's share of the stage's masked scores S = tril(Q K^T), as A fragments
             // (rows query i, cols key j); the second fragment buffers serve as scratch
             for (int i = cg; i < n; i += CG) {
@@ -265,7 +271,7 @@ linear_prefill_fused_kernel(const __grid_constant__ CUtensorMap tmQ, const __gri
             if (lane == 0) mbar_arrive(smem_u32(&sc_bar[s]));
             load_kq(0, st, 0);
             load_kt(st, 0);
-            if (!(ok = wait(sc_bar[s], par))) break;
+            if (!(ok = wait_all(sc_bar[s], par))) break;
             // one 16-token sub-block; n is a compile-time SPS on full stages, so their loop body
             // has no branches and the compiler schedules across sub-blocks
             auto step = [&](const int i, const int n) {
@@ -400,7 +406,8 @@ cudaError_t launch_cfg(const LinearArgs& a, cudaStream_t s, int* status) {
     if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) != cudaSuccess) return e;
     dim3 grid(unsigned(a.B) * unsigned(a.H), D / 16 / CG);
     kern<<<grid, C::THREADS, bytes, s>>>(mq, mk, mv, a.eta, a.W0, static_cast<__nv_bfloat16*>(a.Z), a.W_out, a.T,
-                                         a.chunk, status, static_cast<__nv_bfloat16*>(a.W_hist));
+                                         a.chunk, status, static_cast<__nv_bfloat16*>(a.W_hist),
+                                         a.wait_ns ? a.wait_ns : kWaitLimitNs);
     return cudaGetLastError();
 }
 

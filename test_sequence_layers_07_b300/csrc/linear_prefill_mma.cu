@@ -139,6 +139,11 @@ linear_prefill_mma_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_
         }
         return true;
     };
+    // the same wait taken by a whole warp, with a warp-uniform outcome: lanes must never part ways
+    // before the warp-wide ldmatrix / mma.sync that follow
+    auto wait_all = [&](uint64_t& bar, uint32_t parity) -> bool {
+        return __all_sync(0xffffffffu, wait(bar, parity));
+    };
     auto subs_in = [&](int si) { return nsb - si * SPS < SPS ? nsb - si * SPS : SPS; };
 
     // lane-dependent ldmatrix coordinates (byte offsets inside a sub-tile)
@@ -184,7 +189,7 @@ linear_prefill_mma_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_
         const bool m0 = 2 * t <= g, m1 = 2 * t + 1 <= g;
         for (int si = 0; si < nstg; ++si) {
             const int s = si % NST, n = subs_in(si);
-            if (!wait(full_bar[s], (si / NST) & 1)) break;
+            if (!wait_all(full_bar[s], (si / NST) & 1)) break;
             const uint32_t st = sbase + s * C::STAGE;
             for (int i = 0; i < n; ++i) {
                 float sc[2][4] = {}, sd[2][4] = {};
@@ -257,7 +262,7 @@ linear_prefill_mma_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_
                 nv[4] = e23.x * bf16_lo(vv[2]); nv[5] = e23.y * bf16_hi(vv[2]);
                 nv[6] = e23.x * bf16_lo(vv[3]); nv[7] = e23.y * bf16_hi(vv[3]);
             };
-            bool ok = wait(full_bar[0], 0);
+            bool ok = wait_all(full_bar[0], 0);
             if (ok) load(sbase, 0);
             for (int si = 0; ok && si < nstg; ++si) {
                 const int s = si % NST, n = subs_in(si), x = si % NX;
@@ -321,7 +326,7 @@ linear_prefill_mma_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_
                 if (lane == 0) mbar_arrive(smem_u32(&xf_bar[cg][x]));
                 if (si + 1 < nstg) {
                     const int s1 = (si + 1) % NST;
-                    ok = wait(full_bar[s1], ((si + 1) / NST) & 1);
+                    ok = wait_all(full_bar[s1], ((si + 1) / NST) & 1);
                     if (ok) load(sbase + s1 * C::STAGE, 0);
                 }
             }
@@ -345,7 +350,8 @@ linear_prefill_mma_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_
             for (int si = 0; si < nstg; ++si) {
                 const int s = si % NST, n = subs_in(si), x = si % NX;
                 const uint32_t par = (si / NST) & 1;
-                if (!wait(full_bar[s], par) || !wait(sc_bar[s], par) || !wait(xf_bar[cg][x], (si / NX) & 1)) break;
+                if (!wait_all(full_bar[s], par) || !wait_all(sc_bar[s], par) || !wait_all(xf_bar[cg][x], (si / NX) & 1))
+                    break;
                 const uint32_t st = sbase + s * C::STAGE;
                 const uint8_t* gin = gslots + x * SPS * 512;
                 auto step = [&](int i) {

@@ -184,6 +184,11 @@ linear_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_c
         }
         return true;
     };
+    // the same wait taken by a whole warp, with a warp-uniform outcome: lanes must never part ways
+    // before the warp-wide ldmatrix / mma.sync that follow
+    auto wait_all = [&](uint64_t& bar, uint32_t parity) -> bool {
+        return __all_sync(0xffffffffu, wait(bar, parity));
+    };
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
@@ -287,7 +292,7 @@ linear_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_c
             nv[4] = e23.x * bf16_lo(vv[2]); nv[5] = e23.y * bf16_hi(vv[2]);
             nv[6] = e23.x * bf16_lo(vv[3]); nv[7] = e23.y * bf16_hi(vv[3]);
         };
-        bool ok = wait(full_bar[0], 0);
+        bool ok = wait_all(full_bar[0], 0);
         if (ok) load(sbase, 0);
         for (int si = 0; ok && si < nstg; ++si) {
             const int n = subs_in(si);
@@ -337,7 +342,7 @@ linear_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_c
             if (si + 1 < nstg) {
                 // the next slot is filled (so its previous stage is fully consumed): load its first
                 // fragments and publish its start state
-                ok = wait(full_bar[(si + 1) % NST], ((si + 1) / NST) & 1);
+                ok = wait_all(full_bar[(si + 1) % NST], ((si + 1) / NST) & 1);
                 if (ok) {
                     load(slot(si + 1), 0);
                     store_ws(slot(si + 1));
@@ -364,7 +369,7 @@ linear_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_c
         for (int si = 0; si < nstg; ++si) {
             const int x = si & 1;
             const uint32_t buf = tl + x * TM_BUF;
-            if (!__all_sync(0xffffffffu, wait(s_bar[x], (si >> 1) & 1))) break;
+            if (!wait_all(s_bar[x], (si >> 1) & 1)) break;
             tc::fence_after_sync();
             // P = bf16(S) with key k > query row zeroed, written over the S columns already read
 #pragma unroll
@@ -390,7 +395,7 @@ linear_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_c
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&p_bar[x]));
 
-            if (!__all_sync(0xffffffffu, wait(z_bar[x], (si >> 1) & 1))) break;
+            if (!wait_all(z_bar[x], (si >> 1) & 1)) break;
             tc::fence_after_sync();
             float z[64];
 #pragma unroll

@@ -6,7 +6,6 @@
 // and dtype only; there is exactly one implementation per shape.
 #include <cuda_runtime.h>
 
-#include <mutex>
 #include <stdio.h>
 #include <stdlib.h>
 #include <string.h>
@@ -34,27 +33,28 @@ bool supported_d(int d) { return d == 16 || d == 32 || d == 64 || d == 128; }
 
 // Device status word: written by kernels (first error wins), read and cleared
 // by ttt_get_device_status().  One copy per device (a __device__ variable is
-// instantiated in every context that loads the module).
+// instantiated in every context that loads the module).  Its address is looked
+// up on every call, in the context current then, so no address outlives a
+// device reset or a re-created primary context.
 __device__ int g_device_status;
 
-constexpr int kMaxDevices = 64;
-std::mutex g_status_mu;
-int* g_status_ptr[kMaxDevices] = {};
-
 cudaError_t status_ptr(int** out) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    void* p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_device_status);
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-    std::lock_guard<std::mutex> lk(g_status_mu);
-    if (!g_status_ptr[dev]) {
-        void* p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_device_status);
-        if (e != cudaSuccess) return e;
-        g_status_ptr[dev] = static_cast<int*>(p);
-    }
-    *out = g_status_ptr[dev];
+    *out = static_cast<int*>(p);
     return cudaSuccess;
+}
+
+// Diagnostic bound of the fused TTT-Linear prefill's barrier waits, from the environment variable
+// TTT_WAIT_LIMIT_NS (1 ns .. 4 s; 0 or unset: the default 4 s).  A tiny bound makes a real
+// prefill's waits expire, which exercises its failure path (status word, clean exit) without
+// faulting anything.
+uint64_t wait_limit_from_env() {
+    const char* v = getenv("TTT_WAIT_LIMIT_NS");
+    if (!v) return 0;
+    const unsigned long long n = strtoull(v, nullptr, 10);
+    return n > 4000000000ull ? 4000000000ull : n;
 }
 
 #define CHECK_PTR(p)                                                              \
@@ -106,6 +106,7 @@ ttt_status ttt_linear_prefill(const void* Q, const void* K, const void* V, const
     CHECK_PTR(eta);
     CHECK_PTR(Z);
     ttt::LinearArgs a{Q, K, V, eta, W0, Z, W_out, B, H, T, d, chunk, dtype == TTT_BF16 ? 1 : 0};
+    a.wait_ns = wait_limit_from_env();
     int* status = nullptr;
     cudaError_t e = status_ptr(&status);
     if (e != cudaSuccess) return cuda_fail(e, "ttt_linear_prefill status word");

@@ -21,6 +21,7 @@ struct LinearArgs {
     int bf16;                // 1: Q/K/V/Z are bfloat16, 0: float32
     void* W_hist = nullptr;  // optional: the state at the start of every block, [B][H][nblk][d][d],
                              // in the element type of Q (bf16: the state rounded RN-even)
+    uint64_t wait_ns = 0;    // bound of the fused kernel's barrier waits (0: the default 4 s)
 };
 
 // Gradient of the TTT-Linear chunked scan (outer-loop training).

@@ -13,6 +13,11 @@ def pytest_configure(config):
     config.addinivalue_line("markers", "slow: longer CPU test")
 
 
+def pytest_sessionfinish(session, exitstatus):
+    from tests._parity import MARGINS
+    MARGINS.dump()
+
+
 @pytest.fixture(scope="session")
 def golden_dir():
     return os.path.join(ROOT, "tests", "golden")

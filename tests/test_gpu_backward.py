@@ -12,7 +12,7 @@ import torch
 from oracle import oracle as O
 from test_sequence_layers_07_b300 import ttt as T
 from test_sequence_layers_07_b300 import workloads as WL
-from tests._parity import TOL, cuda, f64, heads, rel_err
+from tests._parity import TOL, check, cuda, f64, rel_err
 
 pytestmark = pytest.mark.gpu
 
@@ -113,21 +113,19 @@ def test_recorded_states_tensor_core_forward(d):
         assert rel_err(Wh[:, :, n], Wn) <= TOL["bf16"]
 
 
-def test_backward_headline_shape_sampled_heads():
-    # B=8 H=12 d=64 T=2048 chunk=16 bf16: every head on the GPU, six heads against the oracle
+def test_backward_headline_shape_all_heads():
+    # B=8 H=12 d=64 T=2048 chunk=16 bf16: every element of dQ, dK, dV, deta and dW0 of all 96
+    # sequences, and the recording forward's Z and final state, against the oracle
     w = WL.WORKLOADS["linear_prefill"]
     x = WL.workload_inputs(w)
     g = WL.backward_inputs(w.B, w.H, w.T, w.d, seed=w.seed + 100, dtype=w.dtype)
-    _, _, _, grads = _run(x, g, w.chunk)
-    for t in grads:
-        assert torch.isfinite(t.float()).all()
-    idx = [(0, 0), (3, 7), (7, 11), (5, 2), (1, 9), (6, 5)]
-    xs = heads(f64(x), idx)
-    gs = heads({"dZ": WL.to_f64(g["dZ"]), "dWT": WL.to_f64(g["dWT"])}, idx)
-    ref = O.linear_backward(xs["Q"], xs["K"], xs["V"], xs["eta"], xs["W0"], gs["dZ"], gs["dWT"], w.chunk)
-    for name, got, want in zip(("dQ", "dK", "dV", "deta", "dW0"), grads, ref):
-        sel = torch.stack([got[b, h] for b, h in idx])[None]
-        assert rel_err(sel, want) <= TOL["bf16"], name
+    Z, W, _, grads = _run(x, g, w.chunk)
+    r = f64(x)
+    Zr, Wr = O.linear_dual(r["Q"], r["K"], r["V"], r["eta"], r["W0"], w.chunk)
+    ref = _oracle(x, g, w.chunk)
+    check("linear_backward B=8 H=12 d=64 T=2048 b=16 (recording forward, gradients)", TOL["bf16"],
+          Z=(Z, Zr), W=(W, Wr), **{n: (got, want) for n, got, want in
+                                   zip(("dQ", "dK", "dV", "deta", "dW0"), grads, ref)})
 
 
 def test_backward_without_tokens_passes_the_state_gradient_through():
