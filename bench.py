@@ -464,8 +464,9 @@ def cpu_model() -> str:
     return platform.processor() or "unknown"
 
 
-def oracle_single_thread(O, flat, chunk, T):
-    """tokens/s of the oracle's dual form on one sequence with one thread (restores the count)."""
+def oracle_single_thread(O, flat, chunk, T, H):
+    """tokens/s of the oracle's dual form on one (batch, head) sequence with one thread (restores the
+    count); a token carries H heads, so one sequence of T tokens is T / H tokens of the workload."""
     n0 = O.num_threads()
     O.set_num_threads(1)
     try:
@@ -475,8 +476,8 @@ def oracle_single_thread(O, flat, chunk, T):
         dt = time.perf_counter() - t0
     finally:
         O.set_num_threads(n0)
-    return {"value": T / dt, "unit": "tokens/s", "cores": 1, "seconds": dt,
-            "sample": f"fp64 dual form on 1 sequence ({T} tokens), 1 thread"}
+    return {"value": T / H / dt, "unit": "tokens/s", "cores": 1, "seconds": dt,
+            "sample": f"fp64 dual form on 1 (batch, head) sequence ({T} tokens, one of {H} heads), 1 thread"}
 
 
 def oracle_flat(w):
@@ -501,10 +502,10 @@ def cpu_baseline(w, target_s=12.0, heads=None):
         if heads or dt * 2 >= target_s or n >= BH:
             break
         n = min(BH, max(n + 1, int(n * min(8.0, target_s / max(dt, 1e-3)))))
-    return {"value": n * w.T / dt, "unit": "tokens/s", "cores": O.num_threads(), "kind": "oracle",
+    return {"value": n * w.T / w.H / dt, "unit": "tokens/s", "cores": O.num_threads(), "kind": "oracle",
             "sample": f"fp64 dual form on {n} of {BH} (batch, head) sequences of the {w.name} workload "
                       f"({w.T} tokens each, {dt:.2f} s)", "seconds": dt, "cpu_model": cpu_model(),
-            "single_thread": oracle_single_thread(O, flat, w.chunk, w.T)}
+            "single_thread": oracle_single_thread(O, flat, w.chunk, w.T, w.H)}
 
 
 def run_ours(args):
@@ -596,17 +597,17 @@ def run_reference(args, budget_s=150.0):
         if i >= args.warmup:
             times.append(time.perf_counter() - t0)
     step_s = sum(times) / len(times)
-    value = n * w.T / step_s
-    sample = (f"fp64 oracle dual form on {n} of the {BH} sequences of the workload per step "
-              f"({n * w.T} tokens), {cores} threads")
+    value = n * w.T / w.H / step_s  # a token carries H heads: n sequences are n T / H tokens
+    sample = (f"fp64 oracle dual form on {n} of the {BH} (batch, head) sequences of the workload per step "
+              f"({n * w.T / w.H:g} tokens), {cores} threads")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": 1,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_s * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": "TTT-Linear prefill B=8 H=12 d=64 T=2048 chunk=16", "global_batch": w.B,
-                       "seq_len": w.T, "sequences_per_step": n, "tokens_per_step": n * w.T},
+                       "seq_len": w.T, "sequences_per_step": n, "tokens_per_step": n * w.T / w.H},
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                              "sample": sample, "cpu_model": cpu_model(),
-                             "single_thread": oracle_single_thread(O, flat, w.chunk, w.T)},
+                             "single_thread": oracle_single_thread(O, flat, w.chunk, w.T, w.H)},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
