@@ -270,22 +270,47 @@ def rotating_copies(x: dict, n: int) -> list:
     return [base] + [{k: v.clone() for k, v in base.items()} for _ in range(n - 1)]
 
 
-def bench_linear(T_mod, w, chunk, steps, warmup, world, peaks, sampler=None, nrot=NROT):
+def linear_launches(T_mod, w, chunk, split):
+    """Kernel launches of one prefill call: the split path runs maps, combine and scan (3) when its
+    workspace is non-empty, the one-pass path 1."""
+    if not split:
+        return 1
+    n = T_mod.ttt_linear_prefill_workspace_size(w.B, w.H, w.T, w.d, chunk, WL.torch_dtype(w.dtype))
+    return 3 if n else 1
+
+
+def segments_of(ws, w):
+    """Segment count of a split prefill from its workspace size (B*H*(3S-2)*d*d fp32 words)."""
+    if ws is None:
+        return 1
+    return (ws.numel() // (w.B * w.H * w.d * w.d) + 2) // 3
+
+
+def bench_linear(T_mod, w, chunk, steps, warmup, world, peaks, sampler=None, nrot=NROT, split=True):
+    """One TTT-Linear prefill per step: split along the sequence (ttt_linear_prefill_ws, scratch
+    allocated once, outside the timed region) or the one-pass scan (ttt_linear_prefill)."""
     x = WL.workload_inputs(w)
     sets = rotating_copies(x, nrot)
     outs = [(torch.empty_like(s["Q"]), torch.empty_like(s["W0"])) for s in sets]
+    ws = T_mod.linear_workspace(sets[0]["Q"], chunk) if split else None
 
     def step(i):
         s, (Z, W) = sets[i % nrot], outs[i % nrot]
-        T_mod.ttt_linear_prefill(s["Q"], s["K"], s["V"], s["eta"], s["W0"], Z, W, chunk)
+        if split:
+            T_mod.ttt_linear_prefill_ws(s["Q"], s["K"], s["V"], s["eta"], s["W0"], Z, W, chunk, ws)
+        else:
+            T_mod.ttt_linear_prefill(s["Q"], s["K"], s["V"], s["eta"], s["W0"], Z, W, chunk)
 
     ms, ms_launch = timed_loop(step, steps, warmup, world, sampler=sampler)
     toks = w.B * w.T
     nbytes = linear_bytes(w.B, w.H, w.T, w.d)
     flops = linear_flops(w.B, w.H, w.T, w.d, chunk)
     t_roof = max(nbytes / (peaks["hbm_gbs"] * 1e9), flops / (peaks["bf16_tflops"] * 1e12))
-    del sets, outs
+    del sets, outs, ws
     return {"tokens_per_s": toks / (ms * 1e-3), "ms_per_step": ms, "ms_per_launch": ms_launch,
+            "path": "split along the sequence" if split else "one pass",
+            "segments": segments_of(ws, w) if split else 1,
+            "kernel_launches_per_call": linear_launches(T_mod, w, chunk, split),
             "bytes_per_launch": nbytes, "flops_per_launch": flops,
             "achieved_gbs": nbytes / (ms_launch * 1e-3) / 1e9, "roofline_us": t_roof * 1e6,
             "frac": t_roof / (ms_launch * 1e-3), "bound": "hbm",
@@ -438,10 +463,12 @@ def bench_e2e(T_mod, w, steps, warmup, world):
     Zh = torch.empty_like(host["Q"]).pin_memory()
     Wh = torch.empty_like(host["W0"]).pin_memory()
 
+    ws = T_mod.linear_workspace(dev["Q"], w.chunk)  # scratch, allocated once like any workspace
+
     def step(i):
         for k in dev:
             dev[k].copy_(host[k], non_blocking=True)
-        T_mod.ttt_linear_prefill(dev["Q"], dev["K"], dev["V"], dev["eta"], dev["W0"], Z, W, w.chunk)
+        T_mod.ttt_linear_prefill_ws(dev["Q"], dev["K"], dev["V"], dev["eta"], dev["W0"], Z, W, w.chunk, ws)
         Zh.copy_(Z, non_blocking=True)
         Wh.copy_(W, non_blocking=True)
 
@@ -525,6 +552,7 @@ def run_ours(args):
         "warmup": args.warmup, "ms_per_step": head["ms_per_step"], "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": "TTT-Linear prefill B=8 H=12 d=64 T=2048 chunk=16 (bf16 Q/K/V/Z, fp32 state)",
+                   "path": f"split along the sequence, {head['segments']} segments per (batch, head)",
                    "global_batch": w.B * world, "seq_len": w.T, "heads": w.H, "head_dim": w.d, "chunk": w.chunk,
                    "parallelism": f"dp{world}" if world > 1 else "single-gpu",
                    "l2": f"{NROT} rotating input copies ({NROT * linear_bytes(w.B, w.H, w.T, w.d) / 1e6:.0f} MB > "
@@ -537,13 +565,16 @@ def run_ours(args):
                      "rated_peak": RATED_PEAKS["hbm_gbs"], "bytes_per_launch": head["bytes_per_launch"],
                      "ms_per_launch": head["ms_per_launch"]},
         "clocks": clocks,
-        "gpu_launches": args.steps,
+        "gpu_launches": args.steps * head["kernel_launches_per_call"],
     }
     if not args.no_e2e:
         line["e2e"] = bench_e2e(T_mod, w, max(5, min(200, args.steps // 10)), args.warmup, world)
     if args.rows != "none":
         want = lambda name: args.rows in ("all", name)
         rows = {"linear_prefill": head}
+        if want("linear_prefill_one_pass"):
+            rows["linear_prefill_one_pass"] = bench_linear(T_mod, w, w.chunk, rsteps * 4, args.warmup, world, peaks,
+                                                           split=False)
         rsteps = max(5, min(50, args.steps // 20))
         if want("mlp_prefill"):
             rows["mlp_prefill"] = bench_mlp(T_mod, WL.WORKLOADS["mlp_prefill"], rsteps, args.warmup, world, peaks)
@@ -612,7 +643,7 @@ def run_reference(args, budget_s=150.0):
     print(json.dumps(line), flush=True)
 
 
-LINEAR_SRC = ["linear_prefill_fused.cu", "ptx.cuh"]
+LINEAR_SRC = ["linear_segment.cu", "mma_tile.cuh", "ptx.cuh"]
 
 
 def main(argv=None):
@@ -621,8 +652,8 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--rows", choices=["all", "none", "mlp_prefill", "long_context", "decode", "mlp_decode",
-                                       "backward"],
+    ap.add_argument("--rows", choices=["all", "none", "linear_prefill_one_pass", "mlp_prefill", "long_context",
+                                       "decode", "mlp_decode", "backward"],
                     default="all",
                     help="workload rows timed after the headline (default: all)")
     ap.add_argument("--no-e2e", action="store_true")

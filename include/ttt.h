@@ -55,6 +55,7 @@
 #ifndef TTT_H_
 #define TTT_H_
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -103,6 +104,45 @@ typedef enum ttt_dtype {
 ttt_status ttt_linear_prefill(const void* Q, const void* K, const void* V, const float* eta,
                               const float* W0, void* Z, float* W_out, int B, int H, int T, int d,
                               int chunk, ttt_dtype dtype, void* stream);
+
+/*
+ * TTT-Linear prefill split along the sequence: the same results as
+ * ttt_linear_prefill (same arguments, up to fp32 rounding), for a caller that
+ * supplies scratch memory.  A block's update is affine in its start state,
+ *     W <- (I - K^T diag(eta) K) W + K^T diag(eta) V,
+ * so a run of whole blocks (a segment) maps its start state W_s to
+ * W_s + Delta_s W_s + B_s.  Each (batch, head) is cut into S segments; the
+ * maps of all segments but the last are formed in parallel (the recurrence
+ * from zero with targets -K for Delta_s and V for B_s), combined in order into
+ * every segment's start state (fp32), and every segment is then scanned from
+ * its own start state: S times the parallelism of the one-pass scan.
+ *
+ *   workspace        device scratch of at least
+ *                    ttt_linear_prefill_workspace_size(B, H, T, d, chunk, dtype)
+ *                    bytes, 16-byte aligned, owned by the caller, not shared
+ *                    with a call in flight; contents on return (fp32, P = B*H):
+ *                      maps   [P][S-1][2][d][d]  Delta_s, B_s
+ *                      starts [P][S][d][d]       the start state of every segment
+ *                    (S is chosen from the shape and the SM count, about two
+ *                    segments per SM and at least 256 tokens per segment; the
+ *                    environment variable TTT_LINEAR_SEGMENTS = n asks for n.
+ *                    With nblk = T / chunk blocks, a segment holds
+ *                    L = ceil(nblk / n) blocks, the last one the rest, and
+ *                    S = ceil(nblk / L) <= n)
+ *   workspace_bytes  its size; smaller than needed: TTT_ERR_INVALID_ARG
+ *
+ * Shapes the split covers: bf16, d = 64, 16 | chunk, chunk | T.  For any other
+ * shape, or when a single segment is best, the workspace size is 0 and the call
+ * is ttt_linear_prefill (workspace may then be NULL).  W_out may be W0.
+ * Source: "Test-Time Training Layers ...", sections "The Core Mechanism" (the
+ * step) and "Hardware Parallelization"; TTT essay, paragraph on the dual form.
+ * The affine segment maps are our parallelisation of that scan.
+ */
+size_t ttt_linear_prefill_workspace_size(int B, int H, int T, int d, int chunk, ttt_dtype dtype);
+ttt_status ttt_linear_prefill_ws(const void* Q, const void* K, const void* V, const float* eta,
+                                 const float* W0, void* Z, float* W_out, int B, int H, int T, int d,
+                                 int chunk, ttt_dtype dtype, void* workspace, size_t workspace_bytes,
+                                 void* stream);
 
 /*
  * TTT-Linear prefill that also records the state at the start of every block

@@ -124,6 +124,53 @@ ttt_status ttt_linear_prefill(const void* Q, const void* K, const void* V, const
     return TTT_OK;
 }
 
+// Segment plan of the split prefill for this shape (TTT_LINEAR_SEGMENTS = n asks for n segments).
+static ttt::SegPlan seg_plan_for(const ttt::LinearArgs& a) {
+    const char* v = getenv("TTT_LINEAR_SEGMENTS");
+    const int force = v ? atoi(v) : 0;
+    return ttt::linear_segment_plan(a, force > 0 ? force : 0);
+}
+
+size_t ttt_linear_prefill_workspace_size(int B, int H, int T, int d, int chunk, ttt_dtype dtype) {
+    if (B <= 0 || H <= 0 || T <= 0 || chunk < 1 || chunk > 512 || !supported_d(d) ||
+        (dtype != TTT_F32 && dtype != TTT_BF16))
+        return 0;
+    ttt::LinearArgs a{nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, B, H, T, d, chunk,
+                      dtype == TTT_BF16 ? 1 : 0};
+    return ttt::linear_segment_workspace_bytes(a, seg_plan_for(a));
+}
+
+ttt_status ttt_linear_prefill_ws(const void* Q, const void* K, const void* V, const float* eta, const float* W0,
+                                 void* Z, float* W_out, int B, int H, int T, int d, int chunk, ttt_dtype dtype,
+                                 void* workspace, size_t workspace_bytes, void* stream) {
+    g_last_error[0] = 0;
+    if (B < 0 || H < 0 || T < 0) return fail(TTT_ERR_INVALID_ARG, "negative size%s");
+    if (chunk < 1 || chunk > 512) return fail(TTT_ERR_INVALID_ARG, "chunk must be in 1..512%s");
+    if (dtype != TTT_F32 && dtype != TTT_BF16) return fail(TTT_ERR_INVALID_ARG, "unknown dtype%s");
+    if (d <= 0) return fail(TTT_ERR_INVALID_ARG, "head dim must be positive%s");
+    if (!supported_d(d)) return fail(TTT_ERR_UNSUPPORTED, "head dim must be 16, 32, 64 or 128%s");
+    const size_t need = ttt_linear_prefill_workspace_size(B, H, T, d, chunk, dtype);
+    if (need == 0)  // no split for this shape: the one-pass scan
+        return ttt_linear_prefill(Q, K, V, eta, W0, Z, W_out, B, H, T, d, chunk, dtype, stream);
+    CHECK_PTR(Q);
+    CHECK_PTR(K);
+    CHECK_PTR(V);
+    CHECK_PTR(eta);
+    CHECK_PTR(W0);
+    CHECK_PTR(Z);
+    CHECK_PTR(W_out);
+    if (!workspace || workspace_bytes < need)
+        return fail(TTT_ERR_INVALID_ARG, "workspace smaller than ttt_linear_prefill_workspace_size()%s");
+    CHECK_PTR(workspace);
+    ttt::LinearArgs a{Q, K, V, eta, W0, Z, W_out, B, H, T, d, chunk, dtype == TTT_BF16 ? 1 : 0};
+    int* status = nullptr;
+    cudaError_t e = status_ptr(&status);
+    if (e != cudaSuccess) return cuda_fail(e, "ttt_linear_prefill_ws status word");
+    e = ttt::launch_linear_prefill_segmented(a, seg_plan_for(a), workspace, static_cast<cudaStream_t>(stream), status);
+    if (e != cudaSuccess) return cuda_fail(e, "ttt_linear_prefill_ws launch");
+    return TTT_OK;
+}
+
 ttt_status ttt_linear_prefill_hist(const void* Q, const void* K, const void* V, const float* eta, const float* W0,
                                    void* Z, float* W_out, void* W_hist, int B, int H, int T, int d, int chunk,
                                    ttt_dtype dtype, void* stream) {
@@ -344,6 +391,6 @@ const char* ttt_status_string(ttt_status s) {
 
 const char* ttt_last_error(void) { return g_last_error; }
 
-int ttt_version(void) { return 10300; }
+int ttt_version(void) { return 10400; }
 
 }  // extern "C"

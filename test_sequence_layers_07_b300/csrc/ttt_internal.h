@@ -91,6 +91,20 @@ cudaError_t launch_linear_prefill_generic(const LinearArgs& a, cudaStream_t s);
 cudaError_t launch_mlp_prefill_generic(const MlpArgs& a, cudaStream_t s);
 size_t mlp_generic_smem_bytes(int d, int hidden, int chunk);
 
+// TTT-Linear prefill split along the sequence (bf16, d = 64, 16 | chunk, chunk | T): nseg segments
+// of seg_len tokens (a multiple of chunk; the last may be shorter); maps of every segment but the
+// last, their combination into the segments' start states, then the scan of every segment.
+struct SegPlan {
+    int nseg;
+    int seg_len;
+};
+bool linear_segmented_supported(const LinearArgs& a);
+// force_nseg > 0 asks for that many segments (at most one per block); 0 chooses by SM count.
+SegPlan linear_segment_plan(const LinearArgs& a, int force_nseg);
+size_t linear_segment_workspace_bytes(const LinearArgs& a, const SegPlan& p);
+cudaError_t launch_linear_prefill_segmented(const LinearArgs& a, const SegPlan& p, void* workspace, cudaStream_t s,
+                                            int* status);
+
 // Tensor-core TTT-Linear prefill (bf16, register-resident state).  Returns
 // cudaErrorNotSupported when the shape is not covered, so the caller can use
 // the generic kernel instead.

@@ -25,7 +25,7 @@ LIB_PATH = os.path.join(_PKG, "libttt.so")
 TTT_OK, TTT_ERR_INVALID_ARG, TTT_ERR_UNSUPPORTED, TTT_ERR_CUDA, TTT_ERR_TIMEOUT = range(5)
 TTT_F32, TTT_BF16 = 0, 1
 
-EXPORTED = ("ttt_linear_prefill", "ttt_linear_prefill_hist", "ttt_linear_prefill_backward", "ttt_mlp_prefill",
+EXPORTED = ("ttt_linear_prefill", "ttt_linear_prefill_workspace_size", "ttt_linear_prefill_ws", "ttt_linear_prefill_hist", "ttt_linear_prefill_backward", "ttt_mlp_prefill",
             "ttt_linear_decode_step", "ttt_mlp_decode_step",
             "ttt_get_device_status", "ttt_selftest_wait_timeout", "ttt_status_string", "ttt_last_error", "ttt_version")
 
@@ -52,6 +52,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
             lib = ctypes.CDLL(path)
             vp, fp, i = ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int
             lib.ttt_linear_prefill.argtypes = [vp, vp, vp, fp, fp, vp, fp, i, i, i, i, i, i, vp]
+            lib.ttt_linear_prefill_workspace_size.argtypes = [i, i, i, i, i, i]
+            lib.ttt_linear_prefill_workspace_size.restype = ctypes.c_size_t
+            lib.ttt_linear_prefill_ws.argtypes = [vp, vp, vp, fp, fp, vp, fp, i, i, i, i, i, i, vp, ctypes.c_size_t, vp]
+            lib.ttt_linear_prefill_ws.restype = i
             lib.ttt_linear_prefill_hist.argtypes = [vp, vp, vp, fp, fp, vp, fp, fp, i, i, i, i, i, i, vp]
             lib.ttt_linear_prefill_backward.argtypes = [vp, vp, vp, fp, fp, vp, fp, vp, vp, vp, fp, fp,
                                                         i, i, i, i, i, i, vp]
@@ -122,6 +126,30 @@ def ttt_linear_prefill(Q, K, V, eta, W0, Z, W_out, chunk: int, stream=None) -> N
     st = load_library().ttt_linear_prefill(
         _ptr(Q, "Q"), _ptr(K, "K"), _ptr(V, "V"), _ptr(eta, "eta", torch.float32), _ptr(W0, "W0", torch.float32),
         _ptr(Z, "Z"), _ptr(W_out, "W_out", torch.float32), B, H, T, d, int(chunk), dt, _stream(stream))
+    _check(st)
+
+
+def ttt_linear_prefill_workspace_size(B: int, H: int, T: int, d: int, chunk: int, dtype: torch.dtype) -> int:
+    """Bytes of scratch ttt_linear_prefill_ws needs for this shape (0: it runs the one-pass scan)."""
+    dt = TTT_BF16 if dtype == torch.bfloat16 else TTT_F32
+    return int(load_library().ttt_linear_prefill_workspace_size(B, H, T, d, int(chunk), dt))
+
+
+def ttt_linear_prefill_ws(Q, K, V, eta, W0, Z, W_out, chunk: int, workspace, stream=None) -> None:
+    """TTT-Linear prefill split along the sequence, with caller-owned scratch `workspace` (a CUDA
+    tensor of at least ttt_linear_prefill_workspace_size bytes, or None when that size is 0)."""
+    B, H, T, d = Q.shape
+    dt = _io_dtype(Q)
+    for name, t in (("K", K), ("V", V), ("Z", Z)):
+        if t.shape != Q.shape or t.dtype != Q.dtype:
+            raise ValueError(f"{name} must match Q in shape and dtype")
+    if eta.shape != (B, H, T) or W0.shape != (B, H, d, d) or W_out.shape != (B, H, d, d):
+        raise ValueError("eta must be [B,H,T] and W0/W_out [B,H,d,d]")
+    nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = load_library().ttt_linear_prefill_ws(
+        _ptr(Q, "Q"), _ptr(K, "K"), _ptr(V, "V"), _ptr(eta, "eta", torch.float32), _ptr(W0, "W0", torch.float32),
+        _ptr(Z, "Z"), _ptr(W_out, "W_out", torch.float32), B, H, T, d, int(chunk), dt,
+        _ptr(workspace, "workspace"), nbytes, _stream(stream))
     _check(st)
 
 
@@ -236,6 +264,24 @@ def linear_prefill(Q, K, V, eta, W0, chunk: int, stream=None):
     Z = torch.empty_like(Q)
     W = torch.empty_like(W0)
     ttt_linear_prefill(Q, K, V, eta, W0, Z, W, chunk, stream)
+    return Z, W
+
+
+def linear_workspace(Q, chunk: int):
+    """A scratch buffer for ttt_linear_prefill_ws on Q's shape (None when none is needed)."""
+    B, H, T, d = Q.shape
+    n = ttt_linear_prefill_workspace_size(B, H, T, d, chunk, Q.dtype)
+    return torch.empty(n // 4, dtype=torch.float32, device=Q.device) if n else None
+
+
+def linear_prefill_ws(Q, K, V, eta, W0, chunk: int, workspace=None, stream=None):
+    """Returns (Z, W_final) for the TTT-Linear prefill split along the sequence (scratch allocated by
+    torch when not given)."""
+    if workspace is None:
+        workspace = linear_workspace(Q, chunk)
+    Z = torch.empty_like(Q)
+    W = torch.empty_like(W0)
+    ttt_linear_prefill_ws(Q, K, V, eta, W0, Z, W, chunk, workspace, stream)
     return Z, W
 
 

@@ -198,3 +198,44 @@ def test_missing_library_fails_loudly(tmp_path):
             mod.load_library(str(tmp_path / "libttt.so"))
         finally:
             mod._lib = saved
+
+
+def test_linear_prefill_ws_sizes_and_validation(lib, monkeypatch):
+    monkeypatch.delenv("TTT_LINEAR_SEGMENTS", raising=False)
+    ws = lib.ttt_linear_prefill_workspace_size
+    unit = 64 * 64 * 4
+    n = ws(8, 12, 2048, 64, 16, 1)  # the headline shape is split
+    assert n > 0 and n % (96 * unit) == 0
+    S = (n // (96 * unit) + 2) // 3
+    assert n == 96 * (3 * S - 2) * unit and 2 <= S <= 2048 // 256
+    # shapes outside the split, or too short to split: 0 (the call is the one-pass scan)
+    assert ws(8, 12, 2048, 64, 16, 0) == 0        # fp32
+    assert ws(8, 12, 2048, 128, 16, 1) == 0       # d = 128
+    assert ws(8, 12, 2048, 64, 8, 1) == 0         # chunk not a multiple of 16
+    assert ws(8, 12, 2000, 64, 48, 1) == 0        # chunk does not divide T
+    assert ws(1, 1, 255, 64, 1, 1) == 0
+    assert ws(1, 1, 128, 64, 16, 1) == 0          # under 256 tokens: one segment
+    assert ws(0, 12, 2048, 64, 16, 1) == 0 and ws(8, 12, 0, 64, 16, 1) == 0
+    # an explicit segment count: 10 blocks of 16 in 3 segments of 4, 4, 2 blocks
+    monkeypatch.setenv("TTT_LINEAR_SEGMENTS", "3")
+    assert ws(2, 3, 160, 64, 16, 1) == 6 * (3 * 3 - 2) * unit
+    monkeypatch.setenv("TTT_LINEAR_SEGMENTS", "4")  # 10 blocks: segments of 3 -> 4 segments
+    assert ws(2, 3, 160, 64, 16, 1) == 6 * (3 * 4 - 2) * unit
+    monkeypatch.setenv("TTT_LINEAR_SEGMENTS", "6")  # segments of 2 blocks -> 5 segments
+    assert ws(2, 3, 160, 64, 16, 1) == 6 * (3 * 5 - 2) * unit
+    monkeypatch.setenv("TTT_LINEAR_SEGMENTS", "1")
+    assert ws(8, 12, 2048, 64, 16, 1) == 0
+    monkeypatch.delenv("TTT_LINEAR_SEGMENTS")
+
+    def call(workspace=A, nbytes=n, Q=A, **kw):
+        return lib.ttt_linear_prefill_ws(Q, A, A, A, A, A, A, 8, 12, 2048, 64, 16, 1, workspace, nbytes, None)
+
+    assert call(nbytes=n - 16) == T.TTT_ERR_INVALID_ARG
+    assert b"workspace" in lib.ttt_last_error()
+    assert call(workspace=NULL) == T.TTT_ERR_INVALID_ARG
+    assert call(workspace=MIS) == T.TTT_ERR_INVALID_ARG
+    assert call(Q=NULL) == T.TTT_ERR_INVALID_ARG
+    assert lib.ttt_linear_prefill_ws(A, A, A, A, A, A, A, 8, 12, 2048, 48, 16, 1, A, n, None) == T.TTT_ERR_UNSUPPORTED
+    # nothing to do: no device access even with null pointers and no workspace
+    assert lib.ttt_linear_prefill_ws(NULL, NULL, NULL, NULL, NULL, NULL, NULL, 0, 12, 2048, 64, 16, 1, NULL, 0,
+                                     None) == T.TTT_OK
