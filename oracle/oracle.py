@@ -53,6 +53,10 @@ def _load():
                 f.restype = None
             lib.oracle_linear_backward.argtypes = [dp] * 12 + [i] * 5
             lib.oracle_linear_backward.restype = None
+            lib.oracle_mlp_backward.argtypes = [dp] * 15 + [i] * 6
+            lib.oracle_mlp_backward.restype = None
+            lib.oracle_gelu_second.argtypes = [ctypes.c_double]
+            lib.oracle_gelu_second.restype = ctypes.c_double
             lib.oracle_linear_decode.argtypes = [dp] * 6 + [i] * 3
             lib.oracle_linear_decode.restype = None
             lib.oracle_mlp_token_grad.argtypes = [dp] * 7 + [i] * 2
@@ -157,6 +161,35 @@ def mlp_primal(Q, K, V, eta, W1, W2, chunk):
 def mlp_dual(Q, K, V, eta, W1, W2, chunk):
     """Dual form of the TTT-MLP scan. Returns (Z, W1_final, W2_final)."""
     return _mlp("oracle_mlp_dual", Q, K, V, eta, W1, W2, chunk)
+
+
+def mlp_backward(Q, K, V, eta, W1, W2, dZ, dW1T, dW2T, chunk):
+    """Gradient of the TTT-MLP scan with respect to (Q, K, V, eta, W1_0, W2_0), given dZ and the
+    gradients dW1T, dW2T of the final state (None: zero).  Returns (dQ, dK, dV, deta, dW1, dW2)."""
+    Q, K, V, eta, W1, W2, dZ = (_f64(a) for a in (Q, K, V, eta, W1, W2, dZ))
+    B, H, T, d = Q.shape
+    hd = W1.shape[-1]
+    assert K.shape == V.shape == dZ.shape == Q.shape and eta.shape == (B, H, T)
+    assert W1.shape == (B, H, d, hd) and W2.shape == (B, H, hd, d) and chunk >= 1
+    ptrs = []
+    for g, ref in ((dW1T, W1), (dW2T, W2)):
+        if g is None:
+            ptrs.append(None)
+        else:
+            g = _f64(g)
+            assert g.shape == ref.shape
+            ptrs.append(g)
+    dQ, dK, dV = np.zeros_like(Q), np.zeros_like(Q), np.zeros_like(Q)
+    deta = np.zeros_like(eta)
+    dW1, dW2 = np.zeros_like(W1), np.zeros_like(W2)
+    _load().oracle_mlp_backward(_p(Q), _p(K), _p(V), _p(eta), _p(W1), _p(W2), _p(dZ),
+                                None if ptrs[0] is None else _p(ptrs[0]), None if ptrs[1] is None else _p(ptrs[1]),
+                                _p(dQ), _p(dK), _p(dV), _p(deta), _p(dW1), _p(dW2), B, H, T, d, hd, int(chunk))
+    return dQ, dK, dV, deta, dW1, dW2
+
+
+def gelu_second(x: float) -> float:
+    return _load().oracle_gelu_second(float(x))
 
 
 def linear_decode(q, k, v, eta, W):

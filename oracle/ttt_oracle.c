@@ -553,6 +553,249 @@ void oracle_mlp_dual(const double *Q, const double *K, const double *V, const do
     mlp_all(mlp_dual_head, Q, K, V, eta, W1_0, W2_0, Z, W1, W2, B, H, T, d, hd, chunk);
 }
 
+/* Second derivative of the tanh-form GELU: with u = c (x + a x^3), t = tanh u, u' = c (1 + 3 a x^2),
+ * u'' = 6 a c x:  GELU'' = (1 - t^2) u' + 1/2 x (1 - t^2) (u'' - 2 t u'^2). */
+double oracle_gelu_second(double x)
+{
+    double t = tanh(GELU_C * (x + GELU_A * x * x * x));
+    double u1 = GELU_C * (1.0 + 3.0 * GELU_A * x * x);
+    double u2 = 6.0 * GELU_A * GELU_C * x;
+    double s = 1.0 - t * t;
+    return s * u1 + 0.5 * x * s * (u2 - 2.0 * t * u1 * u1);
+}
+
+/* y[m] = A[m][n] x[n]   (matrix times vector) */
+static void matvec(const double *A, const double *x, double *y, int m, int n)
+{
+    for (int i = 0; i < m; ++i) y[i] = dot(A + (size_t)i * n, x, n);
+}
+
+/*
+ * Gradient of the TTT-MLP scan (outer-loop training through the inner loop: the slow weights learn
+ * the initialisation and the update rule, [ES] paragraph on the two time scales).  Given dZ and the
+ * gradients dW1T, dW2T of the final state (NULL: zero), returns dQ, dK, dV, deta, dW1_0, dW2_0.
+ *
+ * The forward is mlp_dual_head (readings R1-R7), per block with start state (W1, W2), D = diag(eta),
+ * M the causal mask (j <= i), g = GELU:
+ *   Zk = K W1, Hk = g(Zk), E2 = Hk W2 - V, Gk = E2 W2^T, E1 = Gk . g'(Zk),
+ *   A1 = (M . Q K^T) D, Zq = Q W1 - A1 E1, Hq = g(Zq), A2 = (M . Hq Hk^T) D, Z = Hq W2 - A2 E2,
+ *   W1' = W1 - K^T D E1, W2' = W2 - Hk^T D E2.
+ * Its chain rule, block by block in reverse order (dW1', dW2' the gradients of the state after the
+ * block; every d* accumulates):
+ *   W2':  dW2 += dW2';  dHk += -D E2 dW2'^T;  dE2 += -D Hk dW2';  deta_j += -(Hk dW2')_j . E2_j
+ *   W1':  dW1 += dW1';  dK += -D E1 dW1'^T;   dE1 += -D K dW1';   deta_j += -(K dW1')_j . E1_j
+ *   Z:    dHq += dZ W2^T;  dW2 += Hq^T dZ;  dA2 = -dZ E2^T;  dE2 += -A2^T dZ
+ *   A2:   deta_j += sum_i M_ij (Hq Hk^T)_ij dA2_ij;  dHq += (M . dA2 D) Hk;  dHk += (M . dA2 D)^T Hq
+ *   Hq:   dZq = dHq . g'(Zq)
+ *   Zq:   dQ += dZq W1^T;  dW1 += Q^T dZq;  dA1 = -dZq E1^T;  dE1 += -A1^T dZq
+ *   A1:   deta_j += sum_i M_ij (Q K^T)_ij dA1_ij;  dQ += (M . dA1 D) K;  dK += (M . dA1 D)^T Q
+ *   E1:   dGk = dE1 . g'(Zk);  dZk += dE1 . Gk . g''(Zk)
+ *   Gk:   dE2 += dGk W2;  dW2 += dGk^T E2
+ *   E2:   dV = -dE2;  dHk += dE2 W2^T;  dW2 += Hk^T dE2
+ *   Hk:   dZk += dHk . g'(Zk)
+ *   Zk:   dK += dZk W1^T;  dW1 += K^T dZk
+ * The block-start states come from a forward pass over the whole sequence first.
+ * Pinned by central finite differences of the token-level definition (mlp_primal_head).
+ */
+static void mlp_backward_head(const double *Q, const double *K, const double *V, const double *eta,
+                              const double *W1_0, const double *W2_0, const double *dZ,
+                              const double *dW1T, const double *dW2T, double *dQ, double *dK,
+                              double *dV, double *deta, double *dW1_0, double *dW2_0, int T, int d,
+                              int hd, int chunk)
+{
+    int nblk = (T + chunk - 1) / chunk;
+    size_t n1 = (size_t)d * hd, bh_ = (size_t)chunk * hd, bd = (size_t)chunk * d, bb = (size_t)chunk * chunk;
+    double *W1s = xmalloc((size_t)(nblk + 1) * n1 * sizeof(double)); /* block-start W1, W2 */
+    double *W2s = xmalloc((size_t)(nblk + 1) * n1 * sizeof(double));
+    double *Zk = xmalloc(bh_ * sizeof(double)), *Hk = xmalloc(bh_ * sizeof(double));
+    double *Gk = xmalloc(bh_ * sizeof(double)), *E1 = xmalloc(bh_ * sizeof(double));
+    double *Zq = xmalloc(bh_ * sizeof(double)), *Hq = xmalloc(bh_ * sizeof(double));
+    double *dHk = xmalloc(bh_ * sizeof(double)), *dHq = xmalloc(bh_ * sizeof(double));
+    double *dE1 = xmalloc(bh_ * sizeof(double)), *dZq = xmalloc(bh_ * sizeof(double));
+    double *dZk = xmalloc(bh_ * sizeof(double)), *dGk = xmalloc(bh_ * sizeof(double));
+    double *E2 = xmalloc(bd * sizeof(double)), *dE2 = xmalloc(bd * sizeof(double));
+    double *S1 = xmalloc(bb * sizeof(double)), *S2 = xmalloc(bb * sizeof(double));
+    double *dA1 = xmalloc(bb * sizeof(double)), *dA2 = xmalloc(bb * sizeof(double));
+    double *dW1 = xmalloc(n1 * sizeof(double)), *dW2 = xmalloc(n1 * sizeof(double));
+    double *tmp = xmalloc((size_t)(hd > d ? hd : d) * sizeof(double));
+
+    /* forward: the state at the start of every block (the dual form of mlp_dual_head) */
+    memcpy(W1s, W1_0, n1 * sizeof(double));
+    memcpy(W2s, W2_0, n1 * sizeof(double));
+    for (int n = 0; n < nblk; ++n) {
+        int t0 = n * chunk, b = (T - t0 < chunk) ? (T - t0) : chunk;
+        const double *Kc = K + (size_t)t0 * d, *Vc = V + (size_t)t0 * d, *ec = eta + t0;
+        const double *W1 = W1s + (size_t)n * n1, *W2 = W2s + (size_t)n * n1;
+        double *W1e = W1s + (size_t)(n + 1) * n1, *W2e = W2s + (size_t)(n + 1) * n1;
+        memcpy(W1e, W1, n1 * sizeof(double));
+        memcpy(W2e, W2, n1 * sizeof(double));
+        for (int j = 0; j < b; ++j) {
+            double *zk = Zk + (size_t)j * hd, *hk = Hk + (size_t)j * hd, *e2 = E2 + (size_t)j * d;
+            vecmat(Kc + (size_t)j * d, W1, zk, d, hd);
+            for (int m = 0; m < hd; ++m) hk[m] = oracle_gelu(zk[m]);
+            vecmat(hk, W2, e2, hd, d);
+            for (int c = 0; c < d; ++c) e2[c] -= Vc[(size_t)j * d + c];
+            for (int m = 0; m < hd; ++m)
+                E1[(size_t)j * hd + m] = dot(e2, W2 + (size_t)m * d, d) * oracle_gelu_prime(zk[m]);
+        }
+        for (int j = 0; j < b; ++j) {
+            rank1_sub(W1e, ec[j], Kc + (size_t)j * d, E1 + (size_t)j * hd, d, hd);
+            rank1_sub(W2e, ec[j], Hk + (size_t)j * hd, E2 + (size_t)j * d, hd, d);
+        }
+    }
+
+    if (dW1T) memcpy(dW1, dW1T, n1 * sizeof(double)); else memset(dW1, 0, n1 * sizeof(double));
+    if (dW2T) memcpy(dW2, dW2T, n1 * sizeof(double)); else memset(dW2, 0, n1 * sizeof(double));
+    for (int n = nblk - 1; n >= 0; --n) {
+        int t0 = n * chunk, b = (T - t0 < chunk) ? (T - t0) : chunk;
+        const double *Qc = Q + (size_t)t0 * d, *Kc = K + (size_t)t0 * d, *Vc = V + (size_t)t0 * d;
+        const double *ec = eta + t0, *dZc = dZ + (size_t)t0 * d;
+        double *dQc = dQ + (size_t)t0 * d, *dKc = dK + (size_t)t0 * d, *dVc = dV + (size_t)t0 * d;
+        double *detac = deta + t0;
+        const double *W1 = W1s + (size_t)n * n1, *W2 = W2s + (size_t)n * n1;
+        /* the block's forward quantities at its start state */
+        for (int j = 0; j < b; ++j) {
+            double *zk = Zk + (size_t)j * hd, *hk = Hk + (size_t)j * hd, *e2 = E2 + (size_t)j * d;
+            vecmat(Kc + (size_t)j * d, W1, zk, d, hd);
+            for (int m = 0; m < hd; ++m) hk[m] = oracle_gelu(zk[m]);
+            vecmat(hk, W2, e2, hd, d);
+            for (int c = 0; c < d; ++c) e2[c] -= Vc[(size_t)j * d + c];
+            for (int m = 0; m < hd; ++m) {
+                Gk[(size_t)j * hd + m] = dot(e2, W2 + (size_t)m * d, d);
+                E1[(size_t)j * hd + m] = Gk[(size_t)j * hd + m] * oracle_gelu_prime(zk[m]);
+            }
+        }
+        for (int i = 0; i < b; ++i)
+            for (int j = 0; j < b; ++j) S1[(size_t)i * b + j] = dot(Qc + (size_t)i * d, Kc + (size_t)j * d, d);
+        for (int i = 0; i < b; ++i) {
+            double *zq = Zq + (size_t)i * hd;
+            vecmat(Qc + (size_t)i * d, W1, zq, d, hd);
+            for (int j = 0; j <= i; ++j) {
+                double a1 = ec[j] * S1[(size_t)i * b + j];
+                for (int m = 0; m < hd; ++m) zq[m] -= a1 * E1[(size_t)j * hd + m];
+            }
+            for (int m = 0; m < hd; ++m) Hq[(size_t)i * hd + m] = oracle_gelu(zq[m]);
+        }
+        for (int i = 0; i < b; ++i)
+            for (int j = 0; j < b; ++j)
+                S2[(size_t)i * b + j] = dot(Hq + (size_t)i * hd, Hk + (size_t)j * hd, hd);
+
+        /* the state update: W2' = W2 - Hk^T D E2, W1' = W1 - K^T D E1 (dW1, dW2 hold dW1', dW2') */
+        for (int j = 0; j < b; ++j) {
+            const double *hk = Hk + (size_t)j * hd, *e2 = E2 + (size_t)j * d, *e1 = E1 + (size_t)j * hd;
+            const double *kj = Kc + (size_t)j * d;
+            matvec(dW2, e2, dHk + (size_t)j * hd, hd, d);                  /* (E2 dW2'^T)_j */
+            for (int m = 0; m < hd; ++m) dHk[(size_t)j * hd + m] *= -ec[j];
+            vecmat(hk, dW2, tmp, hd, d);                                   /* (Hk dW2')_j */
+            detac[j] = -dot(tmp, e2, d);
+            for (int c = 0; c < d; ++c) dE2[(size_t)j * d + c] = -ec[j] * tmp[c];
+            matvec(dW1, e1, dKc + (size_t)j * d, d, hd);                   /* (E1 dW1'^T)_j */
+            for (int k = 0; k < d; ++k) dKc[(size_t)j * d + k] *= -ec[j];
+            vecmat(kj, dW1, tmp, d, hd);                                   /* (K dW1')_j */
+            detac[j] -= dot(tmp, e1, hd);
+            for (int m = 0; m < hd; ++m) dE1[(size_t)j * hd + m] = -ec[j] * tmp[m];
+        }
+        /* Z = Hq W2 - A2 E2 */
+        for (int i = 0; i < b; ++i) {
+            matvec(W2, dZc + (size_t)i * d, dHq + (size_t)i * hd, hd, d);  /* dZ W2^T */
+            for (int j = 0; j < b; ++j)
+                dA2[(size_t)i * b + j] = (j <= i) ? -dot(dZc + (size_t)i * d, E2 + (size_t)j * d, d) : 0.0;
+        }
+        for (int i = 0; i < b; ++i) rank1_sub(dW2, -1.0, Hq + (size_t)i * hd, dZc + (size_t)i * d, hd, d);
+        for (int j = 0; j < b; ++j)
+            for (int i = j; i < b; ++i) {
+                double a2 = ec[j] * S2[(size_t)i * b + j];
+                for (int c = 0; c < d; ++c) dE2[(size_t)j * d + c] -= a2 * dZc[(size_t)i * d + c];
+            }
+        /* A2 = (M . Hq Hk^T) D */
+        for (int i = 0; i < b; ++i)
+            for (int j = 0; j <= i; ++j) {
+                double g = dA2[(size_t)i * b + j];
+                detac[j] += g * S2[(size_t)i * b + j];
+                double ds = g * ec[j];
+                for (int m = 0; m < hd; ++m) {
+                    dHq[(size_t)i * hd + m] += ds * Hk[(size_t)j * hd + m];
+                    dHk[(size_t)j * hd + m] += ds * Hq[(size_t)i * hd + m];
+                }
+            }
+        /* Hq = g(Zq);  Zq = Q W1 - A1 E1 */
+        for (int i = 0; i < b; ++i)
+            for (int m = 0; m < hd; ++m)
+                dZq[(size_t)i * hd + m] = dHq[(size_t)i * hd + m] * oracle_gelu_prime(Zq[(size_t)i * hd + m]);
+        for (int i = 0; i < b; ++i) {
+            matvec(W1, dZq + (size_t)i * hd, dQc + (size_t)i * d, d, hd);  /* dZq W1^T */
+            for (int j = 0; j < b; ++j)
+                dA1[(size_t)i * b + j] = (j <= i) ? -dot(dZq + (size_t)i * hd, E1 + (size_t)j * hd, hd) : 0.0;
+        }
+        for (int i = 0; i < b; ++i) rank1_sub(dW1, -1.0, Qc + (size_t)i * d, dZq + (size_t)i * hd, d, hd);
+        for (int j = 0; j < b; ++j)
+            for (int i = j; i < b; ++i) {
+                double a1 = ec[j] * S1[(size_t)i * b + j];
+                for (int m = 0; m < hd; ++m) dE1[(size_t)j * hd + m] -= a1 * dZq[(size_t)i * hd + m];
+            }
+        /* A1 = (M . Q K^T) D */
+        for (int i = 0; i < b; ++i)
+            for (int j = 0; j <= i; ++j) {
+                double g = dA1[(size_t)i * b + j];
+                detac[j] += g * S1[(size_t)i * b + j];
+                double ds = g * ec[j];
+                for (int k = 0; k < d; ++k) {
+                    dQc[(size_t)i * d + k] += ds * Kc[(size_t)j * d + k];
+                    dKc[(size_t)j * d + k] += ds * Qc[(size_t)i * d + k];
+                }
+            }
+        /* E1 = Gk . g'(Zk);  Gk = E2 W2^T */
+        for (int j = 0; j < b; ++j)
+            for (int m = 0; m < hd; ++m) {
+                size_t at = (size_t)j * hd + m;
+                dGk[at] = dE1[at] * oracle_gelu_prime(Zk[at]);
+                dZk[at] = dE1[at] * Gk[at] * oracle_gelu_second(Zk[at]);
+            }
+        for (int j = 0; j < b; ++j) {
+            vecmat(dGk + (size_t)j * hd, W2, tmp, hd, d);                  /* dGk W2 */
+            for (int c = 0; c < d; ++c) dE2[(size_t)j * d + c] += tmp[c];
+        }
+        for (int j = 0; j < b; ++j) rank1_sub(dW2, -1.0, dGk + (size_t)j * hd, E2 + (size_t)j * d, hd, d);
+        /* E2 = Hk W2 - V;  Hk = g(Zk);  Zk = K W1 */
+        for (int j = 0; j < b; ++j) {
+            for (int c = 0; c < d; ++c) dVc[(size_t)j * d + c] = -dE2[(size_t)j * d + c];
+            matvec(W2, dE2 + (size_t)j * d, tmp, hd, d);                   /* dE2 W2^T */
+            for (int m = 0; m < hd; ++m) {
+                size_t at = (size_t)j * hd + m;
+                dHk[at] += tmp[m];
+                dZk[at] += dHk[at] * oracle_gelu_prime(Zk[at]);
+            }
+        }
+        for (int j = 0; j < b; ++j) {
+            rank1_sub(dW2, -1.0, Hk + (size_t)j * hd, dE2 + (size_t)j * d, hd, d);
+            matvec(W1, dZk + (size_t)j * hd, tmp, d, hd);                  /* dZk W1^T */
+            for (int k = 0; k < d; ++k) dKc[(size_t)j * d + k] += tmp[k];
+            rank1_sub(dW1, -1.0, Kc + (size_t)j * d, dZk + (size_t)j * hd, d, hd);
+        }
+    }
+    memcpy(dW1_0, dW1, n1 * sizeof(double));
+    memcpy(dW2_0, dW2, n1 * sizeof(double));
+    free(W1s); free(W2s); free(Zk); free(Hk); free(Gk); free(E1); free(Zq); free(Hq);
+    free(dHk); free(dHq); free(dE1); free(dZq); free(dZk); free(dGk); free(E2); free(dE2);
+    free(S1); free(S2); free(dA1); free(dA2); free(dW1); free(dW2); free(tmp);
+}
+
+void oracle_mlp_backward(const double *Q, const double *K, const double *V, const double *eta,
+                         const double *W1_0, const double *W2_0, const double *dZ,
+                         const double *dW1T, const double *dW2T, double *dQ, double *dK, double *dV,
+                         double *deta, double *dW1_0, double *dW2_0, int B, int H, int T, int d, int hd,
+                         int chunk)
+{
+    long BH = (long)B * H;
+    size_t td = (size_t)T * d, n1 = (size_t)d * hd;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (long bh = 0; bh < BH; ++bh)
+        mlp_backward_head(Q + bh * td, K + bh * td, V + bh * td, eta + bh * (size_t)T, W1_0 + bh * n1,
+                          W2_0 + bh * n1, dZ + bh * td, dW1T ? dW1T + bh * n1 : NULL,
+                          dW2T ? dW2T + bh * n1 : NULL, dQ + bh * td, dK + bh * td, dV + bh * td,
+                          deta + bh * (size_t)T, dW1_0 + bh * n1, dW2_0 + bh * n1, T, d, hd, chunk);
+}
+
 /* Threads OpenMP will use (1 when built without OpenMP). */
 int oracle_num_threads(void)
 {

@@ -72,6 +72,21 @@ MUTANTS = [
      "const double *W = Ws + (size_t)(n + 1) * dd; /* the state at the start of block n */"),
     ("backward dQ scores term uses the query's eta", "acc += dA[(size_t)i * b + j] * ec[j] * Kc[(size_t)j * d + k];",
      "acc += dA[(size_t)i * b + j] * ec[i] * Kc[(size_t)j * d + k];"),
+    ("MLP backward drops GELU''", "dZk[at] = dE1[at] * Gk[at] * oracle_gelu_second(Zk[at]);",
+     "dZk[at] = 0.0 * dE1[at] * Gk[at] * oracle_gelu_second(Zk[at]);"),
+    ("GELU'' sign of the tanh term", "return s * u1 + 0.5 * x * s * (u2 - 2.0 * t * u1 * u1);",
+     "return s * u1 + 0.5 * x * s * (u2 + 2.0 * t * u1 * u1);"),
+    ("MLP backward layer-2 scores mask drops the diagonal",
+     "dA2[(size_t)i * b + j] = (j <= i) ? -dot(dZc + (size_t)i * d, E2 + (size_t)j * d, d) : 0.0;",
+     "dA2[(size_t)i * b + j] = (j < i) ? -dot(dZc + (size_t)i * d, E2 + (size_t)j * d, d) : 0.0;"),
+    ("MLP backward dW2 from the read-out uses Hk",
+     "for (int i = 0; i < b; ++i) rank1_sub(dW2, -1.0, Hq + (size_t)i * hd, dZc + (size_t)i * d, hd, d);",
+     "for (int i = 0; i < b; ++i) rank1_sub(dW2, -1.0, Hk + (size_t)i * hd, dZc + (size_t)i * d, hd, d);"),
+    ("MLP backward drops dGk^T E2 in dW2",
+     "for (int j = 0; j < b; ++j) rank1_sub(dW2, -1.0, dGk + (size_t)j * hd, E2 + (size_t)j * d, hd, d);",
+     "for (int j = 0; j < b; ++j) rank1_sub(dW2, -0.0, dGk + (size_t)j * hd, E2 + (size_t)j * d, hd, d);"),
+    ("MLP backward layer-1 scores use the query's eta", "double a1 = ec[j] * S1[(size_t)i * b + j];\n                for (int m = 0; m < hd; ++m) dE1",
+     "double a1 = ec[i] * S1[(size_t)i * b + j];\n                for (int m = 0; m < hd; ++m) dE1"),
 ]
 
 
@@ -254,9 +269,41 @@ def pin_backward_finite_differences(M):
     return True
 
 
+def pin_mlp_backward_finite_differences(M):
+    # gradient of L = sum(dZ . Z) + sum(dW1T . W1_T) + sum(dW2T . W2_T) of the token-level TTT-MLP scan
+    rng = np.random.default_rng(11)
+    Q, K, V, eta, W1, W2 = _mlp(1, 1, 4, 2, 3, 11)
+    dZ, dW1T, dW2T = rng.standard_normal(Q.shape), rng.standard_normal(W1.shape), rng.standard_normal(W2.shape)
+    args = [Q, K, V, eta, W1, W2]
+    for chunk in (3,):
+        g = M.mlp_backward(Q, K, V, eta, W1, W2, dZ, dW1T, dW2T, chunk)
+
+        def L(*a):
+            Z, A, Bm = M.mlp_primal(*a, chunk)
+            return float(np.sum(dZ * Z) + np.sum(dW1T * A) + np.sum(dW2T * Bm))
+
+        for ai, a in enumerate(args):
+            fd = np.zeros_like(a)
+            for idx in np.ndindex(a.shape):
+                ap = [x.copy() for x in args]
+                am = [x.copy() for x in args]
+                ap[ai][idx] += 1e-5
+                am[ai][idx] -= 1e-5
+                fd[idx] = (L(*ap) - L(*am)) / 2e-5
+            if np.max(np.abs(g[ai] - fd)) > 2e-7 * max(1.0, np.max(np.abs(fd))):
+                return False
+    return True
+
+
+def pin_gelu_second(M):
+    h = 1e-5
+    return all(abs(M.gelu_second(x) - (M.gelu_prime(x + h) - M.gelu_prime(x - h)) / (2 * h)) < 1e-8
+               for x in (-2.3, -0.4, 0.0, 0.7, 3.1))
+
+
 PINS = [pin_golden, pin_primal_dual, pin_linear_attention, pin_delta_rule, pin_consistent_targets,
         pin_mlp_kernelised_attention, pin_mlp_finite_differences, pin_gelu, pin_mlp_online_gd,
-        pin_backward_finite_differences]
+        pin_backward_finite_differences, pin_mlp_backward_finite_differences, pin_gelu_second]
 
 
 def _bind(src_text, tmpdir, tag):
