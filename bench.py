@@ -286,7 +286,7 @@ def segments_of(ws, w):
     return (ws.numel() // (w.B * w.H * w.d * w.d) + 2) // 3
 
 
-def bench_linear(T_mod, w, chunk, steps, warmup, world, peaks, sampler=None, nrot=NROT, split=True):
+def bench_linear(T_mod, w, chunk, steps, warmup, world, peaks, sampler=None, nrot=NROT, split=False):
     """One TTT-Linear prefill per step: split along the sequence (ttt_linear_prefill_ws, scratch
     allocated once, outside the timed region) or the one-pass scan (ttt_linear_prefill)."""
     x = WL.workload_inputs(w)
@@ -306,10 +306,10 @@ def bench_linear(T_mod, w, chunk, steps, warmup, world, peaks, sampler=None, nro
     nbytes = linear_bytes(w.B, w.H, w.T, w.d)
     flops = linear_flops(w.B, w.H, w.T, w.d, chunk)
     t_roof = max(nbytes / (peaks["hbm_gbs"] * 1e9), flops / (peaks["bf16_tflops"] * 1e12))
+    nseg = segments_of(ws, w) if split else 1
     del sets, outs, ws
     return {"tokens_per_s": toks / (ms * 1e-3), "ms_per_step": ms, "ms_per_launch": ms_launch,
-            "path": "split along the sequence" if split else "one pass",
-            "segments": segments_of(ws, w) if split else 1,
+            "path": "split along the sequence" if split else "one pass", "segments": nseg,
             "kernel_launches_per_call": linear_launches(T_mod, w, chunk, split),
             "bytes_per_launch": nbytes, "flops_per_launch": flops,
             "achieved_gbs": nbytes / (ms_launch * 1e-3) / 1e9, "roofline_us": t_roof * 1e6,
@@ -552,7 +552,7 @@ def run_ours(args):
         "warmup": args.warmup, "ms_per_step": head["ms_per_step"], "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": "TTT-Linear prefill B=8 H=12 d=64 T=2048 chunk=16 (bf16 Q/K/V/Z, fp32 state)",
-                   "path": f"split along the sequence, {head['segments']} segments per (batch, head)",
+                   "path": head["path"],
                    "global_batch": w.B * world, "seq_len": w.T, "heads": w.H, "head_dim": w.d, "chunk": w.chunk,
                    "parallelism": f"dp{world}" if world > 1 else "single-gpu",
                    "l2": f"{NROT} rotating input copies ({NROT * linear_bytes(w.B, w.H, w.T, w.d) / 1e6:.0f} MB > "
@@ -572,10 +572,15 @@ def run_ours(args):
     if args.rows != "none":
         want = lambda name: args.rows in ("all", name)
         rows = {"linear_prefill": head}
-        if want("linear_prefill_one_pass"):
-            rows["linear_prefill_one_pass"] = bench_linear(T_mod, w, w.chunk, rsteps * 4, args.warmup, world, peaks,
-                                                           split=False)
         rsteps = max(5, min(50, args.steps // 20))
+        if want("linear_split"):
+            # few heads, long sequence: where the one-pass scan leaves most SMs idle and the split
+            # along the sequence pays; both paths timed on the same inputs
+            wf = WL.WORKLOADS["linear_few_heads"]
+            rows["linear_few_heads_one_pass"] = bench_linear(T_mod, wf, wf.chunk, rsteps, args.warmup, world, peaks,
+                                                             nrot=2)
+            rows["linear_few_heads_split"] = bench_linear(T_mod, wf, wf.chunk, rsteps, args.warmup, world, peaks,
+                                                          nrot=2, split=True)
         if want("mlp_prefill"):
             rows["mlp_prefill"] = bench_mlp(T_mod, WL.WORKLOADS["mlp_prefill"], rsteps, args.warmup, world, peaks)
         if want("long_context"):
@@ -652,7 +657,7 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--rows", choices=["all", "none", "linear_prefill_one_pass", "mlp_prefill", "long_context",
+    ap.add_argument("--rows", choices=["all", "none", "linear_split", "mlp_prefill", "long_context",
                                        "decode", "mlp_decode", "backward"],
                     default="all",
                     help="workload rows timed after the headline (default: all)")

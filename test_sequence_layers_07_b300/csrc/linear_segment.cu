@@ -252,8 +252,25 @@ __global__ void __launch_bounds__(256) linear_segcombine_kernel(const float* __r
     for (int s = 0; s + 1 < nseg; ++s) {
         const float* Dm = maps + (bh * (nseg - 1) + s) * 2 * size_t(D) * D;
         const float* Bm = Dm + size_t(D) * D;
-        for (int i = tid; i < D * D; i += 256) Dl[(i / D) * (D + 1) + (i % D)] = Dm[i];
-        for (int i = tid; i < D * 16; i += 256) Bc[i] = Bm[size_t(i >> 4) * D + c0 + (i & 15)];
+        // all loads of the hop in flight at once: D*D/4 float4 of Delta and 4 floats of B per thread
+        constexpr int NV = D * D / 4 / 256;
+        float4 dv[NV];
+#pragma unroll
+        for (int u = 0; u < NV; ++u) dv[u] = reinterpret_cast<const float4*>(Dm)[tid + 256 * u];
+        float bv[D * 16 / 256];
+#pragma unroll
+        for (int u = 0; u < D * 16 / 256; ++u) {
+            const int i = tid + 256 * u;
+            bv[u] = Bm[size_t(i >> 4) * D + c0 + (i & 15)];
+        }
+#pragma unroll
+        for (int u = 0; u < NV; ++u) {
+            const int i = 4 * (tid + 256 * u), r = i / D, c = i % D;
+            float* dst = Dl + r * (D + 1) + c;
+            dst[0] = dv[u].x; dst[1] = dv[u].y; dst[2] = dv[u].z; dst[3] = dv[u].w;
+        }
+#pragma unroll
+        for (int u = 0; u < D * 16 / 256; ++u) Bc[tid + 256 * u] = bv[u];
         __syncthreads();
         float acc[RPT];
 #pragma unroll
@@ -613,9 +630,14 @@ SegPlan linear_segment_plan(const LinearArgs& a, int force_nseg) {
     if (!linear_segmented_supported(a)) return p;
     const long long heads = (long long)a.B * a.H;
     const int nblk = a.T / a.chunk;
-    // two segments per SM (one CTA of two slots): as many segments per head as fill the SMs, at
-    // least 16 sub-blocks each so the maps pay for themselves
-    long long nseg = force_nseg > 0 ? force_nseg : (2LL * sm_count()) / heads;
+    // The maps cost as much warp-MMA work as the scan of their segments, and the one-pass kernel
+    // already saturates the warp-MMA rate of every SM it occupies (measured on B300), so a split
+    // pays only where the one-pass scan (one CTA per head, four column groups) leaves at least three
+    // quarters of the SMs idle.  Then: two segments per SM (one CTA of two slots), at least 256
+    // tokens per segment.
+    const int sms = sm_count();
+    if (force_nseg <= 0 && heads * 4 > sms) return p;
+    long long nseg = force_nseg > 0 ? force_nseg : (2LL * sms) / heads;
     const long long max_by_len = (long long)a.T / 256 > 0 ? (long long)a.T / 256 : 1;
     if (force_nseg <= 0 && nseg > max_by_len) nseg = max_by_len;
     if (nseg > nblk) nseg = nblk;

@@ -26,8 +26,9 @@ The named workloads are those the library is measured and checked on:
 ``oracle_check`` (d=16, fp32), ``linear_prefill`` (B=8, H=12, d=64, T=2048,
 b=16, bf16), ``mlp_prefill`` (same tokens, hidden 256), ``long_context``
 (B=1, H=16, d=128, T=32768, b in {16, 64, 512}), ``decode`` (B=256, H=12,
-d=64, 1024 single-token steps, per-sequence initial state) and ``mlp_decode``
-(B=64, H=12, d=64, hidden 256, 256 single-token steps).
+d=64, 1024 single-token steps, per-sequence initial state), ``mlp_decode``
+(B=64, H=12, d=64, hidden 256, 256 single-token steps) and ``linear_few_heads`` (B=1, H=4, d=64,
+T=16384, b=16: a batch-1 prompt with few heads, where the split along the sequence pays).
 """
 from __future__ import annotations
 
@@ -69,6 +70,8 @@ WORKLOADS = {
                              chunks=(16, 64, 512)),
     # decode: T is the number of successive single-token steps
     "decode": Workload("decode", B=256, H=12, T=1024, d=64, chunk=1, dtype="bf16", seed=1005),
+    # few heads, long sequence (batch-1 prompt): one-pass scan against the split along the sequence
+    "linear_few_heads": Workload("linear_few_heads", B=1, H=4, T=16384, d=64, chunk=16, dtype="bf16", seed=1007),
     # TTT-MLP decode: 768 heads x 128 KB of fp32 state (the same 100.7 MB of state as the Linear decode)
     "mlp_decode": Workload("mlp_decode", B=64, H=12, T=256, d=64, chunk=1, dtype="bf16", seed=1006, hidden=256),
 }
