@@ -204,10 +204,12 @@ def test_linear_prefill_ws_sizes_and_validation(lib, monkeypatch):
     monkeypatch.delenv("TTT_LINEAR_SEGMENTS", raising=False)
     ws = lib.ttt_linear_prefill_workspace_size
     unit = 64 * 64 * 4
-    n = ws(8, 12, 2048, 64, 16, 1)  # the headline shape is split
-    assert n > 0 and n % (96 * unit) == 0
-    S = (n // (96 * unit) + 2) // 3
-    assert n == 96 * (3 * S - 2) * unit and 2 <= S <= 2048 // 256
+    # the headline shape (96 heads) fills most SMs in one pass: not split
+    assert ws(8, 12, 2048, 64, 16, 1) == 0
+    n = ws(1, 4, 16384, 64, 16, 1)  # four heads, long prompt: split into segments of >= 256 tokens
+    assert n > 0 and n % (4 * unit) == 0
+    S = (n // (4 * unit) + 2) // 3
+    assert n == 4 * (3 * S - 2) * unit and 2 <= S <= 16384 // 256
     # shapes outside the split, or too short to split: 0 (the call is the one-pass scan)
     assert ws(8, 12, 2048, 64, 16, 0) == 0        # fp32
     assert ws(8, 12, 2048, 128, 16, 1) == 0       # d = 128
@@ -228,14 +230,14 @@ def test_linear_prefill_ws_sizes_and_validation(lib, monkeypatch):
     monkeypatch.delenv("TTT_LINEAR_SEGMENTS")
 
     def call(workspace=A, nbytes=n, Q=A, **kw):
-        return lib.ttt_linear_prefill_ws(Q, A, A, A, A, A, A, 8, 12, 2048, 64, 16, 1, workspace, nbytes, None)
+        return lib.ttt_linear_prefill_ws(Q, A, A, A, A, A, A, 1, 4, 16384, 64, 16, 1, workspace, nbytes, None)
 
     assert call(nbytes=n - 16) == T.TTT_ERR_INVALID_ARG
     assert b"workspace" in lib.ttt_last_error()
     assert call(workspace=NULL) == T.TTT_ERR_INVALID_ARG
     assert call(workspace=MIS) == T.TTT_ERR_INVALID_ARG
     assert call(Q=NULL) == T.TTT_ERR_INVALID_ARG
-    assert lib.ttt_linear_prefill_ws(A, A, A, A, A, A, A, 8, 12, 2048, 48, 16, 1, A, n, None) == T.TTT_ERR_UNSUPPORTED
+    assert lib.ttt_linear_prefill_ws(A, A, A, A, A, A, A, 1, 4, 16384, 48, 16, 1, A, n, None) == T.TTT_ERR_UNSUPPORTED
     # nothing to do: no device access even with null pointers and no workspace
     assert lib.ttt_linear_prefill_ws(NULL, NULL, NULL, NULL, NULL, NULL, NULL, 0, 12, 2048, 64, 16, 1, NULL, 0,
                                      None) == T.TTT_OK

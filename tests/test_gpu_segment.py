@@ -124,11 +124,11 @@ def test_segment_shapes_outside_the_split_run_the_one_pass_scan(monkeypatch):
         assert rel_err(Z, Zr) <= TOL[dtype] and rel_err(W, Wr) <= TOL[dtype]
 
 
-def test_linear_prefill_ws_workload_all_heads(monkeypatch):
-    # B=8 H=12 d=64 T=2048 chunk=16 bf16, in the segment plan the benchmark times (chosen from the
-    # SM count): every element of Z and of the final state of all 96 sequences against the oracle
+def test_linear_prefill_ws_few_heads_workload_all_heads(monkeypatch):
+    # B=1 H=4 d=64 T=16384 chunk=16 bf16 (few heads, long prompt), in the segment plan the library
+    # chooses from the SM count and the benchmark times: every element of Z and of the final state
     monkeypatch.delenv("TTT_LINEAR_SEGMENTS", raising=False)
-    w = WL.WORKLOADS["linear_prefill"]
+    w = WL.WORKLOADS["linear_few_heads"]
     x = WL.workload_inputs(w)
     g = cuda(x)
     assert T.ttt_linear_prefill_workspace_size(w.B, w.H, w.T, w.d, w.chunk, g["Q"].dtype) > 0
@@ -136,5 +136,18 @@ def test_linear_prefill_ws_workload_all_heads(monkeypatch):
     torch.cuda.synchronize()
     r = f64(x)
     Zr, Wr = O.linear_dual(r["Q"], r["K"], r["V"], r["eta"], r["W0"], w.chunk)
-    check("linear_prefill split along the sequence, B=8 H=12 d=64 T=2048 b=16", TOL["bf16"], Z=(Z, Zr),
+    check("linear_prefill split along the sequence, B=1 H=4 d=64 T=16384 b=16", TOL["bf16"], Z=(Z, Zr),
           W=(W, Wr))
+
+
+def test_linear_prefill_ws_headline_runs_one_pass(monkeypatch):
+    # the headline shape needs no workspace (one pass); the call through the split entry point matches
+    monkeypatch.delenv("TTT_LINEAR_SEGMENTS", raising=False)
+    w = WL.WORKLOADS["linear_prefill"]
+    x = WL.linear_inputs(w.B, w.H, 256, w.d, seed=w.seed, dtype=w.dtype)
+    g = cuda(x)
+    assert T.ttt_linear_prefill_workspace_size(w.B, w.H, w.T, w.d, w.chunk, g["Q"].dtype) == 0
+    Z, W = T.linear_prefill_ws(g["Q"], g["K"], g["V"], g["eta"], g["W0"], w.chunk)
+    Z1, W1 = T.linear_prefill(g["Q"], g["K"], g["V"], g["eta"], g["W0"], w.chunk)
+    torch.cuda.synchronize()
+    assert torch.equal(Z, Z1) and torch.equal(W, W1)
