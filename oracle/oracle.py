@@ -57,6 +57,10 @@ def _load():
             lib.oracle_mlp_backward.restype = None
             lib.oracle_gelu_second.argtypes = [ctypes.c_double]
             lib.oracle_gelu_second.restype = ctypes.c_double
+            for name in ("oracle_linear_momentum_primal", "oracle_linear_momentum_dual"):
+                f = getattr(lib, name)
+                f.argtypes = [dp] * 6 + [ctypes.c_double] + [dp] * 3 + [i] * 5
+                f.restype = None
             lib.oracle_linear_decode.argtypes = [dp] * 6 + [i] * 3
             lib.oracle_linear_decode.restype = None
             lib.oracle_mlp_token_grad.argtypes = [dp] * 7 + [i] * 2
@@ -118,6 +122,32 @@ def linear_primal(Q, K, V, eta, W0, chunk):
 def linear_dual(Q, K, V, eta, W0, chunk):
     """Dual (matrix) form of the same scan. Returns (Z, W_final)."""
     return _linear("oracle_linear_dual", Q, K, V, eta, W0, chunk)
+
+
+def _momentum(fn_name, Q, K, V, eta, W0, M0, beta, chunk):
+    Q, K, V, eta, W0 = (_f64(a) for a in (Q, K, V, eta, W0))
+    B, H, T, d = Q.shape
+    assert K.shape == V.shape == Q.shape and eta.shape == (B, H, T) and W0.shape == (B, H, d, d) and chunk >= 1
+    Mp = None
+    if M0 is not None:
+        M0 = _f64(M0)
+        assert M0.shape == W0.shape
+        Mp = _p(M0)
+    Z, W, M = np.zeros_like(Q), np.zeros_like(W0), np.zeros_like(W0)
+    getattr(_load(), fn_name)(_p(Q), _p(K), _p(V), _p(eta), _p(W0), Mp, float(beta), _p(Z), _p(W), _p(M),
+                              B, H, T, d, int(chunk))
+    return Z, W, M
+
+
+def linear_momentum_primal(Q, K, V, eta, W0, M0, beta, chunk):
+    """Token-level TTT-Linear scan with momentum (gradients at each chunk's start; M0 None = zero).
+    Returns (Z, W_final, M_final)."""
+    return _momentum("oracle_linear_momentum_primal", Q, K, V, eta, W0, M0, beta, chunk)
+
+
+def linear_momentum_dual(Q, K, V, eta, W0, M0, beta, chunk):
+    """Closed (dual) form of the same scan. Returns (Z, W_final, M_final)."""
+    return _momentum("oracle_linear_momentum_dual", Q, K, V, eta, W0, M0, beta, chunk)
 
 
 def linear_backward(Q, K, V, eta, W0, dZ, dWT, chunk):

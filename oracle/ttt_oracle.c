@@ -38,6 +38,8 @@
  *   R6  the MLP is f(x) = GELU(x W1) W2, no biases, with the tanh form of GELU
  *       and its exact derivative.
  *   R7  a final mini-batch shorter than b is processed as a shorter block.
+ *   R13 (momentum variant) every token takes its own momentum step with the gradient at the chunk
+ *       start: M_i = beta M_{i-1} + g_i, W_i = W_{i-1} - eta_i M_i (see the momentum section).
  *
  * Layouts (row-major, contiguous): Q,K,V,Z [B][H][T][d]; eta [B][H][T];
  * W [B][H][d][d]; W1 [B][H][d][hd]; W2 [B][H][hd][d].  All arrays are double.
@@ -383,6 +385,154 @@ void oracle_linear_decode(const double *q, const double *k, const double *v, con
                           double *W, double *z, int B, int H, int d)
 {
     linear_all(linear_primal_head, q, k, v, eta, W, z, W, B, H, 1, d, 1);
+}
+
+/* ------------------------------------------------------------------ */
+/* TTT-Linear with momentum (reading R13)                              */
+/* ------------------------------------------------------------------ */
+
+/*
+ * [E2] "E^2-TTT" article (zhichai.net), section "Technical Details and Practical Implications":
+ * gradient descent with momentum, squared loss, gradients computed at the chunk start, fast
+ * weights W and momentum M carried from chunk to chunk (the closed form itself is missing from
+ * the page).  Reading R13: every token keeps its own momentum step, with its gradient taken at
+ * the chunk-start state W_s:
+ *     g_i = k_i^T (k_i W_s - v_i),   M_i = beta M_{i-1} + g_i,   W_i = W_{i-1} - eta_i M_i,
+ *     z_i = q_i W_i   (read-out after the token's own step, R2),
+ * with M_0, W_0 the chunk-start momentum and state.  beta = 0 is the plain scan above.
+ * Token-level definition, one (batch, head).
+ */
+static void momentum_primal_head(const double *Q, const double *K, const double *V, const double *eta,
+                                 const double *W0, const double *M0, double beta, double *Z, double *W,
+                                 double *M, int T, int d, int chunk)
+{
+    size_t dd = (size_t)d * d;
+    double *Ws = xmalloc(dd * sizeof(double));
+    double *e = xmalloc((size_t)d * sizeof(double));
+    memcpy(W, W0, dd * sizeof(double));
+    if (M0) memcpy(M, M0, dd * sizeof(double)); else memset(M, 0, dd * sizeof(double));
+    for (int t0 = 0; t0 < T; t0 += chunk) {
+        int n = (T - t0 < chunk) ? (T - t0) : chunk;
+        memcpy(Ws, W, dd * sizeof(double));
+        for (int i = t0; i < t0 + n; ++i) {
+            const double *k = K + (size_t)i * d;
+            oracle_linear_token_error(k, V + (size_t)i * d, Ws, e, d);   /* e = k W_s - v */
+            for (size_t x = 0; x < dd; ++x) M[x] *= beta;                 /* M = beta M + k^T e */
+            rank1_sub(M, -1.0, k, e, d, d);
+            for (size_t x = 0; x < dd; ++x) W[x] -= eta[i] * M[x];        /* W -= eta_i M */
+            vecmat(Q + (size_t)i * d, W, Z + (size_t)i * d, d, d);        /* z = q W */
+        }
+    }
+    free(Ws);
+    free(e);
+}
+
+/*
+ * Closed form of one chunk (indices 1..n inside the chunk), written out from the recursion above:
+ *   M_i = beta^i M_s + sum_{j<=i} beta^{i-j} g_j,
+ *   W_i = W_s - c_i M_s - sum_{j<=i} G_ij k_j^T e_j,   c_i = sum_{l<=i} eta_l beta^l,
+ *                                                     G_ij = sum_{l=j..i} eta_l beta^{l-j}, so
+ *   Z      = Q W_s - diag(c) Q M_s - (G . M . Q K^T) E          (M the causal mask, E = K W_s - V)
+ *   W_end  = W_s - c_n M_s - K^T diag(G_n.) E
+ *   M_end  = beta^n M_s + K^T diag(beta^{n-j}) E.
+ * With beta = 0: c = 0, G_ij = eta_j, the dual form of the plain scan.
+ */
+static void momentum_dual_head(const double *Q, const double *K, const double *V, const double *eta,
+                               const double *W0, const double *M0, double beta, double *Z, double *W,
+                               double *M, int T, int d, int chunk)
+{
+    size_t dd = (size_t)d * d;
+    double *E = xmalloc((size_t)chunk * d * sizeof(double));
+    double *G = xmalloc((size_t)chunk * chunk * sizeof(double));
+    double *c = xmalloc((size_t)chunk * sizeof(double));
+    double *QM = xmalloc((size_t)d * sizeof(double));
+    double *Wn = xmalloc(dd * sizeof(double)), *Mn = xmalloc(dd * sizeof(double));
+    memcpy(W, W0, dd * sizeof(double));
+    if (M0) memcpy(M, M0, dd * sizeof(double)); else memset(M, 0, dd * sizeof(double));
+    for (int t0 = 0; t0 < T; t0 += chunk) {
+        int n = (T - t0 < chunk) ? (T - t0) : chunk;
+        const double *Qc = Q + (size_t)t0 * d, *Kc = K + (size_t)t0 * d, *Vc = V + (size_t)t0 * d;
+        const double *ec = eta + t0;
+        double *Zc = Z + (size_t)t0 * d;
+        for (int j = 0; j < n; ++j) {
+            vecmat(Kc + (size_t)j * d, W, E + (size_t)j * d, d, d);
+            for (int x = 0; x < d; ++x) E[(size_t)j * d + x] -= Vc[(size_t)j * d + x];
+        }
+        /* c_i and G_ij with 0-based i, j: the token at position p carries beta^(p+1) in c */
+        double bp = 1.0, acc = 0.0;
+        for (int i = 0; i < n; ++i) {
+            bp *= beta;
+            acc += ec[i] * bp;
+            c[i] = acc;
+        }
+        for (int j = 0; j < n; ++j) {
+            double g = 0.0, bl = 1.0;
+            for (int i = 0; i < n; ++i) {
+                if (i < j) {
+                    G[(size_t)i * n + j] = 0.0;
+                    continue;
+                }
+                g += ec[i] * bl;  /* adds eta_i beta^(i-j) */
+                bl *= beta;
+                G[(size_t)i * n + j] = g;
+            }
+        }
+        for (int i = 0; i < n; ++i) {
+            double *z = Zc + (size_t)i * d;
+            vecmat(Qc + (size_t)i * d, W, z, d, d);
+            vecmat(Qc + (size_t)i * d, M, QM, d, d);
+            for (int x = 0; x < d; ++x) z[x] -= c[i] * QM[x];
+            for (int j = 0; j <= i; ++j) {
+                double a = G[(size_t)i * n + j] * dot(Qc + (size_t)i * d, Kc + (size_t)j * d, d);
+                for (int x = 0; x < d; ++x) z[x] -= a * E[(size_t)j * d + x];
+            }
+        }
+        memcpy(Wn, W, dd * sizeof(double));
+        for (size_t x = 0; x < dd; ++x) Wn[x] -= c[n - 1] * M[x];
+        double bn = 1.0;
+        for (int j = 0; j < n; ++j) bn *= beta;
+        for (size_t x = 0; x < dd; ++x) Mn[x] = bn * M[x];
+        for (int j = 0; j < n; ++j) {
+            rank1_sub(Wn, G[(size_t)(n - 1) * n + j], Kc + (size_t)j * d, E + (size_t)j * d, d, d);
+            double w = 1.0;
+            for (int l = j + 1; l < n; ++l) w *= beta;  /* beta^(n-1-j) */
+            rank1_sub(Mn, -w, Kc + (size_t)j * d, E + (size_t)j * d, d, d);
+        }
+        memcpy(W, Wn, dd * sizeof(double));
+        memcpy(M, Mn, dd * sizeof(double));
+    }
+    free(E); free(G); free(c); free(QM); free(Wn); free(Mn);
+}
+
+typedef void (*momentum_head_fn)(const double *, const double *, const double *, const double *,
+                                 const double *, const double *, double, double *, double *, double *,
+                                 int, int, int);
+
+static void momentum_all(momentum_head_fn fn, const double *Q, const double *K, const double *V,
+                         const double *eta, const double *W0, const double *M0, double beta, double *Z,
+                         double *W, double *M, int B, int H, int T, int d, int chunk)
+{
+    long BH = (long)B * H;
+    size_t td = (size_t)T * d, dd = (size_t)d * d;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (long bh = 0; bh < BH; ++bh)
+        fn(Q + bh * td, K + bh * td, V + bh * td, eta + bh * (size_t)T, W0 + bh * dd, M0 ? M0 + bh * dd : NULL,
+           beta, Z + bh * td, W + bh * dd, M + bh * dd, T, d, chunk);
+}
+
+/* M0 may be NULL (zero momentum).  Z [B][H][T][d]; W, M [B][H][d][d] are outputs. */
+void oracle_linear_momentum_primal(const double *Q, const double *K, const double *V, const double *eta,
+                                   const double *W0, const double *M0, double beta, double *Z, double *W,
+                                   double *M, int B, int H, int T, int d, int chunk)
+{
+    momentum_all(momentum_primal_head, Q, K, V, eta, W0, M0, beta, Z, W, M, B, H, T, d, chunk);
+}
+
+void oracle_linear_momentum_dual(const double *Q, const double *K, const double *V, const double *eta,
+                                 const double *W0, const double *M0, double beta, double *Z, double *W,
+                                 double *M, int B, int H, int T, int d, int chunk)
+{
+    momentum_all(momentum_dual_head, Q, K, V, eta, W0, M0, beta, Z, W, M, B, H, T, d, chunk);
 }
 
 /* ------------------------------------------------------------------ */

@@ -85,6 +85,14 @@ MUTANTS = [
     ("MLP backward drops dGk^T E2 in dW2",
      "for (int j = 0; j < b; ++j) rank1_sub(dW2, -1.0, dGk + (size_t)j * hd, E2 + (size_t)j * d, hd, d);",
      "for (int j = 0; j < b; ++j) rank1_sub(dW2, -0.0, dGk + (size_t)j * hd, E2 + (size_t)j * d, hd, d);"),
+    ("momentum closed form: c without the token's own beta power", "bp *= beta;\n            acc += ec[i] * bp;",
+     "acc += ec[i] * bp;\n            bp *= beta;"),
+    ("momentum closed form scales by the key's eta", "g += ec[i] * bl;  /* adds eta_i beta^(i-j) */",
+     "g += ec[j] * bl;  /* adds eta_i beta^(i-j) */"),
+    ("momentum closed form: chunk-end momentum not decayed", "for (size_t x = 0; x < dd; ++x) Mn[x] = bn * M[x];",
+     "for (size_t x = 0; x < dd; ++x) Mn[x] = M[x];"),
+    ("momentum primal without the decay", "for (size_t x = 0; x < dd; ++x) M[x] *= beta;",
+     "for (size_t x = 0; x < dd; ++x) M[x] *= 1.0;"),
     ("MLP backward layer-1 scores use the query's eta", "double a1 = ec[j] * S1[(size_t)i * b + j];\n                for (int m = 0; m < hd; ++m) dE1",
      "double a1 = ec[i] * S1[(size_t)i * b + j];\n                for (int m = 0; m < hd; ++m) dE1"),
 ]
@@ -301,9 +309,34 @@ def pin_gelu_second(M):
                for x in (-2.3, -0.4, 0.0, 0.7, 3.1))
 
 
+def pin_momentum(M):
+    # beta = 0 is the plain scan; primal = closed form; chunk 1 is heavy-ball SGD (torch autograd)
+    Q, K, V, eta, W0 = _lin(1, 2, 13, 4, 12)
+    M0 = np.random.default_rng(12).standard_normal(W0.shape) * 0.2
+    Zr, Wr = M.linear_primal(Q, K, V, eta, W0, 3)
+    for fn in (M.linear_momentum_primal, M.linear_momentum_dual):
+        Z, W, _ = fn(Q, K, V, eta, W0, M0, 0.0, 3)
+        if _rel(Z, Zr) > 1e-12 or _rel(W, Wr) > 1e-12:
+            return False
+    a = M.linear_momentum_primal(Q, K, V, eta, W0, M0, 0.6, 3)
+    b = M.linear_momentum_dual(Q, K, V, eta, W0, M0, 0.6, 3)
+    if any(_rel(y, x) > 1e-12 for x, y in zip(a, b)):
+        return False
+    Z, W, Mo = M.linear_momentum_primal(Q, K, V, eta, W0, M0, 0.6, 1)
+    Wt, Mt = torch.tensor(W0[0, 0]), torch.tensor(M0[0, 0])
+    for t in range(13):
+        w = Wt.clone().requires_grad_(True)
+        (0.5 * ((torch.tensor(K[0, 0, t]) @ w - torch.tensor(V[0, 0, t])) ** 2).sum()).backward()
+        Mt = 0.6 * Mt + w.grad
+        Wt = Wt - eta[0, 0, t] * Mt
+        if _rel(Z[0, 0, t], (torch.tensor(Q[0, 0, t]) @ Wt).numpy()) > 1e-12:
+            return False
+    return _rel(W[0, 0], Wt.numpy()) < 1e-12 and _rel(Mo[0, 0], Mt.numpy()) < 1e-12
+
+
 PINS = [pin_golden, pin_primal_dual, pin_linear_attention, pin_delta_rule, pin_consistent_targets,
         pin_mlp_kernelised_attention, pin_mlp_finite_differences, pin_gelu, pin_mlp_online_gd,
-        pin_backward_finite_differences, pin_mlp_backward_finite_differences, pin_gelu_second]
+        pin_backward_finite_differences, pin_mlp_backward_finite_differences, pin_gelu_second, pin_momentum]
 
 
 def _bind(src_text, tmpdir, tag):
