@@ -339,6 +339,40 @@ def bench_mlp(T_mod, w, steps, warmup, world, peaks):
             "frac_of_rated": rated_roof(nbytes, flops) / (ms_launch * 1e-3)}
 
 
+def momentum_bytes(B, H, T, d, elt=2):
+    """Momentum prefill: the plain prefill's bytes plus the fp32 momentum read and written once."""
+    return linear_bytes(B, H, T, d, elt) + 2 * B * H * d * d * 4
+
+
+def momentum_flops(B, H, T, d, b):
+    """Q W, K W, Q M and the two rank updates (W and M), 2 d^2 each per token, plus the causal
+    products ((b + 1) d each, two)."""
+    return B * H * T * (10 * d * d + 2 * (b + 1) * d)
+
+
+def bench_momentum(T_mod, w, beta, steps, warmup, world, peaks, nrot=2):
+    x = WL.workload_inputs(w)
+    rng = torch.Generator().manual_seed(w.seed + 200)
+    x["M0"] = (torch.randn(x["W0"].shape, generator=rng) * 0.02).float()
+    sets = rotating_copies(x, nrot)
+    outs = [(torch.empty_like(s["Q"]), torch.empty_like(s["W0"]), torch.empty_like(s["W0"])) for s in sets]
+
+    def step(i):
+        s, (Z, W, M) = sets[i % nrot], outs[i % nrot]
+        T_mod.ttt_linear_momentum_prefill(s["Q"], s["K"], s["V"], s["eta"], s["W0"], s["M0"], Z, W, M, w.chunk, beta)
+
+    ms, ms_launch = timed_loop(step, steps, warmup, world)
+    nbytes = momentum_bytes(w.B, w.H, w.T, w.d)
+    flops = momentum_flops(w.B, w.H, w.T, w.d, w.chunk)
+    t_roof = max(nbytes / (peaks["hbm_gbs"] * 1e9), flops / (peaks["bf16_tflops"] * 1e12))
+    del sets, outs
+    return {"tokens_per_s": w.B * w.T / (ms * 1e-3), "ms_per_step": ms, "ms_per_launch": ms_launch, "beta": beta,
+            "bytes_per_launch": nbytes, "flops_per_launch": flops, "roofline_us": t_roof * 1e6,
+            "frac": t_roof / (ms_launch * 1e-3), "frac_of_rated": rated_roof(nbytes, flops) / (ms_launch * 1e-3),
+            "bound": "hbm" if nbytes / (peaks["hbm_gbs"] * 1e9) > flops / (peaks["bf16_tflops"] * 1e12) else "tensor",
+            "kernel": "SIMT fp32 (generic)"}
+
+
 def backward_bytes(B, H, T, d, chunk, elt=2):
     """Backward pass: Q,K,V,dZ read and dQ,dK,dV written (elt bytes each), eta read and deta written,
     the block-start states read once (elt bytes each: recorded in the dtype of Q), dW_T read and dW0
@@ -593,6 +627,8 @@ def run_ours(args):
         if want("mlp_decode"):
             wd = WL.WORKLOADS["mlp_decode"]
             rows["mlp_decode"] = bench_mlp_decode(T_mod, wd, max(3, rsteps // 5), args.warmup, world, peaks)
+        if want("momentum"):
+            rows["linear_momentum"] = bench_momentum(T_mod, w, 0.9, max(3, rsteps // 5), args.warmup, world, peaks)
         if want("backward"):
             rows["linear_backward"] = bench_backward(T_mod, w, max(3, rsteps // 5), args.warmup, world, peaks)
         line["rows"] = rows
@@ -658,7 +694,7 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--rows", choices=["all", "none", "linear_split", "mlp_prefill", "long_context",
-                                       "decode", "mlp_decode", "backward"],
+                                       "decode", "mlp_decode", "backward", "momentum"],
                     default="all",
                     help="workload rows timed after the headline (default: all)")
     ap.add_argument("--no-e2e", action="store_true")

@@ -145,6 +145,36 @@ ttt_status ttt_linear_prefill_ws(const void* Q, const void* K, const void* V, co
                                  void* stream);
 
 /*
+ * TTT-Linear prefill with momentum: gradient descent with momentum on the same
+ * loss, every gradient taken at the block-start weights, and every token
+ * taking its own step with the momentum carried from token to token and from
+ * block to block:
+ *
+ *   g_i = k_i^T (k_i W_s - v_i)      (W_s, M_s: weights and momentum at the block start)
+ *   M_i = beta M_{i-1} + g_i,   W_i = W_{i-1} - eta_i M_i,   z_i = q_i W_i
+ *
+ * (M_0 = M_s, W_0 = W_s).  Per block of n tokens this has the exact closed form
+ *   Z = Q W_s - diag(c) Q M_s - (G . tril(Q K^T)) E,   E = K W_s - V,
+ *   W = W_s - c_{n-1} M_s - K^T diag(G_{n-1,.}) E,    M = beta^n M_s + K^T diag(beta^(n-1-j)) E,
+ * with c_i = sum_{l<=i} eta_l beta^(l+1) and G_ij = sum_{l=j..i} eta_l beta^(l-j) (0-based);
+ * beta = 0 is ttt_linear_prefill.
+ *
+ *   M0       [B][H][d][d]  fp32   momentum at the start, or NULL for zero
+ *   M_out    [B][H][d][d]  fp32   momentum after the last token (written; may be M0)
+ *   W_out    may be W0; beta in [0, 1] (else TTT_ERR_INVALID_ARG)
+ *   Other arguments as ttt_linear_prefill.  Runs on the SIMT fp32 kernel for every shape.
+ *
+ * Source: E^2-TTT article (zhichai.net), section "Technical Details and Practical
+ * Implications" (momentum gradient descent, squared loss, gradients at the
+ * chunk start, fast weights and momentum carried between chunks; the closed form
+ * itself is missing from the page, the recursion above is our reading of it).
+ */
+ttt_status ttt_linear_momentum_prefill(const void* Q, const void* K, const void* V, const float* eta,
+                                       const float* W0, const float* M0, void* Z, float* W_out,
+                                       float* M_out, int B, int H, int T, int d, int chunk, float beta,
+                                       ttt_dtype dtype, void* stream);
+
+/*
  * TTT-Linear prefill that also records the state at the start of every block
  * (the values ttt_linear_prefill_backward needs).  Same arguments and results
  * as ttt_linear_prefill, plus:

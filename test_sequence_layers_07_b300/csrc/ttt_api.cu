@@ -171,6 +171,46 @@ ttt_status ttt_linear_prefill_ws(const void* Q, const void* K, const void* V, co
     return TTT_OK;
 }
 
+ttt_status ttt_linear_momentum_prefill(const void* Q, const void* K, const void* V, const float* eta,
+                                      const float* W0, const float* M0, void* Z, float* W_out, float* M_out, int B,
+                                      int H, int T, int d, int chunk, float beta, ttt_dtype dtype, void* stream) {
+    g_last_error[0] = 0;
+    if (B < 0 || H < 0 || T < 0) return fail(TTT_ERR_INVALID_ARG, "negative size%s");
+    if (chunk < 1 || chunk > 512) return fail(TTT_ERR_INVALID_ARG, "chunk must be in 1..512%s");
+    if (dtype != TTT_F32 && dtype != TTT_BF16) return fail(TTT_ERR_INVALID_ARG, "unknown dtype%s");
+    if (d <= 0) return fail(TTT_ERR_INVALID_ARG, "head dim must be positive%s");
+    if (!(beta >= 0.f && beta <= 1.f)) return fail(TTT_ERR_INVALID_ARG, "beta must be in [0, 1]%s");
+    if (!supported_d(d)) return fail(TTT_ERR_UNSUPPORTED, "head dim must be 16, 32, 64 or 128%s");
+    if (size_t(B) * H == 0) return TTT_OK;
+    CHECK_PTR(W0);
+    CHECK_PTR(W_out);
+    CHECK_PTR(M_out);
+    if (M0 && !aligned16(M0)) return fail(TTT_ERR_INVALID_ARG, "pointer not 16-byte aligned: %s", "M0");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (T == 0) {  // no tokens: the state and the momentum pass through
+        const size_t bytes = size_t(B) * H * d * d * sizeof(float);
+        cudaError_t e = W_out != W0 ? cudaMemcpyAsync(W_out, W0, bytes, cudaMemcpyDeviceToDevice, s) : cudaSuccess;
+        if (e == cudaSuccess)
+            e = M0 ? (M_out != M0 ? cudaMemcpyAsync(M_out, M0, bytes, cudaMemcpyDeviceToDevice, s) : cudaSuccess)
+                   : cudaMemsetAsync(M_out, 0, bytes, s);
+        if (e != cudaSuccess) return cuda_fail(e, "ttt_linear_momentum_prefill copy");
+        return TTT_OK;
+    }
+    CHECK_PTR(Q);
+    CHECK_PTR(K);
+    CHECK_PTR(V);
+    CHECK_PTR(eta);
+    CHECK_PTR(Z);
+    ttt::LinearArgs a{Q, K, V, eta, W0, Z, W_out, B, H, T, d, chunk, dtype == TTT_BF16 ? 1 : 0};
+    a.momentum = true;
+    a.M0 = M0;
+    a.M_out = M_out;
+    a.beta = beta;
+    cudaError_t e = ttt::launch_linear_prefill_generic(a, s);
+    if (e != cudaSuccess) return cuda_fail(e, "ttt_linear_momentum_prefill launch");
+    return TTT_OK;
+}
+
 ttt_status ttt_linear_prefill_hist(const void* Q, const void* K, const void* V, const float* eta, const float* W0,
                                    void* Z, float* W_out, void* W_hist, int B, int H, int T, int d, int chunk,
                                    ttt_dtype dtype, void* stream) {

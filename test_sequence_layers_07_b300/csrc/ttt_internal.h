@@ -22,6 +22,11 @@ struct LinearArgs {
     void* W_hist = nullptr;  // optional: the state at the start of every block, [B][H][nblk][d][d],
                              // in the element type of Q (bf16: the state rounded RN-even)
     uint64_t wait_ns = 0;    // bound of the fused kernel's barrier waits (0: the default 4 s)
+    // the momentum variant (generic kernel only): M0 (nullptr: zero) and M_out [B][H][d][d] fp32
+    bool momentum = false;
+    const float* M0 = nullptr;
+    float* M_out = nullptr;
+    float beta = 0.f;
 };
 
 // Gradient of the TTT-Linear chunked scan (outer-loop training).

@@ -25,7 +25,8 @@ LIB_PATH = os.path.join(_PKG, "libttt.so")
 TTT_OK, TTT_ERR_INVALID_ARG, TTT_ERR_UNSUPPORTED, TTT_ERR_CUDA, TTT_ERR_TIMEOUT = range(5)
 TTT_F32, TTT_BF16 = 0, 1
 
-EXPORTED = ("ttt_linear_prefill", "ttt_linear_prefill_workspace_size", "ttt_linear_prefill_ws", "ttt_linear_prefill_hist", "ttt_linear_prefill_backward", "ttt_mlp_prefill",
+EXPORTED = ("ttt_linear_prefill", "ttt_linear_prefill_workspace_size", "ttt_linear_prefill_ws",
+            "ttt_linear_momentum_prefill", "ttt_linear_prefill_hist", "ttt_linear_prefill_backward", "ttt_mlp_prefill",
             "ttt_linear_decode_step", "ttt_mlp_decode_step",
             "ttt_get_device_status", "ttt_selftest_wait_timeout", "ttt_status_string", "ttt_last_error", "ttt_version")
 
@@ -56,6 +57,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
             lib.ttt_linear_prefill_workspace_size.restype = ctypes.c_size_t
             lib.ttt_linear_prefill_ws.argtypes = [vp, vp, vp, fp, fp, vp, fp, i, i, i, i, i, i, vp, ctypes.c_size_t, vp]
             lib.ttt_linear_prefill_ws.restype = i
+            lib.ttt_linear_momentum_prefill.argtypes = [vp, vp, vp, fp, fp, fp, vp, fp, fp, i, i, i, i, i,
+                                                        ctypes.c_float, i, vp]
+            lib.ttt_linear_momentum_prefill.restype = i
             lib.ttt_linear_prefill_hist.argtypes = [vp, vp, vp, fp, fp, vp, fp, fp, i, i, i, i, i, i, vp]
             lib.ttt_linear_prefill_backward.argtypes = [vp, vp, vp, fp, fp, vp, fp, vp, vp, vp, fp, fp,
                                                         i, i, i, i, i, i, vp]
@@ -150,6 +154,27 @@ def ttt_linear_prefill_ws(Q, K, V, eta, W0, Z, W_out, chunk: int, workspace, str
         _ptr(Q, "Q"), _ptr(K, "K"), _ptr(V, "V"), _ptr(eta, "eta", torch.float32), _ptr(W0, "W0", torch.float32),
         _ptr(Z, "Z"), _ptr(W_out, "W_out", torch.float32), B, H, T, d, int(chunk), dt,
         _ptr(workspace, "workspace"), nbytes, _stream(stream))
+    _check(st)
+
+
+def ttt_linear_momentum_prefill(Q, K, V, eta, W0, M0, Z, W_out, M_out, chunk: int, beta: float,
+                                stream=None) -> None:
+    """TTT-Linear prefill with momentum: M0 [B,H,d,d] fp32 or None (zero), outputs Z, W_out and
+    M_out (each may alias its input state)."""
+    B, H, T, d = Q.shape
+    dt = _io_dtype(Q)
+    for name, t in (("K", K), ("V", V), ("Z", Z)):
+        if t.shape != Q.shape or t.dtype != Q.dtype:
+            raise ValueError(f"{name} must match Q in shape and dtype")
+    for name, t in (("W0", W0), ("W_out", W_out), ("M_out", M_out), ("M0", M0)):
+        if t is not None and t.shape != (B, H, d, d):
+            raise ValueError(f"{name} must be [B,H,d,d]")
+    if eta.shape != (B, H, T):
+        raise ValueError("eta must be [B,H,T]")
+    st = load_library().ttt_linear_momentum_prefill(
+        _ptr(Q, "Q"), _ptr(K, "K"), _ptr(V, "V"), _ptr(eta, "eta", torch.float32), _ptr(W0, "W0", torch.float32),
+        _ptr(M0, "M0", torch.float32), _ptr(Z, "Z"), _ptr(W_out, "W_out", torch.float32),
+        _ptr(M_out, "M_out", torch.float32), B, H, T, d, int(chunk), float(beta), dt, _stream(stream))
     _check(st)
 
 
@@ -283,6 +308,15 @@ def linear_prefill_ws(Q, K, V, eta, W0, chunk: int, workspace=None, stream=None)
     W = torch.empty_like(W0)
     ttt_linear_prefill_ws(Q, K, V, eta, W0, Z, W, chunk, workspace, stream)
     return Z, W
+
+
+def linear_momentum_prefill(Q, K, V, eta, W0, M0, chunk: int, beta: float, stream=None):
+    """Returns (Z, W_final, M_final) for the TTT-Linear prefill with momentum (M0 None: zero)."""
+    Z = torch.empty_like(Q)
+    W = torch.empty_like(W0)
+    M = torch.empty_like(W0)
+    ttt_linear_momentum_prefill(Q, K, V, eta, W0, M0, Z, W, M, chunk, beta, stream)
+    return Z, W, M
 
 
 def linear_prefill_hist(Q, K, V, eta, W0, chunk: int, stream=None):

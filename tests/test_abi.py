@@ -241,3 +241,22 @@ def test_linear_prefill_ws_sizes_and_validation(lib, monkeypatch):
     # nothing to do: no device access even with null pointers and no workspace
     assert lib.ttt_linear_prefill_ws(NULL, NULL, NULL, NULL, NULL, NULL, NULL, 0, 12, 2048, 64, 16, 1, NULL, 0,
                                      None) == T.TTT_OK
+
+
+def test_linear_momentum_validation(lib):
+    import ctypes
+
+    def mp(Q=A, M0=A, Mo=A, B_=1, H=1, T_=16, d=64, chunk=16, beta=0.9, dt=1):
+        return lib.ttt_linear_momentum_prefill(Q, A, A, A, A, M0, A, A, Mo, B_, H, T_, d, chunk, ctypes.c_float(beta),
+                                               dt, None)
+
+    assert mp(beta=-0.1) == T.TTT_ERR_INVALID_ARG
+    assert b"beta" in lib.ttt_last_error()
+    assert mp(beta=1.5) == T.TTT_ERR_INVALID_ARG
+    assert mp(beta=float("nan")) == T.TTT_ERR_INVALID_ARG
+    assert mp(Mo=NULL) == T.TTT_ERR_INVALID_ARG
+    assert mp(M0=MIS) == T.TTT_ERR_INVALID_ARG
+    assert mp(Q=NULL) == T.TTT_ERR_INVALID_ARG
+    assert mp(chunk=0) == T.TTT_ERR_INVALID_ARG
+    assert mp(d=48) == T.TTT_ERR_UNSUPPORTED
+    assert mp(Q=NULL, M0=NULL, Mo=NULL, B_=0) == T.TTT_OK
