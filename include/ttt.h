@@ -145,6 +145,31 @@ ttt_status ttt_linear_prefill_ws(const void* Q, const void* K, const void* V, co
                                  void* stream);
 
 /*
+ * The split prefill of ttt_linear_prefill_ws for callers that cannot allocate
+ * device memory when they run the scan: a serving loop that must never reach
+ * the device allocator (cudaMalloc may synchronise the whole device), or code
+ * whose device memory belongs to an allocator it may not go around.  Same
+ * arguments and results as ttt_linear_prefill; no workspace argument, and
+ * nothing is allocated by the caller or by the library.  The pages have no
+ * counterpart: this is a property of the library, not of the method.
+ *
+ * The segment maps and start states live in a fixed 16 MiB array that every
+ * GPU loading the library holds until the process exits.  A shape whose split
+ * needs more than that (ttt_linear_prefill_workspace_size > 16 MiB) returns
+ * TTT_ERR_UNSUPPORTED with the sizes in ttt_last_error(), before anything is
+ * launched; a shape that is not split (workspace size 0) runs the one-pass
+ * scan.  The first call on each device looks up the array's device address (a
+ * runtime call; it is repeated if the device's context changed), so make that
+ * first call before any stream capture.  All calls share the array, which keeps
+ * the last call's contents (nothing in it has to start at zero): calls that
+ * overlap on the GPU, from different streams or host threads, race and must be
+ * serialised by the caller.
+ */
+ttt_status ttt_linear_prefill_noalloc(const void* Q, const void* K, const void* V, const float* eta,
+                                      const float* W0, void* Z, float* W_out, int B, int H, int T,
+                                      int d, int chunk, ttt_dtype dtype, void* stream);
+
+/*
  * TTT-Linear prefill with momentum: gradient descent with momentum on the same
  * loss, every gradient taken at the block-start weights, and every token
  * taking its own step with the momentum carried from token to token and from

@@ -4,8 +4,10 @@
 // Every entry point validates all arguments before launching anything, so an
 // invalid call has no side effect on the device.  Kernel selection is by shape
 // and dtype only; there is exactly one implementation per shape.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <mutex>
 #include <stdio.h>
 #include <stdlib.h>
 #include <string.h>
@@ -168,6 +170,93 @@ ttt_status ttt_linear_prefill_ws(const void* Q, const void* K, const void* V, co
     if (e != cudaSuccess) return cuda_fail(e, "ttt_linear_prefill_ws status word");
     e = ttt::launch_linear_prefill_segmented(a, seg_plan_for(a), workspace, static_cast<cudaStream_t>(stream), status);
     if (e != cudaSuccess) return cuda_fail(e, "ttt_linear_prefill_ws launch");
+    return TTT_OK;
+}
+
+// ---------------------------------------------------------------- split prefill, built-in scratch
+//
+// For callers that cannot allocate device memory at the moment they run the scan: a serving loop
+// that must never reach the device allocator (cudaMalloc may synchronise the whole device and stall
+// every stream), or code whose device memory is handed out by another allocator it may not go
+// around.  ttt_linear_prefill_noalloc runs the split prefill with its maps and start states in this
+// fixed array instead of caller scratch.  Every GPU that loads the library holds the array until the
+// process exits.  Nothing in it has to start at zero: each call writes every word it later reads.
+// All calls share it, so calls that overlap on the GPU (other streams, other host threads) race.
+constexpr size_t kSplitScratchBytes = size_t(16) << 20;  // 16 MiB
+static __device__ __align__(256) float g_split_scratch[kSplitScratchBytes / sizeof(float)];
+
+// Device address of g_split_scratch for the current device, looked up with that device current on
+// the first call there (and again if the device's context changed since, e.g. after a reset); the
+// lookup is a runtime call, so that first call belongs before any stream capture.
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+
+static cudaError_t split_scratch_ptr(void** out) {
+    constexpr int kMaxDev = 64;
+    static std::mutex mu;
+    static void* ctx_of[kMaxDev] = {};
+    static void* ptr_of[kMaxDev] = {};
+    static CtxGetCurrentFn get_ctx = nullptr;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDev) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lk(mu);
+    if (!get_ctx) {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        e = cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q);
+        if (e != cudaSuccess) return e;
+        if (q != cudaDriverEntryPointSuccess || !f) return cudaErrorSymbolNotFound;
+        get_ctx = reinterpret_cast<CtxGetCurrentFn>(f);
+    }
+    CUcontext ctx = nullptr;
+    if (get_ctx(&ctx) != CUDA_SUCCESS) return cudaErrorDeviceUninitialized;
+    if (!ptr_of[dev] || ctx_of[dev] != static_cast<void*>(ctx)) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_split_scratch);
+        if (e != cudaSuccess) return e;
+        ptr_of[dev] = p;
+        ctx_of[dev] = static_cast<void*>(ctx);
+    }
+    *out = ptr_of[dev];
+    return cudaSuccess;
+}
+
+ttt_status ttt_linear_prefill_noalloc(const void* Q, const void* K, const void* V, const float* eta, const float* W0,
+                                      void* Z, float* W_out, int B, int H, int T, int d, int chunk, ttt_dtype dtype,
+                                      void* stream) {
+    g_last_error[0] = 0;
+    if (B < 0 || H < 0 || T < 0) return fail(TTT_ERR_INVALID_ARG, "negative size%s");
+    if (chunk < 1 || chunk > 512) return fail(TTT_ERR_INVALID_ARG, "chunk must be in 1..512%s");
+    if (dtype != TTT_F32 && dtype != TTT_BF16) return fail(TTT_ERR_INVALID_ARG, "unknown dtype%s");
+    if (d <= 0) return fail(TTT_ERR_INVALID_ARG, "head dim must be positive%s");
+    if (!supported_d(d)) return fail(TTT_ERR_UNSUPPORTED, "head dim must be 16, 32, 64 or 128%s");
+    const size_t need = ttt_linear_prefill_workspace_size(B, H, T, d, chunk, dtype);
+    if (need == 0)  // no split for this shape: the one-pass scan, which needs no scratch either
+        return ttt_linear_prefill(Q, K, V, eta, W0, Z, W_out, B, H, T, d, chunk, dtype, stream);
+    if (need > kSplitScratchBytes) {
+        snprintf(g_last_error, sizeof(g_last_error),
+                 "the split of this shape needs %zu bytes of scratch, more than the %zu of the built-in scratch "
+                 "(use ttt_linear_prefill_ws with caller scratch)",
+                 need, kSplitScratchBytes);
+        return TTT_ERR_UNSUPPORTED;
+    }
+    CHECK_PTR(Q);
+    CHECK_PTR(K);
+    CHECK_PTR(V);
+    CHECK_PTR(eta);
+    CHECK_PTR(W0);
+    CHECK_PTR(Z);
+    CHECK_PTR(W_out);
+    void* scratch = nullptr;
+    cudaError_t e = split_scratch_ptr(&scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "ttt_linear_prefill_noalloc scratch address");
+    int* status = nullptr;
+    e = status_ptr(&status);
+    if (e != cudaSuccess) return cuda_fail(e, "ttt_linear_prefill_noalloc status word");
+    ttt::LinearArgs a{Q, K, V, eta, W0, Z, W_out, B, H, T, d, chunk, dtype == TTT_BF16 ? 1 : 0};
+    e = ttt::launch_linear_prefill_segmented(a, seg_plan_for(a), scratch, static_cast<cudaStream_t>(stream), status);
+    if (e != cudaSuccess) return cuda_fail(e, "ttt_linear_prefill_noalloc launch");
     return TTT_OK;
 }
 

@@ -26,7 +26,7 @@ TTT_OK, TTT_ERR_INVALID_ARG, TTT_ERR_UNSUPPORTED, TTT_ERR_CUDA, TTT_ERR_TIMEOUT 
 TTT_F32, TTT_BF16 = 0, 1
 
 EXPORTED = ("ttt_linear_prefill", "ttt_linear_prefill_workspace_size", "ttt_linear_prefill_ws",
-            "ttt_linear_momentum_prefill", "ttt_linear_prefill_hist", "ttt_linear_prefill_backward", "ttt_mlp_prefill",
+            "ttt_linear_prefill_noalloc", "ttt_linear_momentum_prefill", "ttt_linear_prefill_hist", "ttt_linear_prefill_backward", "ttt_mlp_prefill",
             "ttt_linear_decode_step", "ttt_mlp_decode_step",
             "ttt_get_device_status", "ttt_selftest_wait_timeout", "ttt_status_string", "ttt_last_error", "ttt_version")
 
@@ -57,6 +57,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
             lib.ttt_linear_prefill_workspace_size.restype = ctypes.c_size_t
             lib.ttt_linear_prefill_ws.argtypes = [vp, vp, vp, fp, fp, vp, fp, i, i, i, i, i, i, vp, ctypes.c_size_t, vp]
             lib.ttt_linear_prefill_ws.restype = i
+            lib.ttt_linear_prefill_noalloc.argtypes = [vp, vp, vp, fp, fp, vp, fp, i, i, i, i, i, i, vp]
+            lib.ttt_linear_prefill_noalloc.restype = i
             lib.ttt_linear_momentum_prefill.argtypes = [vp, vp, vp, fp, fp, fp, vp, fp, fp, i, i, i, i, i,
                                                         ctypes.c_float, i, vp]
             lib.ttt_linear_momentum_prefill.restype = i
@@ -154,6 +156,22 @@ def ttt_linear_prefill_ws(Q, K, V, eta, W0, Z, W_out, chunk: int, workspace, str
         _ptr(Q, "Q"), _ptr(K, "K"), _ptr(V, "V"), _ptr(eta, "eta", torch.float32), _ptr(W0, "W0", torch.float32),
         _ptr(Z, "Z"), _ptr(W_out, "W_out", torch.float32), B, H, T, d, int(chunk), dt,
         _ptr(workspace, "workspace"), nbytes, _stream(stream))
+    _check(st)
+
+
+def ttt_linear_prefill_noalloc(Q, K, V, eta, W0, Z, W_out, chunk: int, stream=None) -> None:
+    """The split TTT-Linear prefill with the library's built-in scratch (no workspace argument, nothing
+    allocated): for callers that cannot allocate device memory when they run the scan."""
+    B, H, T, d = Q.shape
+    dt = _io_dtype(Q)
+    for name, t in (("K", K), ("V", V), ("Z", Z)):
+        if t.shape != Q.shape or t.dtype != Q.dtype:
+            raise ValueError(f"{name} must match Q in shape and dtype")
+    if eta.shape != (B, H, T) or W0.shape != (B, H, d, d) or W_out.shape != (B, H, d, d):
+        raise ValueError("eta must be [B,H,T] and W0/W_out [B,H,d,d]")
+    st = load_library().ttt_linear_prefill_noalloc(
+        _ptr(Q, "Q"), _ptr(K, "K"), _ptr(V, "V"), _ptr(eta, "eta", torch.float32), _ptr(W0, "W0", torch.float32),
+        _ptr(Z, "Z"), _ptr(W_out, "W_out", torch.float32), B, H, T, d, int(chunk), dt, _stream(stream))
     _check(st)
 
 
