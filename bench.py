@@ -424,6 +424,64 @@ def bench_backward(T_mod, w, steps, warmup, world, peaks, nrot=2):
             "bound": "hbm" if nbytes / (peaks["hbm_gbs"] * 1e9) > flops / (peaks["bf16_tflops"] * 1e12) else "tensor"}
 
 
+def mlp_backward_bytes(B, H, T, d, hd, chunk, elt=2):
+    """TTT-MLP backward: Q, K, V, dZ read and dQ, dK, dV written (elt bytes each), eta read and deta
+    written, the recorded W1, W2 of every block read once (elt bytes each), dW_T read and dW0 written
+    (fp32, both layers)."""
+    nblk = -(-T // chunk)
+    return B * H * (T * (7 * d * elt + 8) + nblk * 2 * d * hd * elt + 2 * 2 * d * hd * 4)
+
+
+def mlp_backward_flops(B, H, T, d, hd, chunk):
+    """Per head-token: the block's forward at its start state (Zk, Zq, E2, Gk: 4 products) and the
+    backward's products over d x hidden (dHk, dE1 from the state gradients, Hk dW2', E1 dW1'^T,
+    dZ W2^T, dZq W1^T, dGk W2, dE2 W2^T, dZk W1^T, and the five rank updates of dW1, dW2), 2 d h each
+    (18 in all), plus the causal score products ((b + 1)(d + h) each, six)."""
+    return B * H * T * (36 * d * hd + 6 * (chunk + 1) * (d + hd))
+
+
+def bench_mlp_backward(T_mod, w, steps, warmup, world, peaks, nrot=2):
+    """Training step of the TTT-MLP workload shape: the forward that records the block-start states,
+    then the backward; each timed on its own launches."""
+    x = WL.workload_inputs(w)
+    rng = torch.Generator().manual_seed(w.seed + 100)
+    g = {"dZ": (torch.randn(x["Q"].shape, generator=rng) / w.d ** 0.5).to(x["Q"].dtype),
+         "dW1T": torch.randn(x["W1"].shape, generator=rng) / w.d ** 0.5,
+         "dW2T": torch.randn(x["W2"].shape, generator=rng) / w.d ** 0.5}
+    sets = rotating_copies({**x, **g}, nrot)
+    nblk = -(-w.T // w.chunk)
+    hists = [(torch.empty((w.B, w.H, nblk, w.d, w.hidden), dtype=s["Q"].dtype, device="cuda"),
+              torch.empty((w.B, w.H, nblk, w.hidden, w.d), dtype=s["Q"].dtype, device="cuda")) for s in sets]
+    fwd_out = [(torch.empty_like(s["Q"]), torch.empty_like(s["W1"]), torch.empty_like(s["W2"])) for s in sets]
+    bwd_out = [(torch.empty_like(s["Q"]), torch.empty_like(s["Q"]), torch.empty_like(s["Q"]),
+                torch.empty_like(s["eta"]), torch.empty_like(s["W1"]), torch.empty_like(s["W2"])) for s in sets]
+
+    def fwd(i):
+        s, (Z, A, Bm), (H1, H2) = sets[i % nrot], fwd_out[i % nrot], hists[i % nrot]
+        T_mod.ttt_mlp_prefill_hist(s["Q"], s["K"], s["V"], s["eta"], s["W1"], s["W2"], Z, A, Bm, H1, H2, w.chunk)
+
+    def bwd(i):
+        s, o, (H1, H2) = sets[i % nrot], bwd_out[i % nrot], hists[i % nrot]
+        T_mod.ttt_mlp_prefill_backward(s["Q"], s["K"], s["V"], s["eta"], H1, H2, s["dZ"], s["dW1T"], s["dW2T"], *o,
+                                       w.chunk)
+
+    for i in range(nrot):
+        fwd(i)
+    ms_f, ms_f_launch = timed_loop(fwd, steps, warmup, world)
+    ms_b, ms_b_launch = timed_loop(bwd, steps, warmup, world)
+    nbytes = mlp_backward_bytes(w.B, w.H, w.T, w.d, w.hidden, w.chunk)
+    flops = mlp_backward_flops(w.B, w.H, w.T, w.d, w.hidden, w.chunk)
+    t_roof = max(nbytes / (peaks["hbm_gbs"] * 1e9), flops / (peaks["bf16_tflops"] * 1e12))
+    del sets, hists, fwd_out, bwd_out
+    return {"tokens_per_s": w.B * w.T / ((ms_f + ms_b) * 1e-3), "ms_per_step": ms_f + ms_b,
+            "forward_hist_ms_per_launch": ms_f_launch, "backward_ms_per_launch": ms_b_launch,
+            "backward_bytes_per_launch": nbytes, "backward_flops_per_launch": flops,
+            "backward_roofline_us": t_roof * 1e6, "backward_frac": t_roof / (ms_b_launch * 1e-3),
+            "backward_frac_of_rated": rated_roof(nbytes, flops) / (ms_b_launch * 1e-3),
+            "bound": "hbm" if nbytes / (peaks["hbm_gbs"] * 1e9) > flops / (peaks["bf16_tflops"] * 1e12) else "tensor",
+            "backward_kernel": "SIMT fp32"}
+
+
 def bench_decode(T_mod, w, steps, warmup, world, peaks, graph_steps=1024, nrot=NROT):
     """A CUDA graph of `graph_steps` decode steps; `nrot` state copies rotate so the state streams from HBM."""
     x = WL.decode_inputs(w.B, w.H, w.d, graph_steps, w.seed)
@@ -627,6 +685,9 @@ def run_ours(args):
         if want("mlp_decode"):
             wd = WL.WORKLOADS["mlp_decode"]
             rows["mlp_decode"] = bench_mlp_decode(T_mod, wd, max(3, rsteps // 5), args.warmup, world, peaks)
+        if want("mlp_backward"):
+            rows["mlp_backward"] = bench_mlp_backward(T_mod, WL.WORKLOADS["mlp_prefill"], 3, args.warmup, world,
+                                                      peaks)
         if want("momentum"):
             rows["linear_momentum"] = bench_momentum(T_mod, w, 0.9, max(3, rsteps // 5), args.warmup, world, peaks)
         if want("backward"):
@@ -694,7 +755,7 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--rows", choices=["all", "none", "linear_split", "mlp_prefill", "long_context",
-                                       "decode", "mlp_decode", "backward", "momentum"],
+                                       "decode", "mlp_decode", "backward", "momentum", "mlp_backward"],
                     default="all",
                     help="workload rows timed after the headline (default: all)")
     ap.add_argument("--no-e2e", action="store_true")

@@ -279,6 +279,60 @@ ttt_status ttt_mlp_prefill(const void* Q, const void* K, const void* V, const fl
                            ttt_dtype dtype, void* stream);
 
 /*
+ * TTT-MLP prefill that also records the state at the start of every block (the
+ * values ttt_mlp_prefill_backward needs).  Same arguments and results as
+ * ttt_mlp_prefill, plus:
+ *
+ *   W1_hist  [B][H][nblk][d][hidden]  dtype  written: W1 at the start of block n
+ *   W2_hist  [B][H][nblk][hidden][d]  dtype  written: W2 at the start of block n
+ *                                            (n = 0: W1_0, W2_0; nblk = ceil(T / chunk))
+ *
+ * In the element type of Q: fp32 for TTT_F32; for TTT_BF16 the state rounded to
+ * bf16 (RN-even), the operand the forward's products used.  Neither may overlap
+ * another argument.  bf16 with d = 64, hidden = 256, chunk 16 runs the warp-MMA
+ * kernel with the state writes added; every other shape the SIMT kernel.
+ * Source: as ttt_mlp_prefill; the saved states serve the gradient below.
+ */
+ttt_status ttt_mlp_prefill_hist(const void* Q, const void* K, const void* V, const float* eta,
+                                const float* W1_0, const float* W2_0, void* Z, float* W1_out,
+                                float* W2_out, void* W1_hist, void* W2_hist, int B, int H, int T, int d,
+                                int hidden, int chunk, ttt_dtype dtype, void* stream);
+
+/*
+ * Gradient of the TTT-MLP prefill (training the outer model through the inner
+ * loop: TTT essay, ren-xubin.github.io, paragraph on the two time scales; the
+ * two-layer inner model of "Test-Time Training (TTT) Layers for Sequence
+ * Modeling", section "Variants: TTT-Linear vs. TTT-MLP").  Given the gradients
+ * of a scalar loss with respect to Z and to the final W1, W2:
+ *
+ *   Q, K, V        [B][H][T][d]              dtype   forward inputs
+ *   eta            [B][H][T]                 fp32
+ *   W1_hist, W2_hist                         dtype   block-start states from ttt_mlp_prefill_hist
+ *   dZ             [B][H][T][d]              dtype   dL/dZ
+ *   dW1_T, dW2_T   [B][H][d][hidden], [B][H][hidden][d]  fp32  dL/dW1_out, dL/dW2_out, or NULL for zero
+ *   dQ, dK, dV     [B][H][T][d]              dtype   written
+ *   deta           [B][H][T]                 fp32    written
+ *   dW1_0, dW2_0   fp32                              written: dL/dW1_0, dL/dW2_0 (may be dW1_T, dW2_T)
+ *   shapes as ttt_mlp_prefill with chunk <= 16 (else TTT_ERR_UNSUPPORTED)
+ *
+ * Per block, in reverse (g = GELU, tanh form; D = diag(eta); M the causal mask):
+ *   forward at the block start: Zk = K W1, Hk = g(Zk), E2 = Hk W2 - V, Gk = E2 W2^T,
+ *   E1 = Gk . g'(Zk), Zq = Q W1 - (M . Q K^T) D E1, Hq = g(Zq);
+ *   dW2 += Hq^T dZ + dGk^T E2 + Hk^T dE2,  dW1 += Q^T dZq + K^T dZk, with
+ *   dE2 = -D Hk dW2' - (M . Hq Hk^T D)^T dZ + dGk W2,  dZq = (dZ W2^T + dS2 Hk) . g'(Zq),
+ *   dE1 = -D K dW1' - (M . Q K^T D)^T dZq,  dGk = dE1 . g'(Zk),
+ *   dZk = dE1 . Gk . g''(Zk) + (-D E2 dW2'^T + dS2^T Hq + dE2 W2^T) . g'(Zk),
+ *   dQ = dZq W1^T + dS1 K,  dK = -D E1 dW1'^T + dS1^T Q + dZk W1^T,  dV = -dE2,
+ *   with dS1 = M . (-dZq E1^T) D, dS2 = M . (-dZ E2^T) D, and deta from the same terms.
+ * Accumulation in fp32 (SIMT), outputs rounded to dtype (RN-even).
+ */
+ttt_status ttt_mlp_prefill_backward(const void* Q, const void* K, const void* V, const float* eta,
+                                    const void* W1_hist, const void* W2_hist, const void* dZ,
+                                    const float* dW1_T, const float* dW2_T, void* dQ, void* dK, void* dV,
+                                    float* deta, float* dW1_0, float* dW2_0, int B, int H, int T, int d,
+                                    int hidden, int chunk, ttt_dtype dtype, void* stream);
+
+/*
  * TTT-Linear decode: one online step (a block of one token) for every
  * (batch, head), updating the state in place:
  *

@@ -50,7 +50,8 @@ template <typename TI>
 __global__ void __launch_bounds__(kThreads)
 mlp_prefill_generic_kernel(const TI* __restrict__ Q, const TI* __restrict__ K, const TI* __restrict__ V,
                            const float* __restrict__ eta, const float* W1_0, const float* W2_0,
-                           TI* __restrict__ Z, float* W1, float* W2, int T, int d, int hd, int chunk) {
+                           TI* __restrict__ Z, float* W1, float* W2, int T, int d, int hd, int chunk,
+                           TI* __restrict__ W1_hist, TI* __restrict__ W2_hist) {
     extern __shared__ float smem[];
     const size_t bh = blockIdx.x;
     const size_t nw = size_t(d) * hd;
@@ -67,9 +68,18 @@ mlp_prefill_generic_kernel(const TI* __restrict__ Q, const TI* __restrict__ K, c
     TI* Zh = Z + bh * size_t(T) * d;
     __syncthreads();
 
+    const int nblk = (T + chunk - 1) / chunk;
     for (int t0 = 0; t0 < T; t0 += chunk) {
         const int n = min(chunk, T - t0);
         const Smem L{d, hd, chunk};
+        if (W1_hist) {  // the state at the start of this block, in the element type of Q
+            TI* h1 = W1_hist + (bh * nblk + t0 / chunk) * nw;
+            TI* h2 = W2_hist + (bh * nblk + t0 / chunk) * nw;
+            for (size_t i = threadIdx.x; i < nw; i += kThreads) {
+                h1[i] = from_f32<TI>(W1[i]);
+                h2[i] = from_f32<TI>(W2[i]);
+            }
+        }
         float *qs = L.q(smem), *ks = L.k(smem), *vs = L.v(smem), *e2 = L.e2(smem);
         float *gp = L.gp(smem), *hk = L.hk(smem), *e1 = L.e1(smem), *as = L.a(smem), *es = L.eta(smem);
 
@@ -178,14 +188,16 @@ cudaError_t launch_mlp_prefill_generic(const MlpArgs& a, cudaStream_t s) {
         kern<<<unsigned(a.B) * unsigned(a.H), kThreads, bytes, s>>>(
             static_cast<const __nv_bfloat16*>(a.Q), static_cast<const __nv_bfloat16*>(a.K),
             static_cast<const __nv_bfloat16*>(a.V), a.eta, a.W1_0, a.W2_0, static_cast<__nv_bfloat16*>(a.Z),
-            a.W1_out, a.W2_out, a.T, a.d, a.hidden, a.chunk);
+            a.W1_out, a.W2_out, a.T, a.d, a.hidden, a.chunk, static_cast<__nv_bfloat16*>(a.W1_hist),
+            static_cast<__nv_bfloat16*>(a.W2_hist));
     } else {
         auto kern = mlp_prefill_generic_kernel<float>;
         if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(bytes))) != cudaSuccess)
             return e;
         kern<<<unsigned(a.B) * unsigned(a.H), kThreads, bytes, s>>>(
             static_cast<const float*>(a.Q), static_cast<const float*>(a.K), static_cast<const float*>(a.V), a.eta,
-            a.W1_0, a.W2_0, static_cast<float*>(a.Z), a.W1_out, a.W2_out, a.T, a.d, a.hidden, a.chunk);
+            a.W1_0, a.W2_0, static_cast<float*>(a.Z), a.W1_out, a.W2_out, a.T, a.d, a.hidden, a.chunk,
+            static_cast<float*>(a.W1_hist), static_cast<float*>(a.W2_hist));
     }
     return cudaGetLastError();
 }

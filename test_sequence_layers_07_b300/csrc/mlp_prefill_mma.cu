@@ -127,10 +127,13 @@ __device__ __forceinline__ float bf16_at(const uint8_t* tile, int row, int col) 
     return __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(tile + swz(row, col & ~7) + (col & 7) * 2));
 }
 
+// HIST: also write the state at the start of every block to W1_hist / W2_hist (bf16).
+template <bool HIST>
 __global__ void __launch_bounds__(THREADS, 1)
 mlp_prefill_mma_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const float* __restrict__ eta, const float* W1_0,
                        const float* W2_0, __nv_bfloat16* __restrict__ Z, float* W1_out, float* W2_out, int T,
+                       __nv_bfloat16* __restrict__ W1_hist, __nv_bfloat16* __restrict__ W2_hist,
                        int* status) {
     extern __shared__ uint8_t smem_dyn[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
@@ -248,6 +251,28 @@ mlp_prefill_mma_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_con
             const uint32_t st = sb + s * SLOT;
             if (have) {
                 if (!err && !wait(full_bar[s], par)) err = true;
+                if constexpr (HIST) {
+                    // the state at the start of block n (this warp's hidden slice), rounded to bf16: the
+                    // operand the block's products use and what the backward reads
+                    __nv_bfloat16* h1 = W1_hist + (bh * size_t(nblk) + n) * D * HID;
+                    __nv_bfloat16* h2 = W2_hist + (bh * size_t(nblk) + n) * HID * D;
+#pragma unroll
+                    for (int mh = 0; mh < 2; ++mh)
+#pragma unroll
+                        for (int nd = 0; nd < 8; ++nd)
+#pragma unroll
+                            for (int k = 0; k < 4; ++k)
+                                h1[size_t(8 * nd + 2 * t + (k & 1)) * HID + h0 + 16 * mh + g + 8 * (k >> 1)] =
+                                    __float2bfloat16_rn(w1[mh][nd][k]);
+#pragma unroll
+                    for (int mo = 0; mo < 4; ++mo)
+#pragma unroll
+                        for (int nh = 0; nh < 4; ++nh)
+#pragma unroll
+                            for (int k = 0; k < 4; ++k)
+                                h2[size_t(h0 + 8 * nh + 2 * t + (k & 1)) * D + 16 * mo + g + 8 * (k >> 1)] =
+                                    __float2bfloat16_rn(w2[mo][nh][k]);
+                }
                 // ---- Zk = K W1 and Zq = Q W1 (start-of-block W1)
                 float zk[4][4], sc[2][4] = {};
 #pragma unroll
@@ -498,12 +523,15 @@ cudaError_t launch_mlp_prefill_mma(const MlpArgs& a, cudaStream_t s, int* status
     if ((e = make_tma_map_bf16(&mk, a.K, rows, D)) != cudaSuccess) return e;
     if ((e = make_tma_map_bf16(&mv, a.V, rows, D)) != cudaSuccess) return e;
     const int bytes = SMEM_BYTES + 1024;  // + alignment slack
-    if ((e = cudaFuncSetAttribute(mlp_prefill_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) !=
-        cudaSuccess)
-        return e;
-    mlp_prefill_mma_kernel<<<unsigned(a.B) * unsigned(a.H), THREADS, bytes, s>>>(
-        mq, mk, mv, a.eta, a.W1_0, a.W2_0, static_cast<__nv_bfloat16*>(a.Z), a.W1_out, a.W2_out, a.T, status);
-    return cudaGetLastError();
+    auto run = [&](auto kern) -> cudaError_t {
+        cudaError_t e2 = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+        if (e2 != cudaSuccess) return e2;
+        kern<<<unsigned(a.B) * unsigned(a.H), THREADS, bytes, s>>>(
+            mq, mk, mv, a.eta, a.W1_0, a.W2_0, static_cast<__nv_bfloat16*>(a.Z), a.W1_out, a.W2_out, a.T,
+            static_cast<__nv_bfloat16*>(a.W1_hist), static_cast<__nv_bfloat16*>(a.W2_hist), status);
+        return cudaGetLastError();
+    };
+    return a.W1_hist ? run(mlp_prefill_mma_kernel<true>) : run(mlp_prefill_mma_kernel<false>);
 }
 
 }  // namespace ttt

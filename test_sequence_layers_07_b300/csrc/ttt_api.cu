@@ -432,6 +432,103 @@ ttt_status ttt_mlp_prefill(const void* Q, const void* K, const void* V, const fl
     return TTT_OK;
 }
 
+// Validation shared by the TTT-MLP prefill entry points (shapes of ttt_mlp_prefill).
+static ttt_status mlp_shape_check(int B, int H, int T, int d, int hidden, int chunk, ttt_dtype dtype) {
+    if (B < 0 || H < 0 || T < 0) return fail(TTT_ERR_INVALID_ARG, "negative size%s");
+    if (chunk < 1 || chunk > 512) return fail(TTT_ERR_INVALID_ARG, "chunk must be in 1..512%s");
+    if (dtype != TTT_F32 && dtype != TTT_BF16) return fail(TTT_ERR_INVALID_ARG, "unknown dtype%s");
+    if (d <= 0 || hidden <= 0) return fail(TTT_ERR_INVALID_ARG, "dimensions must be positive%s");
+    if (!(d == 16 || d == 32 || d == 64)) return fail(TTT_ERR_UNSUPPORTED, "MLP head dim must be 16, 32 or 64%s");
+    if (hidden % 16 != 0 || size_t(d) * hidden > 16384)
+        return fail(TTT_ERR_UNSUPPORTED, "MLP hidden must be a multiple of 16 with d*hidden <= 16384%s");
+    if (size_t(chunk) * hidden > 4096 || chunk > 64)
+        return fail(TTT_ERR_UNSUPPORTED, "MLP chunk must satisfy chunk <= 64 and chunk*hidden <= 4096%s");
+    return TTT_OK;
+}
+
+ttt_status ttt_mlp_prefill_hist(const void* Q, const void* K, const void* V, const float* eta, const float* W1_0,
+                                const float* W2_0, void* Z, float* W1_out, float* W2_out, void* W1_hist,
+                                void* W2_hist, int B, int H, int T, int d, int hidden, int chunk, ttt_dtype dtype,
+                                void* stream) {
+    g_last_error[0] = 0;
+    ttt_status st = mlp_shape_check(B, H, T, d, hidden, chunk, dtype);
+    if (st != TTT_OK) return st;
+    if (size_t(B) * H == 0) return TTT_OK;
+    if (T == 0)
+        return ttt_mlp_prefill(Q, K, V, eta, W1_0, W2_0, Z, W1_out, W2_out, B, H, T, d, hidden, chunk, dtype, stream);
+    CHECK_PTR(Q);
+    CHECK_PTR(K);
+    CHECK_PTR(V);
+    CHECK_PTR(eta);
+    CHECK_PTR(W1_0);
+    CHECK_PTR(W2_0);
+    CHECK_PTR(Z);
+    CHECK_PTR(W1_out);
+    CHECK_PTR(W2_out);
+    CHECK_PTR(W1_hist);
+    CHECK_PTR(W2_hist);
+    ttt::MlpArgs a{Q, K, V, eta, W1_0, W2_0, Z, W1_out, W2_out, B, H, T, d, hidden, chunk, dtype == TTT_BF16 ? 1 : 0};
+    a.W1_hist = W1_hist;
+    a.W2_hist = W2_hist;
+    int* status = nullptr;
+    cudaError_t e = status_ptr(&status);
+    if (e != cudaSuccess) return cuda_fail(e, "ttt_mlp_prefill_hist status word");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // the warp-MMA kernel records the states for its shape (bf16, d 64, hidden 256, chunk 16); the
+    // generic kernel for every other shape
+    e = ttt::launch_mlp_prefill_mma(a, s, status);
+    if (e == cudaErrorNotSupported) e = ttt::launch_mlp_prefill_generic(a, s);
+    if (e != cudaSuccess) return cuda_fail(e, "ttt_mlp_prefill_hist launch");
+    return TTT_OK;
+}
+
+ttt_status ttt_mlp_prefill_backward(const void* Q, const void* K, const void* V, const float* eta,
+                                    const void* W1_hist, const void* W2_hist, const void* dZ, const float* dW1_T,
+                                    const float* dW2_T, void* dQ, void* dK, void* dV, float* deta, float* dW1_0,
+                                    float* dW2_0, int B, int H, int T, int d, int hidden, int chunk, ttt_dtype dtype,
+                                    void* stream) {
+    g_last_error[0] = 0;
+    ttt_status st = mlp_shape_check(B, H, T, d, hidden, chunk, dtype);
+    if (st != TTT_OK) return st;
+    if (!ttt::mlp_backward_supported(d, hidden, chunk))
+        return fail(TTT_ERR_UNSUPPORTED, "MLP backward: chunk must be at most 16 and the block tiles fit in shared "
+                                         "memory%s");
+    if (size_t(B) * H == 0) return TTT_OK;
+    CHECK_PTR(dW1_0);
+    CHECK_PTR(dW2_0);
+    if (dW1_T && !aligned16(dW1_T)) return fail(TTT_ERR_INVALID_ARG, "pointer not 16-byte aligned: %s", "dW1_T");
+    if (dW2_T && !aligned16(dW2_T)) return fail(TTT_ERR_INVALID_ARG, "pointer not 16-byte aligned: %s", "dW2_T");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (T == 0) {  // no tokens: the state gradients pass through
+        const size_t bytes = size_t(B) * H * d * hidden * sizeof(float);
+        cudaError_t e = dW1_T ? (dW1_T != dW1_0 ? cudaMemcpyAsync(dW1_0, dW1_T, bytes, cudaMemcpyDeviceToDevice, s)
+                                                 : cudaSuccess)
+                              : cudaMemsetAsync(dW1_0, 0, bytes, s);
+        if (e == cudaSuccess)
+            e = dW2_T ? (dW2_T != dW2_0 ? cudaMemcpyAsync(dW2_0, dW2_T, bytes, cudaMemcpyDeviceToDevice, s)
+                                        : cudaSuccess)
+                      : cudaMemsetAsync(dW2_0, 0, bytes, s);
+        if (e != cudaSuccess) return cuda_fail(e, "ttt_mlp_prefill_backward copy");
+        return TTT_OK;
+    }
+    CHECK_PTR(Q);
+    CHECK_PTR(K);
+    CHECK_PTR(V);
+    CHECK_PTR(eta);
+    CHECK_PTR(W1_hist);
+    CHECK_PTR(W2_hist);
+    CHECK_PTR(dZ);
+    CHECK_PTR(dQ);
+    CHECK_PTR(dK);
+    CHECK_PTR(dV);
+    CHECK_PTR(deta);
+    ttt::MlpBwdArgs a{Q, K, V, eta, W1_hist, W2_hist, dZ, dW1_T, dW2_T, dQ, dK, dV, deta, dW1_0, dW2_0,
+                      B, H, T, d, hidden, chunk, dtype == TTT_BF16 ? 1 : 0};
+    cudaError_t e = ttt::launch_mlp_backward(a, s);
+    if (e != cudaSuccess) return cuda_fail(e, "ttt_mlp_prefill_backward launch");
+    return TTT_OK;
+}
+
 ttt_status ttt_linear_decode_step(const void* q, const void* k, const void* v, const float* eta, float* W, void* z,
                                   int B, int H, int d, ttt_dtype dtype, void* stream) {
     g_last_error[0] = 0;

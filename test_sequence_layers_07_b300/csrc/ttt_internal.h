@@ -59,7 +59,32 @@ struct MlpArgs {
     float* W2_out;
     int B, H, T, d, hidden, chunk;
     int bf16;
+    void* W1_hist = nullptr;  // optional: the state at the start of every block, [B][H][nblk][d][hidden] and
+    void* W2_hist = nullptr;  // [B][H][nblk][hidden][d], in the element type of Q
 };
+
+// Gradient of the TTT-MLP chunked scan.
+struct MlpBwdArgs {
+    const void* Q;
+    const void* K;
+    const void* V;
+    const float* eta;
+    const void* W1_hist;  // [B][H][nblk][d][hidden], block-start W1 (element type of Q)
+    const void* W2_hist;  // [B][H][nblk][hidden][d]
+    const void* dZ;
+    const float* dW1_T;   // gradient of the final W1, or nullptr (zero)
+    const float* dW2_T;
+    void* dQ;
+    void* dK;
+    void* dV;
+    float* deta;
+    float* dW1_0;
+    float* dW2_0;
+    int B, H, T, d, hidden, chunk;
+    int bf16;
+};
+bool mlp_backward_supported(int d, int hidden, int chunk);
+cudaError_t launch_mlp_backward(const MlpBwdArgs& a, cudaStream_t s);
 
 struct DecodeArgs {
     const void* q;

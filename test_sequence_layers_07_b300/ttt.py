@@ -26,7 +26,8 @@ TTT_OK, TTT_ERR_INVALID_ARG, TTT_ERR_UNSUPPORTED, TTT_ERR_CUDA, TTT_ERR_TIMEOUT 
 TTT_F32, TTT_BF16 = 0, 1
 
 EXPORTED = ("ttt_linear_prefill", "ttt_linear_prefill_workspace_size", "ttt_linear_prefill_ws",
-            "ttt_linear_prefill_noalloc", "ttt_linear_momentum_prefill", "ttt_linear_prefill_hist", "ttt_linear_prefill_backward", "ttt_mlp_prefill",
+            "ttt_linear_prefill_noalloc", "ttt_linear_momentum_prefill", "ttt_linear_prefill_hist",
+            "ttt_mlp_prefill_hist", "ttt_mlp_prefill_backward", "ttt_linear_prefill_backward", "ttt_mlp_prefill",
             "ttt_linear_decode_step", "ttt_mlp_decode_step",
             "ttt_get_device_status", "ttt_selftest_wait_timeout", "ttt_status_string", "ttt_last_error", "ttt_version")
 
@@ -66,6 +67,11 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
             lib.ttt_linear_prefill_backward.argtypes = [vp, vp, vp, fp, fp, vp, fp, vp, vp, vp, fp, fp,
                                                         i, i, i, i, i, i, vp]
             lib.ttt_mlp_prefill.argtypes = [vp, vp, vp, fp, fp, fp, vp, fp, fp, i, i, i, i, i, i, i, vp]
+            lib.ttt_mlp_prefill_hist.argtypes = [vp, vp, vp, fp, fp, fp, vp, fp, fp, vp, vp, i, i, i, i, i, i, i, vp]
+            lib.ttt_mlp_prefill_hist.restype = i
+            lib.ttt_mlp_prefill_backward.argtypes = [vp, vp, vp, fp, vp, vp, vp, fp, fp, vp, vp, vp, fp, fp, fp,
+                                                     i, i, i, i, i, i, i, vp]
+            lib.ttt_mlp_prefill_backward.restype = i
             lib.ttt_linear_decode_step.argtypes = [vp, vp, vp, fp, fp, vp, i, i, i, i, vp]
             lib.ttt_mlp_decode_step.argtypes = [vp, vp, vp, fp, fp, fp, vp, i, i, i, i, i, vp]
             lib.ttt_get_device_status.argtypes = [vp]
@@ -259,6 +265,41 @@ def ttt_mlp_prefill(Q, K, V, eta, W1_0, W2_0, Z, W1_out, W2_out, chunk: int, str
     _check(st)
 
 
+def ttt_mlp_prefill_hist(Q, K, V, eta, W1_0, W2_0, Z, W1_out, W2_out, W1_hist, W2_hist, chunk: int,
+                         stream=None) -> None:
+    """TTT-MLP prefill that also writes the block-start states into W1_hist [B,H,nblk,d,hidden] and
+    W2_hist [B,H,nblk,hidden,d] (dtype of Q)."""
+    B, H, T, d = Q.shape
+    hd = W1_0.shape[-1]
+    dt = _io_dtype(Q)
+    nblk = -(-T // int(chunk))
+    if W1_hist.shape != (B, H, nblk, d, hd) or W2_hist.shape != (B, H, nblk, hd, d):
+        raise ValueError("W1_hist must be [B,H,nblk,d,hidden] and W2_hist [B,H,nblk,hidden,d]")
+    if W1_hist.dtype != Q.dtype or W2_hist.dtype != Q.dtype:
+        raise TypeError("W1_hist / W2_hist must have the dtype of Q")
+    st = load_library().ttt_mlp_prefill_hist(
+        _ptr(Q, "Q"), _ptr(K, "K"), _ptr(V, "V"), _ptr(eta, "eta", torch.float32), _ptr(W1_0, "W1_0", torch.float32),
+        _ptr(W2_0, "W2_0", torch.float32), _ptr(Z, "Z"), _ptr(W1_out, "W1_out", torch.float32),
+        _ptr(W2_out, "W2_out", torch.float32), _ptr(W1_hist, "W1_hist"), _ptr(W2_hist, "W2_hist"), B, H, T, d, hd,
+        int(chunk), dt, _stream(stream))
+    _check(st)
+
+
+def ttt_mlp_prefill_backward(Q, K, V, eta, W1_hist, W2_hist, dZ, dW1_T, dW2_T, dQ, dK, dV, deta, dW1_0, dW2_0,
+                             chunk: int, stream=None) -> None:
+    """Gradient of the TTT-MLP prefill into caller-allocated dQ, dK, dV, deta, dW1_0, dW2_0."""
+    B, H, T, d = Q.shape
+    hd = W1_hist.shape[-1]
+    dt = _io_dtype(Q)
+    st = load_library().ttt_mlp_prefill_backward(
+        _ptr(Q, "Q"), _ptr(K, "K"), _ptr(V, "V"), _ptr(eta, "eta", torch.float32), _ptr(W1_hist, "W1_hist"),
+        _ptr(W2_hist, "W2_hist"), _ptr(dZ, "dZ"), _ptr(dW1_T, "dW1_T", torch.float32),
+        _ptr(dW2_T, "dW2_T", torch.float32), _ptr(dQ, "dQ"), _ptr(dK, "dK"), _ptr(dV, "dV"),
+        _ptr(deta, "deta", torch.float32), _ptr(dW1_0, "dW1_0", torch.float32), _ptr(dW2_0, "dW2_0", torch.float32),
+        B, H, T, d, hd, int(chunk), dt, _stream(stream))
+    _check(st)
+
+
 def ttt_linear_decode_step(q, k, v, eta, W, z, stream=None) -> None:
     """One online TTT-Linear step; W [B,H,d,d] fp32 is updated in place, z written."""
     B, H, d = q.shape
@@ -363,6 +404,32 @@ def mlp_prefill(Q, K, V, eta, W1, W2, chunk: int, stream=None):
     W2o = torch.empty_like(W2)
     ttt_mlp_prefill(Q, K, V, eta, W1, W2, Z, W1o, W2o, chunk, stream)
     return Z, W1o, W2o
+
+
+def mlp_prefill_hist(Q, K, V, eta, W1, W2, chunk: int, stream=None):
+    """Returns (Z, W1_final, W2_final, W1_hist, W2_hist) for a TTT-MLP prefill that records the
+    block-start states."""
+    B, H, T, d = Q.shape
+    hd = W1.shape[-1]
+    nblk = -(-T // int(chunk))
+    Z, W1o, W2o = torch.empty_like(Q), torch.empty_like(W1), torch.empty_like(W2)
+    H1 = torch.empty((B, H, nblk, d, hd), dtype=Q.dtype, device=Q.device)
+    H2 = torch.empty((B, H, nblk, hd, d), dtype=Q.dtype, device=Q.device)
+    ttt_mlp_prefill_hist(Q, K, V, eta, W1, W2, Z, W1o, W2o, H1, H2, chunk, stream)
+    return Z, W1o, W2o, H1, H2
+
+
+def mlp_prefill_backward(Q, K, V, eta, W1_hist, W2_hist, dZ, dW1_T, dW2_T, chunk: int, stream=None):
+    """Returns (dQ, dK, dV, deta, dW1_0, dW2_0) of the TTT-MLP prefill."""
+    B, H, T, d = Q.shape
+    hd = W1_hist.shape[-1]
+    dQ, dK, dV = torch.empty_like(Q), torch.empty_like(Q), torch.empty_like(Q)
+    deta = torch.empty_like(eta)
+    dW1 = torch.empty((B, H, d, hd), dtype=torch.float32, device=Q.device)
+    dW2 = torch.empty((B, H, hd, d), dtype=torch.float32, device=Q.device)
+    ttt_mlp_prefill_backward(Q, K, V, eta, W1_hist, W2_hist, dZ, dW1_T, dW2_T, dQ, dK, dV, deta, dW1, dW2, chunk,
+                             stream)
+    return dQ, dK, dV, deta, dW1, dW2
 
 
 def mlp_decode_step(q, k, v, eta, W1, W2, stream=None):

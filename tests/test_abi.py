@@ -260,3 +260,24 @@ def test_linear_momentum_validation(lib):
     assert mp(chunk=0) == T.TTT_ERR_INVALID_ARG
     assert mp(d=48) == T.TTT_ERR_UNSUPPORTED
     assert mp(Q=NULL, M0=NULL, Mo=NULL, B_=0) == T.TTT_OK
+
+
+def test_mlp_hist_and_backward_validation(lib):
+    def hp(H1=A, H2=A, d=64, hd=256, chunk=16, B_=1):
+        return lib.ttt_mlp_prefill_hist(A, A, A, A, A, A, A, A, A, H1, H2, B_, 1, 16, d, hd, chunk, 1, None)
+
+    assert hp(H1=NULL) == T.TTT_ERR_INVALID_ARG
+    assert hp(H2=MIS) == T.TTT_ERR_INVALID_ARG
+    assert hp(d=128) == T.TTT_ERR_UNSUPPORTED
+    assert hp(H1=NULL, H2=NULL, B_=0) == T.TTT_OK
+
+    def bp(dW1T=A, dW10=A, chunk=16, d=64, hd=256, B_=1):
+        return lib.ttt_mlp_prefill_backward(A, A, A, A, A, A, A, dW1T, A, A, A, A, A, dW10, A, B_, 1, 16, d, hd,
+                                            chunk, 1, None)
+
+    assert bp(dW10=NULL) == T.TTT_ERR_INVALID_ARG
+    assert bp(dW1T=MIS) == T.TTT_ERR_INVALID_ARG
+    assert bp(chunk=32, hd=64) == T.TTT_ERR_UNSUPPORTED  # the backward takes blocks of at most 16 tokens
+    assert b"16" in lib.ttt_last_error()
+    assert bp(d=48) == T.TTT_ERR_UNSUPPORTED
+    assert bp(B_=0) == T.TTT_OK
