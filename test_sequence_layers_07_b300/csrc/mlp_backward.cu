@@ -236,16 +236,17 @@ mlp_backward_kernel(const TI* __restrict__ Q, const TI* __restrict__ K, const TI
                 for (int k = 0; k < d; ++k) a1 = fmaf(Ks[j * LD + k], c1[k], a1);
                 dHk[j * LH + mm] = -es[j] * a2;
                 dE1[j * LH + mm] = -es[j] * a1;
-                // deta_j -= (K dW1')_jm E1_jm
-                atomicAdd(&des[j], -a1 * E1[j * LH + mm]);
+                dZk[j * LH + mm] = a1 * E1[j * LH + mm];  // (K dW1')_jm E1_jm, summed over m below
             }
         }
         // dE2 = -D (Hk dW2'), with deta_j -= (Hk dW2')_j . E2_j
         hidden_sum(Hk, LH, b, d, h, [&](int m, int c) { return dW2g[size_t(m) * d + c]; }, red, dE2, LD, false, 1.f);
+        // deta_j = -(Hk dW2')_j . E2_j - (K dW1')_j . E1_j, summed in a fixed order (deterministic)
         for (int j = t; j < b; j += kNT) {
-            float s = 0.f;
+            float s = 0.f, s1 = 0.f;
             for (int c = 0; c < d; ++c) s = fmaf(dE2[j * LD + c], E2[j * LD + c], s);
-            atomicAdd(&des[j], -s);
+            for (int m = 0; m < h; ++m) s1 += dZk[j * LH + m];
+            des[j] = -s - s1;
         }
         __syncthreads();
         for (int idx = t; idx < b * d; idx += kNT) dE2[(idx / d) * LD + idx % d] *= -es[idx / d];
@@ -283,7 +284,7 @@ mlp_backward_kernel(const TI* __restrict__ Q, const TI* __restrict__ K, const TI
         for (int j = t; j < b; j += kNT) {
             float s = 0.f;
             for (int i = j; i < b; ++i) s = fmaf(dA2[i * LB + j], S2[i * LB + j], s);
-            atomicAdd(&des[j], s);
+            des[j] += s;
         }
         // dHq += dS2 Hk, dHk += dS2^T Hq with dS2 = M . dA2 D
         for (int idx = t; idx < b * h; idx += kNT) {
@@ -327,7 +328,7 @@ mlp_backward_kernel(const TI* __restrict__ Q, const TI* __restrict__ K, const TI
         for (int j = t; j < b; j += kNT) {
             float s = 0.f;
             for (int i = j; i < b; ++i) s = fmaf(dA1[i * LB + j], S1[i * LB + j], s);
-            atomicAdd(&des[j], s);
+            des[j] += s;
         }
         for (int idx = t; idx < b * d; idx += kNT) {
             const int i = idx / d, k = idx % d;
