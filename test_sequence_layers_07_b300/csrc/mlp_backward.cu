@@ -82,7 +82,20 @@ __device__ void hidden_sum(const float* X, int LH, int b, int d, int h, FY Y, fl
     for (int j = 0; j < 16; ++j) acc[j] = 0.f;
     if (grp < groups) {
         const int m0 = grp * per, m1 = min(h, m0 + per);
-        for (int m = m0; m < m1; ++m) {
+        // eight Y values in flight at a time: Y reads the block's recorded state or the running
+        // gradient from L2, so loading them one dependent step at a time would be latency-bound
+        int m = m0;
+        for (; m + 8 <= m1; m += 8) {
+            float y[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) y[u] = Y(m + u, c);
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                    if (j < b) acc[j] = fmaf(X[j * LH + m + u], y[u], acc[j]);
+        }
+        for (; m < m1; ++m) {
             const float y = Y(m, c);
 #pragma unroll
             for (int j = 0; j < 16; ++j)
