@@ -228,68 +228,85 @@ linear_segmap_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_const
 
 // ============================================================================ 2. combine
 
-// Grid (heads, D / 16), 256 threads: W_0 = the initial state, W_{s+1}[:, c0..c0+16) = W_s +
-// Delta_s W_s + B_s for s = 0..S-2, in fp32 with Delta_s staged in shared memory (rows padded to
-// D + 1 words: conflict-free).
+// Grid (heads, D / CW), D * CW threads (thread: row r = tid / CW, column c0 + tid % CW): W_0 = the
+// initial state, then W_{s+1}[:, c0..c0+CW) = W_s + Delta_s W_s + B_s for s = 0..S-2, in fp32.  Only
+// W_s is on the chain; Delta_s and B_s are known up front, so they stream NS - 1 hops ahead by
+// cp.async into a ring of stages (Delta rows as 16-byte chunks, chunk j of row r at j ^ (r & 7):
+// the eight rows a warp reads at once fall in distinct banks).  The state's columns are kept
+// transposed (column c as a row of D + 4 words, so the four columns a warp reads sit in distinct
+// banks) and double buffered: a hop reads Delta and W in 16-byte pieces and costs one barrier.
 template <int D>
-__global__ void __launch_bounds__(256) linear_segcombine_kernel(const float* __restrict__ W0,
-                                                                const float* __restrict__ maps,
-                                                                float* __restrict__ starts, int nseg) {
-    extern __shared__ float cmb[];
-    float* Dl = cmb;                 // [D][D + 1]
-    float* Wc = Dl + D * (D + 1);    // [D][16], the current start state's columns
-    float* Bc = Wc + D * 16;         // [D][16]
-    constexpr int RPT = D / 16;      // outputs per thread
+struct CombineCfg {
+    static constexpr int CW = 4, NT = D * CW, NS = 4;
+    static constexpr int DELTA = D * D, BROWS = D * CW, STAGE = DELTA + BROWS;  // floats
+    static constexpr int WLD = D + 4;                                           // floats per state column
+    static constexpr int BYTES = (NS * STAGE + 2 * CW * WLD) * 4;
+};
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+template <int D>
+__global__ void __launch_bounds__(CombineCfg<D>::NT) linear_segcombine_kernel(const float* __restrict__ W0,
+                                                                             const float* __restrict__ maps,
+                                                                             float* __restrict__ starts, int nseg) {
+    using C = CombineCfg<D>;
+    constexpr int CW = C::CW, NS = C::NS;
+    extern __shared__ __align__(16) float cmb[];
+    float* ring = cmb;                   // NS x [Delta (swizzled D x D) | B columns (D x CW)]
+    float* Wc = ring + NS * C::STAGE;    // [2][CW][WLD], the current start state's columns
     const size_t bh = blockIdx.x;
-    const int c0 = 16 * blockIdx.y;
-    const int tid = threadIdx.x, cc = tid & 15, r0 = tid >> 4;
-    float* Ws0 = starts + bh * nseg * size_t(D) * D;
-    for (int i = tid; i < D * 16; i += 256) {
-        const size_t at = size_t(i >> 4) * D + c0 + (i & 15);
-        Wc[i] = W0[bh * D * D + at];
-        Ws0[at] = Wc[i];
-    }
-    for (int s = 0; s + 1 < nseg; ++s) {
-        const float* Dm = maps + (bh * (nseg - 1) + s) * 2 * size_t(D) * D;
+    const int c0 = CW * blockIdx.y;
+    const int tid = threadIdx.x, cc = tid % CW, r = tid / CW;
+    const int hops = nseg - 1;
+    const float* mp = maps + bh * size_t(hops) * 2 * D * D;
+
+    auto issue = [&](int hop) {
+        float* st = ring + (hop % NS) * C::STAGE;
+        const float* Dm = mp + size_t(hop) * 2 * D * D;
         const float* Bm = Dm + size_t(D) * D;
-        // all loads of the hop in flight at once: D*D/4 float4 of Delta and 4 floats of B per thread
-        constexpr int NV = D * D / 4 / 256;
-        float4 dv[NV];
 #pragma unroll
-        for (int u = 0; u < NV; ++u) dv[u] = reinterpret_cast<const float4*>(Dm)[tid + 256 * u];
-        float bv[D * 16 / 256];
-#pragma unroll
-        for (int u = 0; u < D * 16 / 256; ++u) {
-            const int i = tid + 256 * u;
-            bv[u] = Bm[size_t(i >> 4) * D + c0 + (i & 15)];
+        for (int u = 0; u < D * D / 4 / C::NT; ++u) {
+            const int i = tid + C::NT * u, row = i / (D / 4), j = i % (D / 4);
+            cp_async16(smem_u32(st + row * D + ((j ^ (row & 7)) << 2)), Dm + size_t(row) * D + 4 * j);
         }
+        if (tid < D) cp_async16(smem_u32(st + C::DELTA + tid * CW), Bm + size_t(tid) * D + c0);
+    };
 #pragma unroll
-        for (int u = 0; u < NV; ++u) {
-            const int i = 4 * (tid + 256 * u), r = i / D, c = i % D;
-            float* dst = Dl + r * (D + 1) + c;
-            dst[0] = dv[u].x; dst[1] = dv[u].y; dst[2] = dv[u].z; dst[3] = dv[u].w;
-        }
-#pragma unroll
-        for (int u = 0; u < D * 16 / 256; ++u) Bc[tid + 256 * u] = bv[u];
-        __syncthreads();
-        float acc[RPT];
-#pragma unroll
-        for (int j = 0; j < RPT; ++j) acc[j] = 0.f;
-        for (int k = 0; k < D; ++k) {
-            const float wk = Wc[k * 16 + cc];
-#pragma unroll
-            for (int j = 0; j < RPT; ++j) acc[j] = fmaf(Dl[(r0 + 16 * j) * (D + 1) + k], wk, acc[j]);
-        }
-        __syncthreads();  // every thread is done reading Wc and Dl
-        float* Ws = starts + (bh * nseg + s + 1) * size_t(D) * D;
-#pragma unroll
-        for (int j = 0; j < RPT; ++j) {
-            const int r = r0 + 16 * j;
-            const float v = Wc[r * 16 + cc] + (acc[j] + Bc[r * 16 + cc]);
-            Ws[size_t(r) * D + c0 + cc] = v;
-            Wc[r * 16 + cc] = v;  // only this thread reads or writes this element in this phase
-        }
+    for (int p = 0; p < NS - 1; ++p) {
+        if (p < hops) issue(p);
+        cp_async_commit();
     }
+    float* Ws0 = starts + bh * nseg * size_t(D) * D;
+    float w = W0[bh * D * D + size_t(r) * D + c0 + cc];
+    Wc[cc * C::WLD + r] = w;
+    Ws0[size_t(r) * D + c0 + cc] = w;
+    for (int s = 0; s < hops; ++s) {
+        cp_async_wait<NS - 2>();  // this thread's copies of hop s have landed
+        __syncthreads();          // everyone's have; W_s is complete; hop s - 1's stage is free
+        if (s + NS - 1 < hops) issue(s + NS - 1);
+        cp_async_commit();
+        const float* st = ring + (s % NS) * C::STAGE;
+        const float* Wcur = Wc + (s & 1) * CW * C::WLD + cc * C::WLD;
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int kc = 0; kc < D / 4; ++kc) {
+            const float4 dq = *reinterpret_cast<const float4*>(st + r * D + ((kc ^ (r & 7)) << 2));
+            const float4 wq = *reinterpret_cast<const float4*>(Wcur + 4 * kc);
+            acc[0] = fmaf(dq.x, wq.x, acc[0]);
+            acc[1] = fmaf(dq.y, wq.y, acc[1]);
+            acc[2] = fmaf(dq.z, wq.z, acc[2]);
+            acc[3] = fmaf(dq.w, wq.w, acc[3]);
+        }
+        w = w + (((acc[0] + acc[1]) + (acc[2] + acc[3])) + st[C::DELTA + r * CW + cc]);
+        Wc[((s + 1) & 1) * CW * C::WLD + cc * C::WLD + r] = w;
+        starts[(bh * nseg + s + 1) * size_t(D) * D + size_t(r) * D + c0 + cc] = w;
+    }
+    cp_async_wait<0>();
 }
 
 // ============================================================================ 3. segment scan, d = 64
@@ -586,11 +603,12 @@ cudaError_t launch_maps(const LinearArgs& a, const SegPlan& p, float* maps, cuda
 
 template <int D>
 cudaError_t launch_combine(const LinearArgs& a, const SegPlan& p, const float* maps, float* starts, cudaStream_t s) {
-    const int bytes = (D * (D + 1) + 2 * D * 16) * 4;
+    using C = CombineCfg<D>;
     auto kern = linear_segcombine_kernel<D>;
     cudaError_t e;
-    if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) != cudaSuccess) return e;
-    kern<<<dim3(unsigned(a.B) * unsigned(a.H), D / 16), 256, bytes, s>>>(a.W0, maps, starts, p.nseg);
+    if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::BYTES)) != cudaSuccess)
+        return e;
+    kern<<<dim3(unsigned(a.B) * unsigned(a.H), D / C::CW), C::NT, C::BYTES, s>>>(a.W0, maps, starts, p.nseg);
     return cudaGetLastError();
 }
 

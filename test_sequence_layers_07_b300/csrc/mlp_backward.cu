@@ -25,7 +25,9 @@
 //
 // One CTA of 512 threads per (batch, head).  The block's intermediates (ten b x h tiles, six b x d,
 // four b x b) live in shared memory in fp32; W1, W2 of the block are read from the recorded states
-// (L2).  The running state gradient lives in dW1_0 / dW2_0 (fp32, L2-resident): every thread owns a
+// (L2).  A thread that needs a whole row of W2 (or of the running dW2) reads it with 16-byte loads:
+// one element per load would touch a 32-byte sector per 2- or 4-byte value, neighbouring threads
+// being a row (128 or 256 bytes) apart.  The running state gradient lives in dW1_0 / dW2_0 (fp32, L2-resident): every thread owns a
 // fixed set of their entries and adds its updates once per block, after the block's products have
 // read them as dW1', dW2'.  Products that sum over the hidden dimension are split over groups of
 // threads and summed through shared memory.
@@ -52,6 +54,60 @@ __device__ __forceinline__ float g_prime(float x) {
     return gp;
 }
 
+// the D elements of a row that starts on a 16-byte boundary into registers, in 16-byte pieces (the
+// entry point rejects buffers that do not start on one; d, h and d * h are multiples of 16)
+template <int D>
+__device__ __forceinline__ void load_row(const float* p, float (&out)[D]) {
+    const float4* q = reinterpret_cast<const float4*>(p);
+#pragma unroll
+    for (int u = 0; u < D / 4; ++u) {
+        const float4 v = q[u];
+        out[4 * u] = v.x, out[4 * u + 1] = v.y, out[4 * u + 2] = v.z, out[4 * u + 3] = v.w;
+    }
+}
+template <int D>
+__device__ __forceinline__ void load_row(const __nv_bfloat16* p, float (&out)[D]) {
+    const uint4* q = reinterpret_cast<const uint4*>(p);
+#pragma unroll
+    for (int u = 0; u < D / 8; ++u) {
+        const uint4 v = q[u];
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {  // a bf16 is the top half of an fp32
+            out[8 * u + 2 * e] = __uint_as_float(w[e] << 16);
+            out[8 * u + 2 * e + 1] = __uint_as_float(w[e] & 0xffff0000u);
+        }
+    }
+}
+
+// the second operand of a sum over the hidden index, Y(m, c): a [h][d] matrix (W2 and dW2: the eight
+// values of m..m+7 for column c sit d apart, one load each, coalesced across c) or a [d][h] one (W1
+// and dW1: the eight sit side by side in row c, read as 16-byte pieces when m is a multiple of 8)
+template <typename E>
+struct ByRow {
+    const E* p;
+    int ld;
+    __device__ float operator()(int m, int c) const { return to_f32(p[size_t(m) * ld + c]); }
+    __device__ void eight(int m, int c, bool, float (&y)[8]) const {
+#pragma unroll
+        for (int u = 0; u < 8; ++u) y[u] = (*this)(m + u, c);
+    }
+};
+template <typename E>
+struct ByCol {
+    const E* p;
+    int ld;
+    __device__ float operator()(int m, int c) const { return to_f32(p[size_t(c) * ld + m]); }
+    __device__ void eight(int m, int c, bool vec, float (&y)[8]) const {
+        if (vec) {
+            load_row<8>(p + size_t(c) * ld + m, y);
+        } else {
+#pragma unroll
+            for (int u = 0; u < 8; ++u) y[u] = (*this)(m + u, c);
+        }
+    }
+};
+
 struct Lay {
     int b, d, h, LD, LH, LB;
     size_t off[24];
@@ -70,40 +126,42 @@ struct Lay {
 };
 
 // sum over the hidden index m of X[j][m] * Y(m, c) for all j < b, c < d, into out[j][c] (+= when add):
-// thread t takes column c = t % d and hidden group t / d (as many groups as `red` holds partials
-// for); partials go through `red`.
+// thread t takes column c = t % d, hidden group (t / d) % groups (as many groups as `red` holds
+// partials for) and the tokens j = js, js + split, ... (js = t / (d * groups)), so that every thread
+// has a share; partials go through `red`.
 template <typename FY>
 __device__ void hidden_sum(const float* X, int LH, int b, int d, int h, FY Y, float* red, float* out, int LD,
                            bool add, float scale) {
     const int groups = min(kNT / d, kRed / (b * d)), per = (h + groups - 1) / groups;
-    const int t = threadIdx.x, c = t % d, grp = t / d;
+    const bool v8 = per % 8 == 0;  // every group's first m, and so every eight, on a 16-byte boundary
+    const int split = kNT / (groups * d);
+    const int t = threadIdx.x, c = t % d, grp = (t / d) % groups, js = t / (d * groups);
     float acc[16];
 #pragma unroll
-    for (int j = 0; j < 16; ++j) acc[j] = 0.f;
-    if (grp < groups) {
+    for (int u = 0; u < 16; ++u) acc[u] = 0.f;
+    {
         const int m0 = grp * per, m1 = min(h, m0 + per);
         // eight Y values in flight at a time: Y reads the block's recorded state or the running
         // gradient from L2, so loading them one dependent step at a time would be latency-bound
         int m = m0;
         for (; m + 8 <= m1; m += 8) {
             float y[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) y[u] = Y(m + u, c);
+            Y.eight(m, c, v8, y);
 #pragma unroll
             for (int u = 0; u < 8; ++u)
 #pragma unroll
-                for (int j = 0; j < 16; ++j)
-                    if (j < b) acc[j] = fmaf(X[j * LH + m + u], y[u], acc[j]);
+                for (int q = 0; q < 16; ++q)
+                    if (js + q * split < b) acc[q] = fmaf(X[(js + q * split) * LH + m + u], y[u], acc[q]);
         }
         for (; m < m1; ++m) {
             const float y = Y(m, c);
 #pragma unroll
-            for (int j = 0; j < 16; ++j)
-                if (j < b) acc[j] = fmaf(X[j * LH + m], y, acc[j]);
+            for (int q = 0; q < 16; ++q)
+                if (js + q * split < b) acc[q] = fmaf(X[(js + q * split) * LH + m], y, acc[q]);
         }
 #pragma unroll
-        for (int j = 0; j < 16; ++j)
-            if (j < b) red[(size_t(grp) * b + j) * d + c] = acc[j];
+        for (int q = 0; q < 16; ++q)
+            if (js + q * split < b) red[(size_t(grp) * b + js + q * split) * d + c] = acc[q];
     }
     __syncthreads();
     for (int idx = t; idx < b * d; idx += kNT) {
@@ -194,8 +252,7 @@ mlp_backward_kernel(const TI* __restrict__ Q, const TI* __restrict__ K, const TI
         }
         __syncthreads();
         // E2 = Hk W2 - V
-        hidden_sum(Hk, LH, b, d, h, [&](int m, int c) { return to_f32(W2[size_t(m) * d + c]); }, red, E2, LD, false,
-                   1.f);
+        hidden_sum(Hk, LH, b, d, h, ByRow<TI>{W2, d}, red, E2, LD, false, 1.f);
         for (int idx = t; idx < b * d; idx += kNT) E2[(idx / d) * LD + idx % d] -= Vs[(idx / d) * LD + idx % d];
         // S1 = Q K^T on the mask
         for (int idx = t; idx < b * b; idx += kNT) {
@@ -209,7 +266,7 @@ mlp_backward_kernel(const TI* __restrict__ Q, const TI* __restrict__ K, const TI
         // Gk = E2 W2^T, E1 = Gk . g'(Zk)
         if (jg < jgroups) {
             float wrow[D];
-            for (int c = 0; c < d; ++c) wrow[c] = to_f32(W2[size_t(mm) * d + c]);
+            load_row(W2 + size_t(mm) * d, wrow);
             for (int j = jg; j < b; j += jgroups) {
                 float gk = 0.f;
                 for (int c = 0; c < d; ++c) gk = fmaf(E2[j * LD + c], wrow[c], gk);
@@ -240,20 +297,23 @@ mlp_backward_kernel(const TI* __restrict__ Q, const TI* __restrict__ K, const TI
         // ---- the state update W2' = W2 - Hk^T D E2, W1' = W1 - K^T D E1 (dW' in dW1g / dW2g)
         // dHk = -D E2 dW2'^T and dE1 = -D K dW1' (thread: hidden unit mm)
         if (jg < jgroups) {
-            float r2[D], c1[D];
-            for (int c = 0; c < d; ++c) r2[c] = dW2g[size_t(mm) * d + c];
-            for (int k = 0; k < d; ++k) c1[k] = dW1g[size_t(k) * h + mm];
+            float r[D];  // row mm of dW2', then column mm of dW1' (one at a time: both would spill)
+            load_row(dW2g + size_t(mm) * d, r);
             for (int j = jg; j < b; j += jgroups) {
-                float a2 = 0.f, a1 = 0.f;
-                for (int c = 0; c < d; ++c) a2 = fmaf(E2[j * LD + c], r2[c], a2);
-                for (int k = 0; k < d; ++k) a1 = fmaf(Ks[j * LD + k], c1[k], a1);
+                float a2 = 0.f;
+                for (int c = 0; c < d; ++c) a2 = fmaf(E2[j * LD + c], r[c], a2);
                 dHk[j * LH + mm] = -es[j] * a2;
+            }
+            for (int k = 0; k < d; ++k) r[k] = dW1g[size_t(k) * h + mm];
+            for (int j = jg; j < b; j += jgroups) {
+                float a1 = 0.f;
+                for (int k = 0; k < d; ++k) a1 = fmaf(Ks[j * LD + k], r[k], a1);
                 dE1[j * LH + mm] = -es[j] * a1;
                 dZk[j * LH + mm] = a1 * E1[j * LH + mm];  // (K dW1')_jm E1_jm, summed over m below
             }
         }
         // dE2 = -D (Hk dW2'), with deta_j -= (Hk dW2')_j . E2_j
-        hidden_sum(Hk, LH, b, d, h, [&](int m, int c) { return dW2g[size_t(m) * d + c]; }, red, dE2, LD, false, 1.f);
+        hidden_sum(Hk, LH, b, d, h, ByRow<float>{dW2g, d}, red, dE2, LD, false, 1.f);
         // deta_j = -(Hk dW2')_j . E2_j - (K dW1')_j . E1_j, summed in a fixed order (deterministic)
         for (int j = t; j < b; j += kNT) {
             float s = 0.f, s1 = 0.f;
@@ -264,14 +324,14 @@ mlp_backward_kernel(const TI* __restrict__ Q, const TI* __restrict__ K, const TI
         __syncthreads();
         for (int idx = t; idx < b * d; idx += kNT) dE2[(idx / d) * LD + idx % d] *= -es[idx / d];
         // dK = -D E1 dW1'^T: sum over m of E1[j][m] dW1'[k][m]
-        hidden_sum(E1, LH, b, d, h, [&](int m, int k) { return dW1g[size_t(k) * h + m]; }, red, dKs, LD, false, 1.f);
+        hidden_sum(E1, LH, b, d, h, ByCol<float>{dW1g, h}, red, dKs, LD, false, 1.f);
         for (int idx = t; idx < b * d; idx += kNT) dKs[(idx / d) * LD + idx % d] *= -es[idx / d];
 
         // ---- Z = Hq W2 - (M . S2 D) E2
         // dHq = dZ W2^T
         if (jg < jgroups) {
             float wrow[D];
-            for (int c = 0; c < d; ++c) wrow[c] = to_f32(W2[size_t(mm) * d + c]);
+            load_row(W2 + size_t(mm) * d, wrow);
             for (int i = jg; i < b; i += jgroups) {
                 float a = 0.f;
                 for (int c = 0; c < d; ++c) a = fmaf(dZs[i * LD + c], wrow[c], a);
@@ -319,8 +379,7 @@ mlp_backward_kernel(const TI* __restrict__ Q, const TI* __restrict__ K, const TI
 
         // ---- Zq = Q W1 - (M . S1 D) E1
         // dQ += dZq W1^T (sum over m of dZq[i][m] W1[k][m])
-        hidden_sum(dZq, LH, b, d, h, [&](int m, int k) { return to_f32(W1[size_t(k) * h + m]); }, red, dQs, LD, true,
-                   1.f);
+        hidden_sum(dZq, LH, b, d, h, ByCol<TI>{W1, h}, red, dQs, LD, true, 1.f);
         // dA1 = -dZq E1^T on the mask
         for (int idx = t; idx < b * b; idx += kNT) {
             const int i = idx / b, j = idx % b;
@@ -365,12 +424,11 @@ mlp_backward_kernel(const TI* __restrict__ Q, const TI* __restrict__ K, const TI
         __syncthreads();
         float* dGk = dE1;
         // dE2 += dGk W2
-        hidden_sum(dGk, LH, b, d, h, [&](int m, int c) { return to_f32(W2[size_t(m) * d + c]); }, red, dE2, LD, true,
-                   1.f);
+        hidden_sum(dGk, LH, b, d, h, ByRow<TI>{W2, d}, red, dE2, LD, true, 1.f);
         // E2: dHk += dE2 W2^T; then dZk += dHk . g'(Zk)
         if (jg < jgroups) {
             float wrow[D];
-            for (int c = 0; c < d; ++c) wrow[c] = to_f32(W2[size_t(mm) * d + c]);
+            load_row(W2 + size_t(mm) * d, wrow);
             for (int j = jg; j < b; j += jgroups) {
                 float a = 0.f;
                 for (int c = 0; c < d; ++c) a = fmaf(dE2[j * LD + c], wrow[c], a);
@@ -381,8 +439,7 @@ mlp_backward_kernel(const TI* __restrict__ Q, const TI* __restrict__ K, const TI
         }
         __syncthreads();
         // dK += dZk W1^T
-        hidden_sum(dZk, LH, b, d, h, [&](int m, int k) { return to_f32(W1[size_t(k) * h + m]); }, red, dKs, LD, true,
-                   1.f);
+        hidden_sum(dZk, LH, b, d, h, ByCol<TI>{W1, h}, red, dKs, LD, true, 1.f);
 
         // ---- outputs of the block's tokens
         for (int idx = t; idx < b * d; idx += kNT) {
