@@ -39,6 +39,9 @@ METRIC = "TTT-Linear/MLP prefill tokens/s & % roofline; decode tokens/s & HBM GB
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 # the B300's rated figures: HBM3e bandwidth and dense bf16 tensor throughput
 RATED_PEAKS = {"hbm_gbs": 7700.0, "bf16_tflops": 2250.0}
+# fp32 FMA peak of the SIMT pipes: 148 SMs x 128 FMA lanes x 2 FLOP x 2.032 GHz (the maximum SM clock), the
+# ceiling of the kernels that run their contractions as plain fp32 multiply-adds
+FP32_ALU_TFLOPS = 148 * 128 * 2 * 2.032e9 / 1e12
 NROT = 4  # rotating input copies for the L2-sized workloads
 
 
@@ -370,7 +373,8 @@ def bench_momentum(T_mod, w, beta, steps, warmup, world, peaks, nrot=2):
             "bytes_per_launch": nbytes, "flops_per_launch": flops, "roofline_us": t_roof * 1e6,
             "frac": t_roof / (ms_launch * 1e-3), "frac_of_rated": rated_roof(nbytes, flops) / (ms_launch * 1e-3),
             "bound": "hbm" if nbytes / (peaks["hbm_gbs"] * 1e9) > flops / (peaks["bf16_tflops"] * 1e12) else "tensor",
-            "kernel": "SIMT fp32 (generic)"}
+            "kernel": "SIMT fp32 (generic)",
+            "alu_frac": flops / (ms_launch * 1e-3) / (FP32_ALU_TFLOPS * 1e12), "alu_peak_tflops": FP32_ALU_TFLOPS}
 
 
 def backward_bytes(B, H, T, d, chunk, elt=2):
@@ -479,7 +483,9 @@ def bench_mlp_backward(T_mod, w, steps, warmup, world, peaks, nrot=2):
             "backward_roofline_us": t_roof * 1e6, "backward_frac": t_roof / (ms_b_launch * 1e-3),
             "backward_frac_of_rated": rated_roof(nbytes, flops) / (ms_b_launch * 1e-3),
             "bound": "hbm" if nbytes / (peaks["hbm_gbs"] * 1e9) > flops / (peaks["bf16_tflops"] * 1e12) else "tensor",
-            "backward_kernel": "SIMT fp32"}
+            "backward_kernel": "SIMT fp32",
+            "backward_alu_frac": flops / (ms_b_launch * 1e-3) / (FP32_ALU_TFLOPS * 1e12),
+            "alu_peak_tflops": FP32_ALU_TFLOPS}
 
 
 def bench_decode(T_mod, w, steps, warmup, world, peaks, graph_steps=1024, nrot=NROT):
@@ -745,7 +751,9 @@ def run_reference(args, budget_s=150.0):
     print(json.dumps(line), flush=True)
 
 
-LINEAR_SRC = ["linear_segment.cu", "mma_tile.cuh", "ptx.cuh"]
+# sources of the headline kernel (the one-pass d = 64 prefill): the committed DRAM traffic counts only while
+# they are unchanged
+LINEAR_SRC = ["linear_prefill_fused.cu", "ptx.cuh", "ttt_common.cuh"]
 
 
 def main(argv=None):

@@ -18,8 +18,10 @@
 //        into it in fp32.
 //    G itself, packed as the A operand of that update, is also the B operand of the read-out's
 //    correction S G^T (S the masked scores), so the error never leaves the registers either.
-//  * Measured on B300, a warp-level m16n8k16 issues at one per ~8.3 cycles per SM sub-partition
-//    (~2.1 cycles per SM over the four), so the MMAs per sub-partition bound the time.  Per 16-token
+//  * Measured on B300: with the same operands in every instruction a warp-level m16n8k16 issues at
+//    one per ~8.1 cycles per warp (~2.0 cycles per SM from four warps on); with operands that change
+//    every instruction, as here, an SM gets through one per ~6 cycles however many warps share it,
+//    so the MMAs per SM bound the time.  Per 16-token
 //    sub-block a warp issues 26: 8 for K W, 8 for the update, 8 for Q W and 2 for the correction;
 //    the masked scores tril(Q K^T) (8 MMAs per sub-block, the same for every column group) are
 //    computed once per CTA: at the start of a stage each warp forms those of every CG-th
