@@ -473,6 +473,11 @@ def bench_mlp_backward(T_mod, w, steps, warmup, world, peaks, nrot=2):
         fwd(i)
     ms_f, ms_f_launch = timed_loop(fwd, steps, warmup, world)
     ms_b, ms_b_launch = timed_loop(bwd, steps, warmup, world)
+    # the library's choice for this shape (include/ttt.h): warp-level MMAs for bf16, d 64, hidden 256,
+    # chunk 16, unless TTT_MLP_BACKWARD_KERNEL=simt
+    mma = (w.dtype == "bf16" and w.d == 64 and w.hidden == 256 and w.chunk == 16 and w.T % 16 == 0
+           and os.environ.get("TTT_MLP_BACKWARD_KERNEL") != "simt")
+    backward_kernel = "warp-level MMA, bf16 operands" if mma else "SIMT fp32"
     nbytes = mlp_backward_bytes(w.B, w.H, w.T, w.d, w.hidden, w.chunk)
     flops = mlp_backward_flops(w.B, w.H, w.T, w.d, w.hidden, w.chunk)
     t_roof = max(nbytes / (peaks["hbm_gbs"] * 1e9), flops / (peaks["bf16_tflops"] * 1e12))
@@ -483,9 +488,7 @@ def bench_mlp_backward(T_mod, w, steps, warmup, world, peaks, nrot=2):
             "backward_roofline_us": t_roof * 1e6, "backward_frac": t_roof / (ms_b_launch * 1e-3),
             "backward_frac_of_rated": rated_roof(nbytes, flops) / (ms_b_launch * 1e-3),
             "bound": "hbm" if nbytes / (peaks["hbm_gbs"] * 1e9) > flops / (peaks["bf16_tflops"] * 1e12) else "tensor",
-            "backward_kernel": "SIMT fp32",
-            "backward_alu_frac": flops / (ms_b_launch * 1e-3) / (FP32_ALU_TFLOPS * 1e12),
-            "alu_peak_tflops": FP32_ALU_TFLOPS}
+            "backward_kernel": backward_kernel}
 
 
 def bench_decode(T_mod, w, steps, warmup, world, peaks, graph_steps=1024, nrot=NROT):

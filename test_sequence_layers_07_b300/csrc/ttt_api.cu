@@ -524,7 +524,12 @@ ttt_status ttt_mlp_prefill_backward(const void* Q, const void* K, const void* V,
     CHECK_PTR(deta);
     ttt::MlpBwdArgs a{Q, K, V, eta, W1_hist, W2_hist, dZ, dW1_T, dW2_T, dQ, dK, dV, deta, dW1_0, dW2_0,
                       B, H, T, d, hidden, chunk, dtype == TTT_BF16 ? 1 : 0};
-    cudaError_t e = ttt::launch_mlp_backward(a, s);
+    // bf16, d = 64, hidden = 256, chunk 16, 16 | T: the warp-MMA kernel; the SIMT kernel otherwise
+    // (TTT_MLP_BACKWARD_KERNEL = "simt" forces the SIMT kernel)
+    const char* kv = getenv("TTT_MLP_BACKWARD_KERNEL");
+    cudaError_t e = cudaErrorNotSupported;
+    if (!(kv && !strcmp(kv, "simt"))) e = ttt::launch_mlp_backward_mma(a, s);
+    if (e == cudaErrorNotSupported) e = ttt::launch_mlp_backward(a, s);
     if (e != cudaSuccess) return cuda_fail(e, "ttt_mlp_prefill_backward launch");
     return TTT_OK;
 }

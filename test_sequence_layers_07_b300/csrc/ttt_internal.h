@@ -85,6 +85,9 @@ struct MlpBwdArgs {
 };
 bool mlp_backward_supported(int d, int hidden, int chunk);
 cudaError_t launch_mlp_backward(const MlpBwdArgs& a, cudaStream_t s);
+// warp-MMA form for bf16, d = 64, hidden = 256, chunk 16, 16 | T (cudaErrorNotSupported otherwise)
+bool mlp_backward_mma_supported(const MlpBwdArgs& a);
+cudaError_t launch_mlp_backward_mma(const MlpBwdArgs& a, cudaStream_t s);
 
 struct DecodeArgs {
     const void* q;

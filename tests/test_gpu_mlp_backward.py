@@ -125,3 +125,41 @@ def test_mlp_backward_workload_shape_all_heads():
     ref = _oracle(x, dZ, dW1, dW2, w.chunk)
     check("mlp_backward B=8 H=12 d=64 h=256 T=2048 b=16", TOL["bf16"],
           **{n: (got, want) for n, got, want in zip(NAMES, grads, ref)})
+
+
+# bf16, d = 64, hidden = 256, chunk 16 with 16 | T runs the warp-MMA kernel; these cases span
+# several blocks and heads of it
+@pytest.mark.parametrize("with_state", [True, False])
+def test_mlp_backward_mma_shape_matches_oracle(with_state):
+    x = WL.mlp_inputs(2, 3, 96, 64, 256, seed=4400, dtype="bf16", w_std=0.1)
+    dZ, dW1, dW2 = _grads(2, 3, 96, 64, 256, 4401, "bf16", with_state)
+    grads = _run(x, dZ, dW1, dW2, 16)[5]
+    ref = _oracle(x, dZ, dW1, dW2, 16)
+    for name, got, want in zip(NAMES, grads, ref):
+        assert rel_err(got, want) <= TOL["bf16"], name
+
+
+def test_mlp_backward_mma_state_gradient_in_place():
+    # dW_T passed as dW_0 (the entry point allows it): read at the start, overwritten with dW_0
+    x = WL.mlp_inputs(1, 2, 48, 64, 256, seed=4500, dtype="bf16", w_std=0.1)
+    dZ, dW1, dW2 = _grads(1, 2, 48, 64, 256, 4501, "bf16")
+    g = cuda(x)
+    _, _, _, H1, H2 = T.mlp_prefill_hist(g["Q"], g["K"], g["V"], g["eta"], g["W1"], g["W2"], 16)
+    o1, o2 = dW1.cuda(), dW2.cuda()
+    dq, dk, dv = (torch.empty_like(g["Q"]) for _ in range(3))
+    de = torch.empty_like(g["eta"])
+    T.ttt_mlp_prefill_backward(g["Q"], g["K"], g["V"], g["eta"], H1, H2, dZ.cuda(), o1, o2, dq, dk, dv, de, o1, o2, 16)
+    torch.cuda.synchronize()
+    ref = _oracle(x, dZ, dW1, dW2, 16)
+    for name, got, want in zip(NAMES, (dq, dk, dv, de, o1, o2), ref):
+        assert rel_err(got, want) <= TOL["bf16"], name
+
+
+def test_mlp_backward_mma_and_simt_kernels_agree(monkeypatch):
+    x = WL.mlp_inputs(2, 2, 64, 64, 256, seed=4600, dtype="bf16", w_std=0.1)
+    dZ, dW1, dW2 = _grads(2, 2, 64, 64, 256, 4601, "bf16")
+    a = _run(x, dZ, dW1, dW2, 16)[5]
+    monkeypatch.setenv("TTT_MLP_BACKWARD_KERNEL", "simt")
+    b = _run(x, dZ, dW1, dW2, 16)[5]
+    for name, u, v in zip(NAMES, a, b):
+        assert rel_err(u, v.double().cpu().numpy()) <= TOL["bf16"], name
