@@ -891,6 +891,16 @@ mlp_backward_mma_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16
                 for (int e = 0; e < 4; ++e) dzk[j][e] = fmaf(dHk[j][e], Zk[j][e], Gk[j][e]);
             pack_slice(dzk, dZkA);
         }
+        // the running dW1 slice, loaded here so that its L2 round trip overlaps the dK partial
+        float2 u1[4][4][2];
+#pragma unroll
+        for (int mt = 0; mt < 4; ++mt)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float* p0 = dW1g + size_t(16 * mt + g) * HID + hw + 8 * j + 2 * t;
+                u1[mt][j][0] = *reinterpret_cast<const float2*>(p0);
+                u1[mt][j][1] = *reinterpret_cast<const float2*>(p0 + 8 * HID);
+            }
         {
             // dK partial = -D (E1 dW1'^T) + dZk W1^T (over this warp's hidden units)
             float P[8][4];
@@ -929,6 +939,16 @@ mlp_backward_mma_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16
         if (n >= 1) issue_state(n - 1);
         cp_async_commit();
         {
+            // the running dW2 slice, loaded before the dW1 products for the same reason
+            float2 u2[2][8][2];
+#pragma unroll
+            for (int p = 0; p < 2; ++p)
+#pragma unroll
+                for (int nt = 0; nt < 8; ++nt) {
+                    const float* p0 = dW2g + size_t(hw + 16 * p + g) * D + 8 * nt + 2 * t;
+                    u2[p][nt][0] = *reinterpret_cast<const float2*>(p0);
+                    u2[p][nt][1] = *reinterpret_cast<const float2*>(p0 + 8 * D);
+                }
             // dW1[:, slice] += Q^T dZq + K^T dZk (over tokens); refresh the bf16 copy
 #pragma unroll
             for (int mt = 0; mt < 4; ++mt) {
@@ -940,8 +960,7 @@ mlp_backward_mma_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16
                     const int r0 = 16 * mt + g, col = 8 * j + 2 * t;
                     float* p0 = dW1g + size_t(r0) * HID + hw + col;
                     float* p1 = p0 + 8 * HID;
-                    const float2 u0 = *reinterpret_cast<const float2*>(p0), u1 = *reinterpret_cast<const float2*>(p1);
-                    float c[4] = {u0.x, u0.y, u1.x, u1.y};
+                    float c[4] = {u1[mt][j][0].x, u1[mt][j][0].y, u1[mt][j][1].x, u1[mt][j][1].y};
                     uint32_t b0, b1;
                     btok(dZqA, j, b0, b1);
                     mma_bf16_16816(c, aQT, b0, b1);
@@ -971,8 +990,8 @@ mlp_backward_mma_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16
                         const int r0 = 16 * p + g, col = 16 * q + 8 * h + 2 * t;
                         float* p0 = dW2g + size_t(hw + r0) * D + col;
                         float* p1 = p0 + 8 * D;
-                        const float2 u0 = *reinterpret_cast<const float2*>(p0), u1 = *reinterpret_cast<const float2*>(p1);
-                        float c[4] = {u0.x, u0.y, u1.x, u1.y};
+                        const int nt = 2 * q + h;
+                        float c[4] = {u2[p][nt][0].x, u2[p][nt][0].y, u2[p][nt][1].x, u2[p][nt][1].y};
                         mma_bf16_16816(c, aHq, bz[2 * h], bz[2 * h + 1]);
                         mma_bf16_16816(c, aGk, be[2 * h], be[2 * h + 1]);
                         mma_bf16_16816(c, aHk, bd[2 * h], bd[2 * h + 1]);
