@@ -365,6 +365,10 @@ def bench_momentum(T_mod, w, beta, steps, warmup, world, peaks, nrot=2):
         T_mod.ttt_linear_momentum_prefill(s["Q"], s["K"], s["V"], s["eta"], s["W0"], s["M0"], Z, W, M, w.chunk, beta)
 
     ms, ms_launch = timed_loop(step, steps, warmup, world)
+    # the library's choice for this shape (include/ttt.h)
+    mma = (w.dtype == "bf16" and w.d == 64 and w.chunk == 16 and w.T % 16 == 0
+           and os.environ.get("TTT_LINEAR_MOMENTUM_KERNEL") != "simt")
+    kernel = "warp-level MMA, bf16 operands" if mma else "SIMT fp32 (generic)"
     nbytes = momentum_bytes(w.B, w.H, w.T, w.d)
     flops = momentum_flops(w.B, w.H, w.T, w.d, w.chunk)
     t_roof = max(nbytes / (peaks["hbm_gbs"] * 1e9), flops / (peaks["bf16_tflops"] * 1e12))
@@ -373,8 +377,7 @@ def bench_momentum(T_mod, w, beta, steps, warmup, world, peaks, nrot=2):
             "bytes_per_launch": nbytes, "flops_per_launch": flops, "roofline_us": t_roof * 1e6,
             "frac": t_roof / (ms_launch * 1e-3), "frac_of_rated": rated_roof(nbytes, flops) / (ms_launch * 1e-3),
             "bound": "hbm" if nbytes / (peaks["hbm_gbs"] * 1e9) > flops / (peaks["bf16_tflops"] * 1e12) else "tensor",
-            "kernel": "SIMT fp32 (generic)",
-            "alu_frac": flops / (ms_launch * 1e-3) / (FP32_ALU_TFLOPS * 1e12), "alu_peak_tflops": FP32_ALU_TFLOPS}
+            "kernel": kernel}
 
 
 def backward_bytes(B, H, T, d, chunk, elt=2):

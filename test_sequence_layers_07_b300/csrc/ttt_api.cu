@@ -295,7 +295,12 @@ ttt_status ttt_linear_momentum_prefill(const void* Q, const void* K, const void*
     a.M0 = M0;
     a.M_out = M_out;
     a.beta = beta;
-    cudaError_t e = ttt::launch_linear_prefill_generic(a, s);
+    // bf16, d = 64, chunk 16, 16 | T: the warp-MMA kernel; the SIMT kernel otherwise
+    // (TTT_LINEAR_MOMENTUM_KERNEL = "simt" forces the SIMT kernel)
+    const char* kv = getenv("TTT_LINEAR_MOMENTUM_KERNEL");
+    cudaError_t e = cudaErrorNotSupported;
+    if (!(kv && !strcmp(kv, "simt"))) e = ttt::launch_linear_momentum_mma(a, s);
+    if (e == cudaErrorNotSupported) e = ttt::launch_linear_prefill_generic(a, s);
     if (e != cudaSuccess) return cuda_fail(e, "ttt_linear_momentum_prefill launch");
     return TTT_OK;
 }

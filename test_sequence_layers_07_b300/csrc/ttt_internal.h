@@ -22,7 +22,7 @@ struct LinearArgs {
     void* W_hist = nullptr;  // optional: the state at the start of every block, [B][H][nblk][d][d],
                              // in the element type of Q (bf16: the state rounded RN-even)
     uint64_t wait_ns = 0;    // bound of the fused kernel's barrier waits (0: the default 4 s)
-    // the momentum variant (generic kernel only): M0 (nullptr: zero) and M_out [B][H][d][d] fp32
+    // the momentum variant: M0 (nullptr: zero) and M_out [B][H][d][d] fp32
     bool momentum = false;
     const float* M0 = nullptr;
     float* M_out = nullptr;
@@ -84,6 +84,10 @@ struct MlpBwdArgs {
     int bf16;
 };
 bool mlp_backward_supported(int d, int hidden, int chunk);
+// TTT-Linear prefill with momentum on warp-level MMAs: bf16, d = 64, chunk 16, 16 | T
+// (cudaErrorNotSupported otherwise)
+bool linear_momentum_mma_supported(const LinearArgs& a);
+cudaError_t launch_linear_momentum_mma(const LinearArgs& a, cudaStream_t s);
 cudaError_t launch_mlp_backward(const MlpBwdArgs& a, cudaStream_t s);
 // warp-MMA form for bf16, d = 64, hidden = 256, chunk 16, 16 | T (cudaErrorNotSupported otherwise)
 bool mlp_backward_mma_supported(const MlpBwdArgs& a);

@@ -100,3 +100,33 @@ def test_momentum_headline_shape_all_heads():
     r = f64(x)
     Zr, Wr, Mr = O.linear_momentum_dual(r["Q"], r["K"], r["V"], r["eta"], r["W0"], WL.to_f64(M0), 0.9, w.chunk)
     check("linear_momentum B=8 H=12 d=64 T=2048 b=16 beta=0.9", TOL["bf16"], Z=(Z, Zr), W=(W, Wr), M=(M, Mr))
+
+
+# bf16, d = 64, chunk 16 with 16 | T runs the warp-MMA kernel
+@pytest.mark.parametrize("beta", [0.0, 0.5, 0.9, 1.0])
+@pytest.mark.parametrize("B,H", [(2, 3), (1, 1)])  # 6 heads: one CTA per head; 1 head: one per column group
+def test_momentum_mma_shape(beta, B, H):
+    x = WL.linear_inputs(B, H, 160, 64, seed=3600 + B * H, dtype="bf16")
+    M0 = _m0(x, 3601, zero=(beta == 0.5))
+    g = cuda(x)
+    Z, W, M = T.linear_momentum_prefill(g["Q"], g["K"], g["V"], g["eta"], g["W0"],
+                                        None if M0 is None else M0.cuda(), 16, beta)
+    torch.cuda.synchronize()
+    r = f64(x)
+    Zr, Wr, Mr = O.linear_momentum_dual(r["Q"], r["K"], r["V"], r["eta"], r["W0"],
+                                        None if M0 is None else WL.to_f64(M0), beta, 16)
+    assert rel_err(Z, Zr) <= TOL["bf16"]
+    assert rel_err(W, Wr) <= TOL["bf16"]
+    assert rel_err(M, Mr) <= TOL["bf16"]
+
+
+def test_momentum_mma_and_simt_kernels_agree(monkeypatch):
+    x = WL.linear_inputs(2, 2, 256, 64, seed=3700, dtype="bf16")
+    M0 = _m0(x, 3701)
+    g = cuda(x)
+    a = T.linear_momentum_prefill(g["Q"], g["K"], g["V"], g["eta"], g["W0"], M0.cuda(), 16, 0.9)
+    monkeypatch.setenv("TTT_LINEAR_MOMENTUM_KERNEL", "simt")
+    b = T.linear_momentum_prefill(g["Q"], g["K"], g["V"], g["eta"], g["W0"], M0.cuda(), 16, 0.9)
+    torch.cuda.synchronize()
+    for u, v in zip(a, b):
+        assert rel_err(u, v.double().cpu().numpy()) <= TOL["bf16"]
