@@ -15,8 +15,11 @@
 // W^T and M^T of its columns in registers in the m16n8k16 accumulator layout; read as bf16 pairs
 // they are the A operand of W^T K^T and the B operand of Q W, Q M.  E^T stays in registers: scaled
 // per token it is the A operand of the two rank-16 updates, unscaled the B operand of the
-// correction.  Each warp forms its own masked scores.  The chunk weights come from four-step warp
-// scans over the 16 step sizes.  Q/K/V/eta tiles are double buffered by cp.async one chunk ahead.
+// correction.  Chunks run in stages of SPS: the state-independent part of a chunk (the chunk weights
+// by four-step warp scans over its step sizes, and the masked, weighted scores -(Gamma . tril(Q K^T))
+// as a bf16 A fragment) is formed once per CTA, each warp taking every CG-th chunk of the stage, and
+// shared through shared memory; Q/K/V/eta of the next stage arrive by cp.async meanwhile.  Two CTA
+// barriers per stage.
 #include "ptx.cuh"
 #include "ttt_common.cuh"
 #include "ttt_internal.h"
@@ -27,7 +30,12 @@ namespace {
 using namespace ptx;
 
 constexpr int D = 64, KS = D / 16, NT = D / 8, TILE = 16 * D * 2;
-constexpr int BUF = 3 * TILE + 64;  // Q K V [16][64] bf16, eta
+constexpr int SPS = 4;                   // chunks per stage
+constexpr int CHUNK = 3 * TILE + 64;     // Q K V [16][64] bf16, eta
+constexpr int STAGE = SPS * CHUNK;
+constexpr int OFF_AC = 2 * STAGE;        // per chunk of the stage: the correction's A fragment, 16 B per lane
+constexpr int OFF_TW = OFF_AC + SPS * 512;  // per chunk: c[16], Bs[17], beta^k (k = 0..16)
+constexpr int SMEM_BYTES = OFF_TW + SPS * 64 * 4;
 
 // byte offset of (row, col) in a [16][64] bf16 tile (128-byte rows, 16-byte chunk XOR row % 8)
 __device__ __forceinline__ uint32_t sw(int row, int col) {
@@ -37,7 +45,6 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait0() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 
 template <int CG>
@@ -52,18 +59,20 @@ linear_momentum_mma_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloa
     const int lj = lane >> 3, lr = lane & 7;
     const size_t bh = blockIdx.x;
     const int cw0 = (blockIdx.y * CG + warp) * 16;  // first output column of this warp's group
-    const int nblk = T / 16;
-    float* wts = reinterpret_cast<float*>(smem + 2 * BUF) + warp * 64;  // [c 16][Bs 17][beta^k 17]
+    const int nblk = T / 16, nstg = (nblk + SPS - 1) / SPS;
+    float* tws = reinterpret_cast<float*>(smem + OFF_TW);
 
-    auto issue = [&](int m) {
-        const uint32_t b = sb + (m & 1) * BUF;
-        const size_t row0 = bh * size_t(T) + size_t(m) * 16;
-        for (int c = tid; c < 3 * 128; c += 32 * CG) {
-            const int tile = c >> 7, row = (c >> 3) & 15, ch = c & 7;
+    auto issue = [&](int si) {
+        const uint32_t b = sb + (si & 1) * STAGE;
+        const int n = min(SPS, nblk - si * SPS);
+        const size_t row0 = bh * size_t(T) + size_t(si) * SPS * 16;
+        for (int c = tid; c < n * 384; c += 32 * CG) {
+            const int i = c / 384, r = c % 384, tile = r >> 7, row = (r >> 3) & 15, ch = r & 7;
             const __nv_bfloat16* src = tile == 0 ? Q : tile == 1 ? K : V;
-            cp_async16(b + tile * TILE + sw(row, 8 * ch), src + (row0 + row) * D + 8 * ch);
+            cp_async16(b + i * CHUNK + tile * TILE + sw(row, 8 * ch), src + (row0 + 16 * i + row) * D + 8 * ch);
         }
-        if (tid < 4) cp_async16(b + 3 * TILE + 16 * tid, eta + row0 + 4 * tid);
+        for (int c = tid; c < n * 4; c += 32 * CG)
+            cp_async16(b + (c >> 2) * CHUNK + 3 * TILE + 16 * (c & 3), eta + row0 + 4 * c);
     };
 
     // ldmatrix coordinates: B with n = token, k = d (K in W^T K^T and Q K^T); A with m = token, k = d
@@ -75,6 +84,7 @@ linear_momentum_mma_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloa
         off_tk[ks] = sw(lr + 8 * (lj & 1), 16 * ks + 8 * (lj >> 1));
     }
     const uint32_t off_v = sw(lr + 8 * (lj >> 1), cw0 + 8 * (lj & 1));
+    const int jc[4] = {2 * t, 2 * t + 1, 8 + 2 * t, 9 + 2 * t};
 
     // W^T and M^T of the columns: x[nt][0..3] = X[8 nt + 2t (+1)][cw0 + g (+8)]
     float w[NT][4], m[NT][4];
@@ -91,186 +101,206 @@ linear_momentum_mma_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloa
         }
     }
 
-    if (nblk > 0) issue(0);
+    if (nstg > 0) issue(0);
     cp_async_commit();
     __nv_bfloat16* zb = Z + bh * size_t(T) * D + cw0 + 2 * t;
-    for (int nb = 0; nb < nblk; ++nb) {
-        if (nb + 1 < nblk) issue(nb + 1);
+    for (int si = 0; si < nstg; ++si) {
+        const int n = min(SPS, nblk - si * SPS);
+        cp_async_wait0();
+        __syncthreads();  // stage si has landed; every warp is done with stage si - 1 and its shared products
+        if (si + 1 < nstg) issue(si + 1);
         cp_async_commit();
-        cp_async_wait1();
-        __syncthreads();
-        const uint32_t b = sb + (nb & 1) * BUF;
-        const float* es = reinterpret_cast<const float*>(smem + (nb & 1) * BUF + 3 * TILE);
+        const uint32_t st = sb + (si & 1) * STAGE;
 
-        // ---- chunk weights (lanes 0..15 hold token i = lane; four-step scans)
-        {
-            const int i = lane & 15;
-            const float ei = es[i];
-            float p = beta;  // beta^(i+1) by a prefix product
+        // ---- the state-independent part of each chunk, once per CTA
+        for (int i = warp; i < n; i += CG) {
+            const uint32_t b = st + i * CHUNK;
+            const float* es = reinterpret_cast<const float*>(smem + (b - sb) + 3 * TILE);
+            float* tw = tws + i * 64;
+            {  // lanes 0..15 hold token k = lane: beta^(k+1), c_k, Bs_k by four-step scans
+                const int k = lane & 15;
+                const float ek = es[k];
+                float p = beta;
 #pragma unroll
-            for (int o = 1; o < 16; o <<= 1) {
-                const float q = __shfl_up_sync(0xffffffffu, p, o, 16);
-                if (i >= o) p *= q;
+                for (int o = 1; o < 16; o <<= 1) {
+                    const float q = __shfl_up_sync(0xffffffffu, p, o, 16);
+                    if (k >= o) p *= q;
+                }
+                float c = ek * p;
+#pragma unroll
+                for (int o = 1; o < 16; o <<= 1) {
+                    const float q = __shfl_up_sync(0xffffffffu, c, o, 16);
+                    if (k >= o) c += q;
+                }
+                float bs = ek, bo = beta;
+#pragma unroll
+                for (int o = 1; o < 16; o <<= 1) {
+                    const float q = __shfl_down_sync(0xffffffffu, bs, o, 16);
+                    if (k + o < 16) bs = fmaf(bo, q, bs);
+                    bo *= bo;
+                }
+                const float pk = __shfl_up_sync(0xffffffffu, p, 1, 16);  // beta^k
+                if (lane < 16) {
+                    tw[k] = c;
+                    tw[16 + k] = bs;
+                    tw[33 + k] = k == 0 ? 1.f : pk;
+                }
+                if (lane == 15) {
+                    tw[32] = 0.f;  // Bs_16
+                    tw[49] = p;    // beta^16
+                }
+                __syncwarp();
             }
-            float c = ei * p;  // c_i: prefix sum of eta_l beta^(l+1)
+            // S = Q K^T, then the correction's A fragment -(Gamma . tril(S))
+            float sa[2][4];
 #pragma unroll
-            for (int o = 1; o < 16; o <<= 1) {
-                const float q = __shfl_up_sync(0xffffffffu, c, o, 16);
-                if (i >= o) c += q;
+            for (int ks = 0; ks < KS; ++ks) {
+                uint32_t kb[4], qa[4];
+                ldsm_x4(b + TILE + off_nk[ks], kb);
+                ldsm_x4(b + off_tk[ks], qa);
+                if (ks == 0) {
+                    mma_bf16_16816_z(sa[0], qa, kb[0], kb[1]);
+                    mma_bf16_16816_z(sa[1], qa, kb[2], kb[3]);
+                } else {
+                    mma_bf16_16816(sa[0], qa, kb[0], kb[1]);
+                    mma_bf16_16816(sa[1], qa, kb[2], kb[3]);
+                }
             }
-            float bs = ei, bo = beta;  // Bs_i = eta_i + beta Bs_{i+1}: suffix recurrence by doubling
-#pragma unroll
-            for (int o = 1; o < 16; o <<= 1) {
-                const float q = __shfl_down_sync(0xffffffffu, bs, o, 16);
-                if (i + o < 16) bs = fmaf(bo, q, bs);
-                bo *= bo;
-            }
-            const float pk = __shfl_up_sync(0xffffffffu, p, 1, 16);  // beta^i (lane 0: 1)
-            if (lane < 16) {
-                wts[i] = c;
-                wts[16 + i] = bs;
-                wts[33 + i] = i == 0 ? 1.f : pk;
-            }
-            if (lane == 15) {
-                wts[32] = 0.f;   // Bs_16
-                wts[49] = p;     // beta^16
-            }
-            __syncwarp();
-        }
-
-        // ---- fragments of the chunk
-        uint32_t kb[KS][4], qa[KS][4], kt[KS][4], vv[4];
-#pragma unroll
-        for (int ks = 0; ks < KS; ++ks) {
-            ldsm_x4(b + TILE + off_nk[ks], kb[ks]);
-            ldsm_x4(b + off_tk[ks], qa[ks]);
-            ldsm_x4_trans(b + TILE + off_tk[ks], kt[ks]);
-        }
-        ldsm_x4_trans(b + 2 * TILE + off_v, vv);
-
-        // ---- S = Q K^T (tokens x tokens)
-        float sa[2][4];
-        mma_bf16_16816_z(sa[0], qa[0], kb[0][0], kb[0][1]);
-        mma_bf16_16816_z(sa[1], qa[0], kb[0][2], kb[0][3]);
-#pragma unroll
-        for (int ks = 1; ks < KS; ++ks) {
-            mma_bf16_16816(sa[0], qa[ks], kb[ks][0], kb[ks][1]);
-            mma_bf16_16816(sa[1], qa[ks], kb[ks][2], kb[ks][3]);
-        }
-        // ---- P^T = W^T K^T (columns x tokens) at the chunk-start state; Q W and Q M
-        uint32_t wa[KS][4], ma[KS][4];
-#pragma unroll
-        for (int ks = 0; ks < KS; ++ks) {
-            wa[ks][0] = pack_bf16(w[2 * ks][0], w[2 * ks][1]);
-            wa[ks][1] = pack_bf16(w[2 * ks][2], w[2 * ks][3]);
-            wa[ks][2] = pack_bf16(w[2 * ks + 1][0], w[2 * ks + 1][1]);
-            wa[ks][3] = pack_bf16(w[2 * ks + 1][2], w[2 * ks + 1][3]);
-            ma[ks][0] = pack_bf16(m[2 * ks][0], m[2 * ks][1]);
-            ma[ks][1] = pack_bf16(m[2 * ks][2], m[2 * ks][3]);
-            ma[ks][2] = pack_bf16(m[2 * ks + 1][0], m[2 * ks + 1][1]);
-            ma[ks][3] = pack_bf16(m[2 * ks + 1][2], m[2 * ks + 1][3]);
-        }
-        float pa[2][2][4], za[2][4], zm[2][4];
-#pragma unroll
-        for (int ks = 0; ks < KS; ++ks) {
-            if (ks < 2) {
-                mma_bf16_16816_z(pa[ks][0], wa[ks], kb[ks][0], kb[ks][1]);
-                mma_bf16_16816_z(pa[ks][1], wa[ks], kb[ks][2], kb[ks][3]);
-            } else {
-                mma_bf16_16816(pa[ks & 1][0], wa[ks], kb[ks][0], kb[ks][1]);
-                mma_bf16_16816(pa[ks & 1][1], wa[ks], kb[ks][2], kb[ks][3]);
-            }
-            if (ks == 0) {
-                mma_bf16_16816_z(za[0], qa[0], wa[0][0], wa[0][2]);
-                mma_bf16_16816_z(za[1], qa[0], wa[0][1], wa[0][3]);
-                mma_bf16_16816_z(zm[0], qa[0], ma[0][0], ma[0][2]);
-                mma_bf16_16816_z(zm[1], qa[0], ma[0][1], ma[0][3]);
-            } else {
-                mma_bf16_16816(za[0], qa[ks], wa[ks][0], wa[ks][2]);
-                mma_bf16_16816(za[1], qa[ks], wa[ks][1], wa[ks][3]);
-                mma_bf16_16816(zm[0], qa[ks], ma[ks][0], ma[ks][2]);
-                mma_bf16_16816(zm[1], qa[ks], ma[ks][1], ma[ks][3]);
-            }
-        }
-        // E^T = P^T - V^T: e[h][0..3] = (c = g, j), (g, j + 1), (g + 8, j), (g + 8, j + 1), j = 8 h + 2t
-        float e[2][4];
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            e[h][0] = (pa[0][h][0] + pa[1][h][0]) - bf16_lo(vv[2 * h]);
-            e[h][1] = (pa[0][h][1] + pa[1][h][1]) - bf16_hi(vv[2 * h]);
-            e[h][2] = (pa[0][h][2] + pa[1][h][2]) - bf16_lo(vv[2 * h + 1]);
-            e[h][3] = (pa[0][h][3] + pa[1][h][3]) - bf16_hi(vv[2 * h + 1]);
-        }
-
-        // ---- read-out Z = Q W - diag(c) Q M - (Gamma . tril(S)) E
-        const int jc[4] = {2 * t, 2 * t + 1, 8 + 2 * t, 9 + 2 * t};
-        float bsj[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) bsj[q] = wts[16 + jc[q]];
-        {
             uint32_t ac[4];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {  // A fragment register q: rows i = g + 8 (q & 1), cols j = 8 (q >> 1) + 2t (+1)
+            for (int q = 0; q < 4; ++q) {  // register q: rows i = g + 8 (q & 1), cols j = 8 (q >> 1) + 2t (+1)
                 float v[2];
 #pragma unroll
                 for (int u = 0; u < 2; ++u) {
-                    const int i = g + 8 * (q & 1), j = 8 * (q >> 1) + 2 * t + u;
+                    const int r = g + 8 * (q & 1), j = 8 * (q >> 1) + 2 * t + u;
                     const float s = sa[q >> 1][2 * (q & 1) + u];
-                    v[u] = j <= i ? -(bsj[2 * (q >> 1) + u] - wts[33 + i + 1 - j] * wts[16 + i + 1]) * s : 0.f;
+                    v[u] = j <= r ? -(tw[16 + j] - tw[33 + r + 1 - j] * tw[16 + r + 1]) * s : 0.f;
                 }
                 ac[q] = pack_bf16(v[0], v[1]);
             }
-            const uint32_t ea[4] = {pack_bf16(e[0][0], e[0][1]), pack_bf16(e[0][2], e[0][3]),
-                                    pack_bf16(e[1][0], e[1][1]), pack_bf16(e[1][2], e[1][3])};
-            const float cg0 = wts[g], cg8 = wts[g + 8];
-            float zp[2][4];
+            *reinterpret_cast<uint4*>(smem + OFF_AC + i * 512 + lane * 16) = make_uint4(ac[0], ac[1], ac[2], ac[3]);
+        }
+        __syncthreads();  // every chunk's weights and correction fragment are written
+
+        // ---- the chain: one chunk at a time through this warp's state; a full stage is unrolled, so
+        // the compiler can load the next chunk's fragments while this chunk's products are in flight
+        auto chunk = [&](const int i) {
+            const uint32_t b = st + i * CHUNK;
+            const float* tw = tws + i * 64;
+            uint32_t kb[KS][4], qa[KS][4], kt[KS][4], vv[4];
+#pragma unroll
+            for (int ks = 0; ks < KS; ++ks) {
+                ldsm_x4(b + TILE + off_nk[ks], kb[ks]);
+                ldsm_x4(b + off_tk[ks], qa[ks]);
+                ldsm_x4_trans(b + TILE + off_tk[ks], kt[ks]);
+            }
+            ldsm_x4_trans(b + 2 * TILE + off_v, vv);
+            uint32_t wa[KS][4], ma[KS][4];
+#pragma unroll
+            for (int ks = 0; ks < KS; ++ks) {
+                wa[ks][0] = pack_bf16(w[2 * ks][0], w[2 * ks][1]);
+                wa[ks][1] = pack_bf16(w[2 * ks][2], w[2 * ks][3]);
+                wa[ks][2] = pack_bf16(w[2 * ks + 1][0], w[2 * ks + 1][1]);
+                wa[ks][3] = pack_bf16(w[2 * ks + 1][2], w[2 * ks + 1][3]);
+                ma[ks][0] = pack_bf16(m[2 * ks][0], m[2 * ks][1]);
+                ma[ks][1] = pack_bf16(m[2 * ks][2], m[2 * ks][3]);
+                ma[ks][2] = pack_bf16(m[2 * ks + 1][0], m[2 * ks + 1][1]);
+                ma[ks][3] = pack_bf16(m[2 * ks + 1][2], m[2 * ks + 1][3]);
+            }
+            // P^T = W^T K^T (columns x tokens) at the chunk-start state; Q W and Q M
+            float pa[2][2][4], za[2][4], zm[2][4];
+#pragma unroll
+            for (int ks = 0; ks < KS; ++ks) {
+                if (ks < 2) {
+                    mma_bf16_16816_z(pa[ks][0], wa[ks], kb[ks][0], kb[ks][1]);
+                    mma_bf16_16816_z(pa[ks][1], wa[ks], kb[ks][2], kb[ks][3]);
+                } else {
+                    mma_bf16_16816(pa[ks & 1][0], wa[ks], kb[ks][0], kb[ks][1]);
+                    mma_bf16_16816(pa[ks & 1][1], wa[ks], kb[ks][2], kb[ks][3]);
+                }
+                if (ks == 0) {
+                    mma_bf16_16816_z(za[0], qa[0], wa[0][0], wa[0][2]);
+                    mma_bf16_16816_z(za[1], qa[0], wa[0][1], wa[0][3]);
+                    mma_bf16_16816_z(zm[0], qa[0], ma[0][0], ma[0][2]);
+                    mma_bf16_16816_z(zm[1], qa[0], ma[0][1], ma[0][3]);
+                } else {
+                    mma_bf16_16816(za[0], qa[ks], wa[ks][0], wa[ks][2]);
+                    mma_bf16_16816(za[1], qa[ks], wa[ks][1], wa[ks][3]);
+                    mma_bf16_16816(zm[0], qa[ks], ma[ks][0], ma[ks][2]);
+                    mma_bf16_16816(zm[1], qa[ks], ma[ks][1], ma[ks][3]);
+                }
+            }
+            // E^T = P^T - V^T: e[h][0..3] = (c = g, j), (g, j + 1), (g + 8, j), (g + 8, j + 1), j = 8 h + 2t
+            float e[2][4];
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
-                zp[h][0] = fmaf(-cg0, zm[h][0], za[h][0]);
-                zp[h][1] = fmaf(-cg0, zm[h][1], za[h][1]);
-                zp[h][2] = fmaf(-cg8, zm[h][2], za[h][2]);
-                zp[h][3] = fmaf(-cg8, zm[h][3], za[h][3]);
+                e[h][0] = (pa[0][h][0] + pa[1][h][0]) - bf16_lo(vv[2 * h]);
+                e[h][1] = (pa[0][h][1] + pa[1][h][1]) - bf16_hi(vv[2 * h]);
+                e[h][2] = (pa[0][h][2] + pa[1][h][2]) - bf16_lo(vv[2 * h + 1]);
+                e[h][3] = (pa[0][h][3] + pa[1][h][3]) - bf16_hi(vv[2 * h + 1]);
             }
-            mma_bf16_16816(zp[0], ac, ea[0], ea[2]);
-            mma_bf16_16816(zp[1], ac, ea[1], ea[3]);
-            __nv_bfloat16* zr = zb + size_t(16 * nb + g) * D;  // rows 16 nb + g (+8), columns cw0 + 2t (+8)
-            *reinterpret_cast<uint32_t*>(zr) = pack_bf16(zp[0][0], zp[0][1]);
-            *reinterpret_cast<uint32_t*>(zr + 8 * D) = pack_bf16(zp[0][2], zp[0][3]);
-            *reinterpret_cast<uint32_t*>(zr + 8) = pack_bf16(zp[1][0], zp[1][1]);
-            *reinterpret_cast<uint32_t*>(zr + 8 * D + 8) = pack_bf16(zp[1][2], zp[1][3]);
-        }
-
-        // ---- W^T <- W^T - c_15 M^T - E^T diag(Bs) K;  M^T <- beta^16 M^T + E^T diag(beta^(15-j)) K
-        {
-            float pj[4];
+            // read-out Z = Q W - diag(c) Q M - (Gamma . tril(S)) E
+            {
+                const uint4 a4 = *reinterpret_cast<const uint4*>(smem + OFF_AC + i * 512 + lane * 16);
+                const uint32_t ac[4] = {a4.x, a4.y, a4.z, a4.w};
+                const uint32_t ea[4] = {pack_bf16(e[0][0], e[0][1]), pack_bf16(e[0][2], e[0][3]),
+                                        pack_bf16(e[1][0], e[1][1]), pack_bf16(e[1][2], e[1][3])};
+                const float cg0 = tw[g], cg8 = tw[g + 8];
+                float zp[2][4];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) pj[q] = wts[33 + 15 - jc[q]];
-            const uint32_t gw[4] = {pack_bf16(-bsj[0] * e[0][0], -bsj[1] * e[0][1]),
-                                    pack_bf16(-bsj[0] * e[0][2], -bsj[1] * e[0][3]),
-                                    pack_bf16(-bsj[2] * e[1][0], -bsj[3] * e[1][1]),
-                                    pack_bf16(-bsj[2] * e[1][2], -bsj[3] * e[1][3])};
-            const uint32_t gm[4] = {pack_bf16(pj[0] * e[0][0], pj[1] * e[0][1]),
-                                    pack_bf16(pj[0] * e[0][2], pj[1] * e[0][3]),
-                                    pack_bf16(pj[2] * e[1][0], pj[3] * e[1][1]),
-                                    pack_bf16(pj[2] * e[1][2], pj[3] * e[1][3])};
-            const float c15 = wts[15], b16 = wts[49];
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                for (int r = 0; r < 4; ++r) {
-                    w[nt][r] = fmaf(-c15, m[nt][r], w[nt][r]);
-                    m[nt][r] *= b16;
+                for (int h = 0; h < 2; ++h) {
+                    zp[h][0] = fmaf(-cg0, zm[h][0], za[h][0]);
+                    zp[h][1] = fmaf(-cg0, zm[h][1], za[h][1]);
+                    zp[h][2] = fmaf(-cg8, zm[h][2], za[h][2]);
+                    zp[h][3] = fmaf(-cg8, zm[h][3], za[h][3]);
                 }
-#pragma unroll
-            for (int kk = 0; kk < KS; ++kk) {
-                mma_bf16_16816(w[2 * kk], gw, kt[kk][0], kt[kk][1]);
-                mma_bf16_16816(w[2 * kk + 1], gw, kt[kk][2], kt[kk][3]);
-                mma_bf16_16816(m[2 * kk], gm, kt[kk][0], kt[kk][1]);
-                mma_bf16_16816(m[2 * kk + 1], gm, kt[kk][2], kt[kk][3]);
+                mma_bf16_16816(zp[0], ac, ea[0], ea[2]);
+                mma_bf16_16816(zp[1], ac, ea[1], ea[3]);
+                __nv_bfloat16* zr = zb + size_t(16 * (si * SPS + i) + g) * D;  // rows g (+8), columns cw0 + 2t (+8)
+                *reinterpret_cast<uint32_t*>(zr) = pack_bf16(zp[0][0], zp[0][1]);
+                *reinterpret_cast<uint32_t*>(zr + 8 * D) = pack_bf16(zp[0][2], zp[0][3]);
+                *reinterpret_cast<uint32_t*>(zr + 8) = pack_bf16(zp[1][0], zp[1][1]);
+                *reinterpret_cast<uint32_t*>(zr + 8 * D + 8) = pack_bf16(zp[1][2], zp[1][3]);
             }
+            // W^T <- W^T - c_15 M^T - E^T diag(Bs) K;  M^T <- beta^16 M^T + E^T diag(beta^(15-j)) K
+            {
+                float bsj[4], pj[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    bsj[q] = tw[16 + jc[q]];
+                    pj[q] = tw[33 + 15 - jc[q]];
+                }
+                const uint32_t gw[4] = {pack_bf16(-bsj[0] * e[0][0], -bsj[1] * e[0][1]),
+                                        pack_bf16(-bsj[0] * e[0][2], -bsj[1] * e[0][3]),
+                                        pack_bf16(-bsj[2] * e[1][0], -bsj[3] * e[1][1]),
+                                        pack_bf16(-bsj[2] * e[1][2], -bsj[3] * e[1][3])};
+                const uint32_t gm[4] = {pack_bf16(pj[0] * e[0][0], pj[1] * e[0][1]),
+                                        pack_bf16(pj[0] * e[0][2], pj[1] * e[0][3]),
+                                        pack_bf16(pj[2] * e[1][0], pj[3] * e[1][1]),
+                                        pack_bf16(pj[2] * e[1][2], pj[3] * e[1][3])};
+                const float c15 = tw[15], b16 = tw[49];
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) {
+                        w[nt][r] = fmaf(-c15, m[nt][r], w[nt][r]);
+                        m[nt][r] *= b16;
+                    }
+#pragma unroll
+                for (int kk = 0; kk < KS; ++kk) {
+                    mma_bf16_16816(w[2 * kk], gw, kt[kk][0], kt[kk][1]);
+                    mma_bf16_16816(w[2 * kk + 1], gw, kt[kk][2], kt[kk][3]);
+                    mma_bf16_16816(m[2 * kk], gm, kt[kk][0], kt[kk][1]);
+                    mma_bf16_16816(m[2 * kk + 1], gm, kt[kk][2], kt[kk][3]);
+                }
+            }
+        };
+        if (n == SPS) {
+#pragma unroll
+            for (int i = 0; i < SPS; ++i) chunk(i);
+        } else {
+            for (int i = 0; i < n; ++i) chunk(i);
         }
-        __syncwarp();     // the chunk weights are read before the next chunk rewrites them
-        __syncthreads();  // every warp is done with this buffer before it is refilled
     }
     cp_async_wait0();
     float* Wo = W_out + bh * D * D;
@@ -287,8 +317,9 @@ linear_momentum_mma_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloa
 template <int CG>
 cudaError_t launch_cg(const LinearArgs& a, cudaStream_t s) {
     auto kern = linear_momentum_mma_kernel<CG>;
-    const int bytes = 2 * BUF + CG * 64 * 4;
-    kern<<<dim3(unsigned(a.B) * unsigned(a.H), 4 / CG), 32 * CG, bytes, s>>>(
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    kern<<<dim3(unsigned(a.B) * unsigned(a.H), 4 / CG), 32 * CG, SMEM_BYTES, s>>>(
         static_cast<const __nv_bfloat16*>(a.Q), static_cast<const __nv_bfloat16*>(a.K),
         static_cast<const __nv_bfloat16*>(a.V), a.eta, a.W0, a.M0, static_cast<__nv_bfloat16*>(a.Z), a.W_out,
         a.M_out, a.T, a.beta);
