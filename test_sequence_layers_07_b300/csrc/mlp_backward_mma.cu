@@ -413,12 +413,18 @@ mlp_backward_mma_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16
         }
         float sa_g = 0.f, sa_g8 = 0.f;  // deta partials of this thread's rows: sum (K dW1') . E1 + (Hk dW2') . E2
         {
-            // E1 = Gk . g'(Zk); P1 = K dW1' (over d); dE1 = -D P1
+            // E1 = Gk . g'(Zk); from here on Zk holds g'(Zk) and Gk holds Gk . g''(Zk), all that the
+            // later steps need of them.  P1 = K dW1' (over d); dE1 = -D P1
             float e1[4][4];
 #pragma unroll
             for (int j = 0; j < 4; ++j)
 #pragma unroll
-                for (int e = 0; e < 4; ++e) e1[j][e] = Gk[j][e] * gelu3(Zk[j][e]).gp;
+                for (int e = 0; e < 4; ++e) {
+                    const Gelu r = gelu3(Zk[j][e]);
+                    e1[j][e] = Gk[j][e] * r.gp;
+                    Zk[j][e] = r.gp;
+                    Gk[j][e] *= r.gpp;
+                }
             pack_slice(e1, E1A);
             uint32_t aK[4][4];
 #pragma unroll
@@ -805,16 +811,14 @@ mlp_backward_mma_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16
                 mma_bf16_16816_z(k4, aT, b0, b1);
                 *reinterpret_cast<float4*>(dkt + (w * 32 + lane) * 4) = make_float4(k4[0], k4[1], k4[2], k4[3]);
             }
-            // dGk = dE1 . g'(Zk) (packed), dZk = dE1 . Gk . g''(Zk) (into Gk); g'(Zk) kept in Zk
+            // dGk = dE1 . g'(Zk) (packed), dZk = dE1 . Gk . g''(Zk) (into Gk)
             float dgk[4][4];
 #pragma unroll
             for (int j = 0; j < 4; ++j)
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    const Gelu r = gelu3(Zk[j][e]);
-                    dgk[j][e] = dE1[j][e] * r.gp;
-                    Gk[j][e] = dE1[j][e] * Gk[j][e] * r.gpp;
-                    Zk[j][e] = r.gp;
+                    dgk[j][e] = dE1[j][e] * Zk[j][e];
+                    Gk[j][e] *= dE1[j][e];
                 }
             pack_slice(dgk, dGkA);
         }

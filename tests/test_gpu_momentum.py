@@ -130,3 +130,17 @@ def test_momentum_mma_and_simt_kernels_agree(monkeypatch):
     torch.cuda.synchronize()
     for u, v in zip(a, b):
         assert rel_err(u, v.double().cpu().numpy()) <= TOL["bf16"]
+
+
+@pytest.mark.parametrize("B,H", [(4, 12), (4, 75)])  # two column groups per CTA; four, more CTAs than SMs
+def test_momentum_mma_column_group_layouts(B, H):
+    x = WL.linear_inputs(B, H, 96, 64, seed=3800 + H, dtype="bf16")
+    M0 = _m0(x, 3801 + H)
+    g = cuda(x)
+    Z, W, M = T.linear_momentum_prefill(g["Q"], g["K"], g["V"], g["eta"], g["W0"], M0.cuda(), 16, 0.8)
+    torch.cuda.synchronize()
+    r = f64(x)
+    Zr, Wr, Mr = O.linear_momentum_dual(r["Q"], r["K"], r["V"], r["eta"], r["W0"], WL.to_f64(M0), 0.8, 16)
+    assert rel_err(Z, Zr) <= TOL["bf16"]
+    assert rel_err(W, Wr) <= TOL["bf16"]
+    assert rel_err(M, Mr) <= TOL["bf16"]
