@@ -43,6 +43,7 @@
 //    TTT_ERR_TIMEOUT, every warp leaves its loop, and the producer drains its copies (with the
 //    4 s bound, whatever `wait_ns` is) before the CTA exits.
 #include <cuda.h>
+#include <string.h>
 
 #include "ptx.cuh"
 #include "ttt_common.cuh"
@@ -94,7 +95,7 @@ __global__ void __launch_bounds__(FusedCfg<D, CG, NST, SPS>::THREADS, 1)
 linear_prefill_fused_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                             const __grid_constant__ CUtensorMap tmV, const float* __restrict__ eta,
                             const float* W0, __nv_bfloat16* __restrict__ Z, float* W_out, int T, int chunk,
-                            int* status, __nv_bfloat16* __restrict__ W_hist, uint64_t wait_ns) {
+                            int* status, const __grid_constant__ CUtensorMap tmH, uint64_t wait_ns) {
     using C = FusedCfg<D, CG, NST, SPS>;
     constexpr int KS = C::KS, NT = C::NT;
 
@@ -286,22 +287,23 @@ linear_prefill_fused_kernel(const __grid_constant__ CUtensorMap tmQ, const __gri
                     pack_state<KS>(w, wa0);
                     if constexpr (HIST) {
                         // the bf16 state at the start of block sb / nsub: the A fragments of W^T
-                        // stored transposed (stmatrix) into this warp's [D][16] slice, then 16-byte
-                        // rows halves to W_hist[d_in][cw0 ..]
+                        // stored transposed (stmatrix) into this warp's [D][16] slice, which one
+                        // TMA store writes to W_hist[block][d_in][cw0 ..]; the warp moves on at once
+                        // (a plain store would hold its source registers until the memory system
+                        // takes them, stalling the chain)
                         const uint32_t hs = sbase + C::HS_OFF + cg * D * 32;
+                        if (lane == 0) bulk_wait_read_all();  // the previous block's store has read the slice
+                        __syncwarp();
 #pragma unroll
                         for (int ks = 0; ks < KS; ++ks)
                             stsm_x4_trans(hs + (16 * ks + 8 * (lj >> 1) + lr) * 32 + (lj & 1) * 16, wa0[ks][0],
                                           wa0[ks][1], wa0[ks][2], wa0[ks][3]);
+                        fence_proxy_async_smem();
                         __syncwarp();
-                        __nv_bfloat16* wh = W_hist + (bh * size_t(nsb / nsub) + sb / nsub) * D * D + cw0;
-#pragma unroll
-                        for (int u = 0; u < D / 16; ++u) {
-                            const int q = lane + 32 * u;  // chunk: row q >> 1, half q & 1
-                            const uint4 v = *reinterpret_cast<const uint4*>(smem + C::HS_OFF + cg * D * 32 + q * 16);
-                            *reinterpret_cast<uint4*>(wh + size_t(q >> 1) * D + 8 * (q & 1)) = v;
+                        if (lane == 0) {
+                            tma_store_2d(&tmH, cw0, int((bh * size_t(nsb / nsub) + sb / nsub) * D), hs);
+                            bulk_commit();
                         }
-                        __syncwarp();
                     }
                 }
                 if constexpr (!SINGLE) {
@@ -379,6 +381,9 @@ linear_prefill_fused_kernel(const __grid_constant__ CUtensorMap tmQ, const __gri
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&empty_bar[s]));  // this warp's reads of the stage are done
         }
+        if constexpr (HIST) {
+            if (lane == 0) bulk_wait_all();  // the state stores are complete before the CTA retires
+        }
         float* Wo = W_out + bh * D * D;
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
@@ -398,18 +403,20 @@ template <int D, int CG, int NST, int SPS, bool SINGLE, bool HIST>
 cudaError_t launch_cfg(const LinearArgs& a, cudaStream_t s, int* status) {
     using C = FusedCfg<D, CG, NST, SPS>;
     const uint64_t rows = uint64_t(a.B) * a.H * a.T;
-    CUtensorMap mq, mk, mv;
+    CUtensorMap mq, mk, mv, mh;
     cudaError_t e;
     if ((e = make_tma_map_bf16(&mq, a.Q, rows, D)) != cudaSuccess) return e;
     if ((e = make_tma_map_bf16(&mk, a.K, rows, D)) != cudaSuccess) return e;
     if ((e = make_tma_map_bf16(&mv, a.V, rows, D)) != cudaSuccess) return e;
+    memset(&mh, 0, sizeof(mh));  // unused without the recorded states
+    if (HIST && (e = make_tma_map_bf16_slice(&mh, a.W_hist, uint64_t(a.B) * a.H * (a.T / 16) * D, D)) != cudaSuccess)
+        return e;
     auto kern = linear_prefill_fused_kernel<D, CG, NST, SPS, SINGLE, HIST>;
     const int bytes = C::BYTES + 1024;  // + alignment slack
     if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) != cudaSuccess) return e;
     dim3 grid(unsigned(a.B) * unsigned(a.H), D / 16 / CG);
     kern<<<grid, C::THREADS, bytes, s>>>(mq, mk, mv, a.eta, a.W0, static_cast<__nv_bfloat16*>(a.Z), a.W_out, a.T,
-                                         a.chunk, status, static_cast<__nv_bfloat16*>(a.W_hist),
-                                         a.wait_ns ? a.wait_ns : kWaitLimitNs);
+                                         a.chunk, status, mh, a.wait_ns ? a.wait_ns : kWaitLimitNs);
     return cudaGetLastError();
 }
 

@@ -82,6 +82,14 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
 
 // Contiguous bulk store shared -> global (size and both addresses multiples of 16 bytes),
 // tracked by the issuing thread's bulk async-group.
+// TMA store of one 2D box from shared memory (completion tracked by the bulk group of the issuing thread);
+// x times the element size must be a multiple of 16 bytes and neither coordinate may be negative
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, int x, int y, uint32_t src) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(map), "r"(x),
+                 "r"(y), "r"(src)
+                 : "memory");
+}
+
 __device__ __forceinline__ void bulk_store(void* dst, uint32_t src, uint32_t bytes) {
     asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src), "r"(bytes)
                  : "memory");

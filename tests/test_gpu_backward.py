@@ -149,3 +149,19 @@ def test_backward_deterministic():
     b = _run(x, g, 16)[3]
     for u, v in zip(a, b):
         assert torch.equal(u, v)
+
+
+def test_recorded_states_headline_all_heads():
+    # B=8 H=12 d=64 T=2048 b=16 bf16: the recording forward (one-pass kernel, four column groups per CTA,
+    # states written by TMA stores) against the oracle's state after n blocks, every head
+    w = WL.WORKLOADS["linear_prefill"]
+    x = WL.workload_inputs(w)
+    xc = cuda(x)
+    Z, W, Wh = T.linear_prefill_hist(xc["Q"], xc["K"], xc["V"], xc["eta"], xc["W0"], w.chunk)
+    torch.cuda.synchronize()
+    assert torch.equal(Wh[:, :, 0], xc["W0"].to(torch.bfloat16))
+    r = f64(x)
+    for n in (1, 37, 127):
+        cut = {k: (v[:, :, :16 * n] if k != "W0" else v) for k, v in r.items()}
+        _, Wn = O.linear_dual(cut["Q"], cut["K"], cut["V"], cut["eta"], cut["W0"], 16)
+        assert rel_err(Wh[:, :, n], Wn) <= TOL["bf16"], n
