@@ -40,15 +40,16 @@ cudaError_t make_tma_map_bf16(CUtensorMap* m, const void* base, uint64_t rows, i
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-// [rows][D] bf16 viewed as a 2D tensor; box = 64 rows x 16 columns (32-byte rows), no swizzle: the
-// [64][16] slice a column-group warp stages for a TMA store.
-cudaError_t make_tma_map_bf16_slice(CUtensorMap* m, const void* base, uint64_t rows, int D) {
+// [rows][D] bf16 viewed as a 2D tensor; box = box_rows x box_cols, row-major in shared memory with no
+// swizzle: a slice a warp stages for a TMA store (box_cols * 2 bytes a multiple of 16).
+cudaError_t make_tma_map_bf16_box(CUtensorMap* m, const void* base, uint64_t rows, int D, int box_cols,
+                                  int box_rows) {
     EncodeTiledFn enc;
     cudaError_t e = get_encoder(&enc);
     if (e != cudaSuccess) return e;
     cuuint64_t dims[2] = {cuuint64_t(D), cuuint64_t(rows)};
     cuuint64_t strides[1] = {cuuint64_t(D) * 2};
-    cuuint32_t box[2] = {16, 64};
+    cuuint32_t box[2] = {cuuint32_t(box_cols), cuuint32_t(box_rows)};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
