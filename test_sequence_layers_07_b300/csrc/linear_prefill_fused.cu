@@ -410,7 +410,7 @@ cudaError_t launch_cfg(const LinearArgs& a, cudaStream_t s, int* status) {
     if ((e = make_tma_map_bf16(&mv, a.V, rows, D)) != cudaSuccess) return e;
     memset(&mh, 0, sizeof(mh));  // unused without the recorded states
     if (HIST &&
-        (e = make_tma_map_bf16_box(&mh, a.W_hist, uint64_t(a.B) * a.H * (a.T / 16) * D, D, 16, 64)) != cudaSuccess)
+        (e = make_tma_map_bf16_box(&mh, a.W_hist, uint64_t(a.B) * a.H * (a.T / 16) * D, D, 16, 64, 0)) != cudaSuccess)
         return e;
     auto kern = linear_prefill_fused_kernel<D, CG, NST, SPS, SINGLE, HIST>;
     const int bytes = C::BYTES + 1024;  // + alignment slack

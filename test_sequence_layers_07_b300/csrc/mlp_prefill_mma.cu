@@ -39,6 +39,7 @@
 //    the per-thread error flag), so after an expired wait they all leave the loop at the same
 //    barrier; thread 0 drains the copies in flight before the CTA exits.
 #include <cuda.h>
+#include <string.h>
 
 #include "ptx.cuh"
 #include "ttt_common.cuh"
@@ -68,7 +69,16 @@ constexpr int OFF_E2T = OFF_SP + NCW * 1024;     // E2^T bf16 [64][16]
 constexpr int OFF_NE2T = OFF_E2T + 2048;         // (-eta E2)^T bf16 [2 blocks][64][16]
 constexpr int OFF_S2 = OFF_NE2T + 2 * 2048;      // tril(Hq Hk^T) bf16 [16][16]
 constexpr int SMEM_BYTES = OFF_S2 + 512;
-static_assert(SMEM_BYTES + 1024 <= 232448, "shared memory");
+// the recording variant: per warp a [64 d][32 hidden] bf16 staging slice of W1 (64-byte rows, 64-byte
+// swizzle), written out by a TMA store; W2 goes out straight from its bf16 copy
+constexpr int OFF_H1S = (SMEM_BYTES + 1023) / 1024 * 1024;
+constexpr int SMEM_BYTES_HIST = OFF_H1S + NCW * 4096;
+static_assert(SMEM_BYTES_HIST + 1024 <= 232448, "shared memory");
+// byte offset of (row, col) in a [rows][32] bf16 block with 64-byte rows and the 64-byte swizzle (16-byte
+// chunk index XOR (row / 2) % 4, the pattern a TMA store with that mode reads); col % 8 == 0
+__device__ __forceinline__ uint32_t sw64(int row, int col) {
+    return uint32_t(row * 64 + ((((col >> 3) ^ (row >> 1)) & 3) << 4));
+}
 
 // byte offset of (row, col) in a [rows][64] bf16 block with 128-byte rows, 16-byte chunk index
 // XOR row % 8 (the layout a TMA box with the 128-byte swizzle writes); col % 8 == 0
@@ -133,7 +143,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 mlp_prefill_mma_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const float* __restrict__ eta, const float* W1_0,
                        const float* W2_0, __nv_bfloat16* __restrict__ Z, float* W1_out, float* W2_out, int T,
-                       __nv_bfloat16* __restrict__ W1_hist, __nv_bfloat16* __restrict__ W2_hist,
+                       const __grid_constant__ CUtensorMap tmH1, const __grid_constant__ CUtensorMap tmH2,
                        int* status) {
     extern __shared__ uint8_t smem_dyn[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
@@ -232,6 +242,7 @@ mlp_prefill_mma_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_con
                                   pack_bf16(w2[2 * mp + 1][nh][2], w2[2 * mp + 1][nh][3]));
         };
         store_w2c();
+        if constexpr (HIST) fence_proxy_async_smem();  // the first block's TMA store reads the copy
         __syncwarp();
 
         const bool m0 = 2 * t <= g, m1 = 2 * t + 1 <= g;  // causal mask of the score fragment
@@ -253,25 +264,29 @@ mlp_prefill_mma_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_con
                 if (!err && !wait(full_bar[s], par)) err = true;
                 if constexpr (HIST) {
                     // the state at the start of block n (this warp's hidden slice), rounded to bf16: the
-                    // operand the block's products use and what the backward reads
-                    __nv_bfloat16* h1 = W1_hist + (bh * size_t(nblk) + n) * D * HID;
-                    __nv_bfloat16* h2 = W2_hist + (bh * size_t(nblk) + n) * HID * D;
+                    // operand the block's products use and what the backward reads.  W1^T is staged
+                    // transposed into [d][32 hidden] (stmatrix.trans), W2 is already in its bf16 copy
+                    // (rows [hidden][d], 128-byte swizzle); one TMA store each, and the warp moves on
+                    // (scalar stores would hold their source registers on the chain)
+                    const uint32_t s1 = sb + OFF_H1S + warp * 4096;
+                    if (lane == 0) bulk_wait_read_all();  // the previous block's stores have read the staging
+                    __syncwarp();
 #pragma unroll
                     for (int mh = 0; mh < 2; ++mh)
 #pragma unroll
-                        for (int nd = 0; nd < 8; ++nd)
-#pragma unroll
-                            for (int k = 0; k < 4; ++k)
-                                h1[size_t(8 * nd + 2 * t + (k & 1)) * HID + h0 + 16 * mh + g + 8 * (k >> 1)] =
-                                    __float2bfloat16_rn(w1[mh][nd][k]);
-#pragma unroll
-                    for (int mo = 0; mo < 4; ++mo)
-#pragma unroll
-                        for (int nh = 0; nh < 4; ++nh)
-#pragma unroll
-                            for (int k = 0; k < 4; ++k)
-                                h2[size_t(h0 + 8 * nh + 2 * t + (k & 1)) * D + 16 * mo + g + 8 * (k >> 1)] =
-                                    __float2bfloat16_rn(w2[mo][nh][k]);
+                        for (int nd = 0; nd < 8; nd += 2)
+                            stsm_x4_trans(s1 + sw64(8 * nd + 8 * (lm >> 1) + lr, 16 * mh + 8 * (lm & 1)),
+                                          pack_bf16(w1[mh][nd][0], w1[mh][nd][1]),
+                                          pack_bf16(w1[mh][nd][2], w1[mh][nd][3]),
+                                          pack_bf16(w1[mh][nd + 1][0], w1[mh][nd + 1][1]),
+                                          pack_bf16(w1[mh][nd + 1][2], w1[mh][nd + 1][3]));
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&tmH1, h0, int((bh * size_t(nblk) + n) * D), s1);
+                        tma_store_2d(&tmH2, 0, int((bh * size_t(nblk) + n) * HID + h0), sb + OFF_W2C + h0 * 128);
+                        bulk_commit();
+                    }
                 }
                 // ---- Zk = K W1 and Zq = Q W1 (start-of-block W1)
                 float zk[4][4], sc[2][4] = {};
@@ -478,8 +493,16 @@ mlp_prefill_mma_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_con
                 }
             }
             __syncwarp();
+            if constexpr (HIST) {  // the block's W2 store has read the bf16 copy before it is rewritten
+                if (lane == 0) bulk_wait_read_all();
+                __syncwarp();
+            }
             store_w2c();
+            if constexpr (HIST) fence_proxy_async_smem();  // the next block's TMA store reads the copy
             __syncwarp();
+        }
+        if constexpr (HIST) {
+            if (lane == 0) bulk_wait_all();  // the state stores are complete before the CTA retires
         }
 
         // final state (fp32)
@@ -517,21 +540,29 @@ bool mlp_prefill_mma_supported(const MlpArgs& a) {
 cudaError_t launch_mlp_prefill_mma(const MlpArgs& a, cudaStream_t s, int* status) {
     if (!mlp_prefill_mma_supported(a)) return cudaErrorNotSupported;
     const uint64_t rows = uint64_t(a.B) * a.H * a.T;
-    CUtensorMap mq, mk, mv;
+    CUtensorMap mq, mk, mv, h1, h2;
     cudaError_t e;
     if ((e = make_tma_map_bf16(&mq, a.Q, rows, D)) != cudaSuccess) return e;
     if ((e = make_tma_map_bf16(&mk, a.K, rows, D)) != cudaSuccess) return e;
     if ((e = make_tma_map_bf16(&mv, a.V, rows, D)) != cudaSuccess) return e;
-    const int bytes = SMEM_BYTES + 1024;  // + alignment slack
-    auto run = [&](auto kern) -> cudaError_t {
+    memset(&h1, 0, sizeof(h1));  // unused without the recorded states
+    memset(&h2, 0, sizeof(h2));
+    if (a.W1_hist) {  // W1_hist as [blocks * d][hidden], W2_hist as [blocks * hidden][d]
+        const uint64_t blocks = uint64_t(a.B) * a.H * (a.T / BT);
+        if ((e = make_tma_map_bf16_box(&h1, a.W1_hist, blocks * D, HID, HS, D, 64)) != cudaSuccess) return e;
+        if ((e = make_tma_map_bf16_box(&h2, a.W2_hist, blocks * HID, D, D, HS, 128)) != cudaSuccess) return e;
+    }
+    auto run = [&](auto kern, int bytes) -> cudaError_t {
         cudaError_t e2 = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
         if (e2 != cudaSuccess) return e2;
-        kern<<<unsigned(a.B) * unsigned(a.H), THREADS, bytes, s>>>(
-            mq, mk, mv, a.eta, a.W1_0, a.W2_0, static_cast<__nv_bfloat16*>(a.Z), a.W1_out, a.W2_out, a.T,
-            static_cast<__nv_bfloat16*>(a.W1_hist), static_cast<__nv_bfloat16*>(a.W2_hist), status);
+        kern<<<unsigned(a.B) * unsigned(a.H), THREADS, bytes, s>>>(mq, mk, mv, a.eta, a.W1_0, a.W2_0,
+                                                                  static_cast<__nv_bfloat16*>(a.Z), a.W1_out,
+                                                                  a.W2_out, a.T, h1, h2, status);
         return cudaGetLastError();
     };
-    return a.W1_hist ? run(mlp_prefill_mma_kernel<true>) : run(mlp_prefill_mma_kernel<false>);
+    // + 1024 bytes of alignment slack
+    return a.W1_hist ? run(mlp_prefill_mma_kernel<true>, SMEM_BYTES_HIST + 1024)
+                     : run(mlp_prefill_mma_kernel<false>, SMEM_BYTES + 1024);
 }
 
 }  // namespace ttt

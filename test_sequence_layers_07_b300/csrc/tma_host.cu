@@ -40,10 +40,12 @@ cudaError_t make_tma_map_bf16(CUtensorMap* m, const void* base, uint64_t rows, i
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-// [rows][D] bf16 viewed as a 2D tensor; box = box_rows x box_cols, row-major in shared memory with no
-// swizzle: a slice a warp stages for a TMA store (box_cols * 2 bytes a multiple of 16).
+// [rows][D] bf16 viewed as a 2D tensor; box = box_rows x box_cols: a slice a warp stages for a TMA store
+// (box_cols * 2 bytes a multiple of 16).  swizzle_bytes: 0 (row-major in shared memory), 64 or 128 (the
+// 16-byte chunks of each box row XOR bits 7.. of the shared-memory offset, as the tensor core's swizzle
+// modes define; the box row is then at most that many bytes).
 cudaError_t make_tma_map_bf16_box(CUtensorMap* m, const void* base, uint64_t rows, int D, int box_cols,
-                                  int box_rows) {
+                                  int box_rows, int swizzle_bytes) {
     EncodeTiledFn enc;
     cudaError_t e = get_encoder(&enc);
     if (e != cudaSuccess) return e;
@@ -51,8 +53,11 @@ cudaError_t make_tma_map_bf16_box(CUtensorMap* m, const void* base, uint64_t row
     cuuint64_t strides[1] = {cuuint64_t(D) * 2};
     cuuint32_t box[2] = {cuuint32_t(box_cols), cuuint32_t(box_rows)};
     cuuint32_t estr[2] = {1, 1};
+    const CUtensorMapSwizzle sw = swizzle_bytes == 128  ? CU_TENSOR_MAP_SWIZZLE_128B
+                                  : swizzle_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                                        : CU_TENSOR_MAP_SWIZZLE_NONE;
     CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_NONE,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }

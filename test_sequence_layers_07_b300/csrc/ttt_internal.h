@@ -172,9 +172,9 @@ cudaError_t make_tma_map_bf16(CUtensorMap* m, const void* base, uint64_t rows, i
 // TMA descriptor of a [rows][64] fp32 row-major tensor: boxes of 64 rows x 32 columns (128 bytes),
 // 128-byte swizzle (two boxes cover a 64 x 64 block).
 cudaError_t make_tma_map_f32x64(CUtensorMap* m, const void* base, uint64_t rows);
-// [rows][D] bf16, box box_rows x box_cols, no swizzle (a warp's staged output slice)
+// [rows][D] bf16, box box_rows x box_cols (a warp's staged output slice), swizzle 0, 64 or 128 bytes
 cudaError_t make_tma_map_bf16_box(CUtensorMap* m, const void* base, uint64_t rows, int D, int box_cols,
-                                  int box_rows);
+                                  int box_rows, int swizzle_bytes);
 
 // Device-side failure path: a bounded wait that nothing satisfies (see selftest.cu).
 cudaError_t launch_wait_timeout_selftest(unsigned long long limit_ns, cudaStream_t s, int* status);
