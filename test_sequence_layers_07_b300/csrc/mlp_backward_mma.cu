@@ -39,6 +39,9 @@
 //    refreshes its bf16 copy.
 //  * Token tiles are double buffered by cp.async one block ahead; the next block's state slices are
 //    prefetched to L2 a block ahead and copied in right after their last use.
+#include <stdlib.h>
+#include <string.h>
+
 #include "ptx.cuh"
 #include "ttt_common.cuh"
 #include "ttt_internal.h"
@@ -48,40 +51,56 @@ namespace {
 
 using namespace ptx;
 
-constexpr int D = 64, HID = 256, BT = 16, NW = 8, NTH = 32 * NW;
-constexpr int SZ_W1S = 64 * 32 * 2;  // a warp's [64][32] slice of W1 (or dW1'), bf16
-constexpr int SZ_W2S = 32 * 64 * 2;  // a warp's [32][64] slice of W2 (or dW2'), bf16
-constexpr int TILE = BT * D * 2;     // [16][64] bf16 token tile
+constexpr int D = 64, HID = 256, BT = 16;
+constexpr int TILE = BT * D * 2;       // [16][64] bf16 token tile
 constexpr int TOKBUF = 4 * TILE + 64;  // Q K V dZ, eta
 
-// shared memory (bytes)
-constexpr int OFF_W1 = 0;
-constexpr int OFF_W2 = OFF_W1 + NW * SZ_W1S;
-constexpr int OFF_G1 = OFF_W2 + NW * SZ_W2S;   // bf16 dW1' slices
-constexpr int OFF_G2 = OFF_G1 + NW * SZ_W1S;   // bf16 dW2' slices
-constexpr int OFF_TOK = OFF_G2 + NW * SZ_W2S;  // two token buffers
-constexpr int OFF_E2B = OFF_TOK + 2 * TOKBUF;  // E2, bf16 [16][64]
-constexpr int OFF_DE2B = OFF_E2B + TILE;       // dE2, bf16 [16][64]
-constexpr int OFF_PART = OFF_DE2B + TILE;      // per-warp 16 x 64 partials [8][8 n-tiles][32 lanes] float4
-constexpr int OFF_PSM = OFF_PART + NW * 4096;  // per-warp 16 x 16 partials [8][2][32] float4
-constexpr int OFF_E2F = OFF_PSM + NW * 1024;   // E2 fp32, fragment order [8][32] float4
-constexpr int OFF_DE2T = OFF_E2F + 4096;       // -(M . S2 D)^T dZ, fragment order
-constexpr int OFF_DQ = OFF_DE2T + 4096;        // dQ, fragment order
-constexpr int OFF_DKT = OFF_DQ + 4096;         // dS1^T Q, fragment order
-constexpr int OFF_S2 = OFF_DKT + 4096;         // S2 fp32 [16][16]
-constexpr int OFF_DA1 = OFF_S2 + 1024;         // dA1 fp32 [16][16]
-constexpr int OFF_DETA = OFF_DA1 + 1024;       // [8 warps][16] partials, then [16] score terms
-constexpr int SMEM_BYTES = OFF_DETA + (NW + 1) * 64;
-static_assert(SMEM_BYTES <= 232448, "shared memory");
+// NW warps, each owning HS = 256 / NW hidden units (NJ 8-wide n-tiles, NKH 16-wide k-steps of them).
+// The per-warp partials of a sum over the hidden dimension go through 8 slots: with 16 warps, warp
+// w + 8 hands its partial to warp w first (two-stage, fixed order).
+template <int NW_>
+struct BwdCfg {
+    static constexpr int NW = NW_, NTH = 32 * NW, HS = HID / NW, NJ = HS / 8, NKH = HS / 16;
+    static constexpr int SZ_W1S = 64 * HS * 2;  // a warp's [64][HS] slice of W1 (or dW1'), bf16
+    static constexpr int SZ_W2S = HS * 64 * 2;  // a warp's [HS][64] slice of W2 (or dW2'), bf16
+    // shared memory (bytes)
+    static constexpr int OFF_W1 = 0;
+    static constexpr int OFF_W2 = OFF_W1 + NW * SZ_W1S;
+    static constexpr int OFF_G1 = OFF_W2 + NW * SZ_W2S;   // bf16 dW1' slices
+    static constexpr int OFF_G2 = OFF_G1 + NW * SZ_W1S;   // bf16 dW2' slices
+    static constexpr int OFF_TOK = OFF_G2 + NW * SZ_W2S;  // two token buffers
+    static constexpr int OFF_E2B = OFF_TOK + 2 * TOKBUF;  // E2, bf16 [16][64]
+    static constexpr int OFF_DE2B = OFF_E2B + TILE;       // dE2, bf16 [16][64]
+    static constexpr int OFF_PART = OFF_DE2B + TILE;      // 16 x 64 partials [8][8 n-tiles][32 lanes] float4
+    static constexpr int OFF_PSM = OFF_PART + 8 * 4096;   // 16 x 16 partials [8][2][32] float4
+    static constexpr int OFF_E2F = OFF_PSM + 8 * 1024;    // E2 fp32, fragment order [8][32] float4
+    static constexpr int OFF_DE2T = OFF_E2F + 4096;       // -(M . S2 D)^T dZ, fragment order
+    static constexpr int OFF_DQ = OFF_DE2T + 4096;        // dQ, fragment order
+    static constexpr int OFF_DKT = OFF_DQ + 4096;         // dS1^T Q, fragment order
+    static constexpr int OFF_S2 = OFF_DKT + 4096;         // S2 fp32 [16][16]
+    static constexpr int OFF_DA1 = OFF_S2 + 1024;         // dA1 fp32 [16][16]
+    static constexpr int OFF_DETA = OFF_DA1 + 1024;       // [NW warps][16] partials, then [16] score terms
+    static constexpr int SMEM_BYTES = OFF_DETA + (NW + 1) * 64;
+    static_assert(SMEM_BYTES <= 232448, "shared memory");
+};
 
 // byte offset of (row, col) in a [rows][64] bf16 block (128-byte rows, 16-byte chunk XOR row % 8)
 __device__ __forceinline__ uint32_t t64(int row, int col) {
     return uint32_t(row * 128 + ((((col >> 3) ^ row) & 7) << 4) + (col & 7) * 2);
 }
-// byte offset of (row, col) in a [rows][32] bf16 block (64-byte rows, chunk XOR (row / 2) % 4): the
-// eight rows an ldmatrix reads at one chunk fall in distinct banks
+// byte offset of (row, col) in a [rows][32] bf16 block (64-byte rows, chunk XOR (row / 2) % 4) or a
+// [rows][16] one (32-byte rows, chunk XOR (row / 4) % 2): the eight rows an ldmatrix reads at one chunk
+// fall in distinct banks
 __device__ __forceinline__ uint32_t t32(int row, int col) {
     return uint32_t(row * 64 + ((((col >> 3) ^ (row >> 1)) & 3) << 4) + (col & 7) * 2);
+}
+__device__ __forceinline__ uint32_t t16(int row, int col) {
+    return uint32_t(row * 32 + ((((col >> 3) ^ (row >> 2)) & 1) << 4) + (col & 7) * 2);
+}
+// the layout of a warp's [64][HS] slice of W1 or dW1' (RB = 0: a [rows][64] block)
+template <int RB>
+__device__ __forceinline__ uint32_t tl(int row, int col) {
+    return RB == 32 ? t32(row, col) : RB == 16 ? t16(row, col) : t64(row, col);
 }
 
 __device__ __forceinline__ uint32_t movt(uint32_t x) {
@@ -132,16 +151,16 @@ __device__ __forceinline__ void lda_tok(uint32_t tile, int kk, int lane, uint32_
     ldsm_x4(tile + t64(r + 8 * (q & 1), 16 * kk + 8 * (q >> 1)), a);
 }
 // B of two n-tiles (n0, n0 + 8), k-step at k0, from [n][k] storage: b[0..1] for n0, b[2..3] for n0 + 8
-template <bool W32>
+template <int RB>
 __device__ __forceinline__ void ldb_nk(uint32_t base, int n0, int k0, int lane, uint32_t (&b)[4]) {
     const int q = lane >> 3, r = lane & 7, row = n0 + 8 * (q >> 1) + r, col = k0 + 8 * (q & 1);
-    ldsm_x4(base + (W32 ? t32(row, col) : t64(row, col)), b);
+    ldsm_x4(base + tl<RB>(row, col), b);
 }
 // the same from [k][n] storage (transposing load)
-template <bool W32>
+template <int RB>
 __device__ __forceinline__ void ldb_kn(uint32_t base, int n0, int k0, int lane, uint32_t (&b)[4]) {
     const int q = lane >> 3, r = lane & 7, row = k0 + 8 * (q & 1) + r, col = n0 + 8 * (q >> 1);
-    ldsm_x4_trans(base + (W32 ? t32(row, col) : t64(row, col)), b);
+    ldsm_x4_trans(base + tl<RB>(row, col), b);
 }
 // B of one n-tile n0 over the 16 tokens of a [16][64] token tile ([k][n] storage)
 __device__ __forceinline__ void ldb_tok1(uint32_t tile, int n0, int lane, uint32_t& b0, uint32_t& b1) {
@@ -154,11 +173,12 @@ __device__ __forceinline__ void lda_tokT(uint32_t tile, int m0, int lane, uint32
     ldsm_x4_trans(tile + t64(r + 8 * (q >> 1), m0 + 8 * (q & 1)), a);
 }
 
-// ---- register slices: X[4][4] is a 16 x 32 accumulator slice (n-tile j = columns 8 j ..)
+// ---- register slices: X[NJ][4] is a 16 x 8 NJ accumulator slice (n-tile j = columns 8 j ..)
 // packed A fragments over its columns, k-step kk = columns 16 kk ..
-__device__ __forceinline__ void pack_slice(const float (&x)[4][4], uint32_t (&xa)[2][4]) {
+template <int NJ>
+__device__ __forceinline__ void pack_slice(const float (&x)[NJ][4], uint32_t (&xa)[NJ / 2][4]) {
 #pragma unroll
-    for (int kk = 0; kk < 2; ++kk) {
+    for (int kk = 0; kk < NJ / 2; ++kk) {
         xa[kk][0] = pack_bf16(x[2 * kk][0], x[2 * kk][1]);
         xa[kk][1] = pack_bf16(x[2 * kk][2], x[2 * kk][3]);
         xa[kk][2] = pack_bf16(x[2 * kk + 1][0], x[2 * kk + 1][1]);
@@ -166,12 +186,14 @@ __device__ __forceinline__ void pack_slice(const float (&x)[4][4], uint32_t (&xa
     }
 }
 // the slice as the B operand over tokens (k = token, n = column tile j)
-__device__ __forceinline__ void btok(const uint32_t (&xa)[2][4], int j, uint32_t& b0, uint32_t& b1) {
+template <int NKH>
+__device__ __forceinline__ void btok(const uint32_t (&xa)[NKH][4], int j, uint32_t& b0, uint32_t& b1) {
     b0 = movt(xa[j >> 1][(j & 1) * 2]);
     b1 = movt(xa[j >> 1][(j & 1) * 2 + 1]);
 }
 // the transposed slice as an A operand: m-tile p = columns 16 p .., k = the 16 tokens
-__device__ __forceinline__ void atr(const uint32_t (&xa)[2][4], int p, uint32_t (&a)[4]) {
+template <int NKH>
+__device__ __forceinline__ void atr(const uint32_t (&xa)[NKH][4], int p, uint32_t (&a)[4]) {
     a[0] = movt(xa[p][0]);
     a[1] = movt(xa[p][2]);
     a[2] = movt(xa[p][1]);
@@ -182,13 +204,21 @@ __device__ __forceinline__ void scale_rows(float (&x)[4], float sg, float sg8) {
     x[0] *= sg, x[1] *= sg, x[2] *= sg8, x[3] *= sg8;
 }
 
-__global__ void __launch_bounds__(NTH, 1)
+template <int NW_>
+__global__ void __launch_bounds__(32 * NW_, 1)
 mlp_backward_mma_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restrict__ K,
                         const __nv_bfloat16* __restrict__ V, const float* __restrict__ eta,
                         const __nv_bfloat16* __restrict__ W1h, const __nv_bfloat16* __restrict__ W2h,
                         const __nv_bfloat16* __restrict__ dZ, const float* dW1_T, const float* dW2_T,
                         __nv_bfloat16* __restrict__ dQ, __nv_bfloat16* __restrict__ dK,
                         __nv_bfloat16* __restrict__ dV, float* __restrict__ deta, float* dW1g, float* dW2g, int T) {
+    using C = BwdCfg<NW_>;
+    constexpr int NW = C::NW, NTH = C::NTH, HS = C::HS, NJ = C::NJ, NKH = C::NKH;
+    constexpr int SZ_W1S = C::SZ_W1S, SZ_W2S = C::SZ_W2S, OFF_W1 = C::OFF_W1, OFF_W2 = C::OFF_W2;
+    constexpr int OFF_G1 = C::OFF_G1, OFF_G2 = C::OFF_G2, OFF_TOK = C::OFF_TOK, OFF_E2B = C::OFF_E2B;
+    constexpr int OFF_DE2B = C::OFF_DE2B, OFF_PART = C::OFF_PART, OFF_PSM = C::OFF_PSM, OFF_E2F = C::OFF_E2F;
+    constexpr int OFF_DE2T = C::OFF_DE2T, OFF_DQ = C::OFF_DQ, OFF_DKT = C::OFF_DKT, OFF_S2 = C::OFF_S2;
+    constexpr int OFF_DA1 = C::OFF_DA1, OFF_DETA = C::OFF_DETA;
     extern __shared__ __align__(128) uint8_t smem[];
     const uint32_t sb = smem_u32(smem);
     const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
@@ -207,16 +237,41 @@ mlp_backward_mma_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16
     float* dkt = reinterpret_cast<float*>(smem + OFF_DKT);
     float* s2s = reinterpret_cast<float*>(smem + OFF_S2);
     float* da1s = reinterpret_cast<float*>(smem + OFF_DA1);
-    float* detap = reinterpret_cast<float*>(smem + OFF_DETA);  // [8][16]
+    float* detap = reinterpret_cast<float*>(smem + OFF_DETA);  // [NW][16]
     float* detac = detap + NW * 16;                             // [16]
-    const int hw = 32 * w;  // first hidden unit of this warp
+    const int hw = HS * w;  // first hidden unit of this warp
+    // this warp's partial of a 16 x 64 (or 16 x 16) sum over the hidden dimension into its slot of
+    // `buf` (nt n-tiles x 32 lanes x float4); with 16 warps, warp w + 8 hands its partial to warp w,
+    // which adds its own (one more barrier).  The caller's barrier then covers the slots.
+    auto put_partial = [&](float* buf, const auto& P) {
+        constexpr int ntiles = sizeof(P) / sizeof(P[0]);
+        if (NW == 16 && w >= 8) {
+#pragma unroll
+            for (int nt = 0; nt < ntiles; ++nt)
+                *reinterpret_cast<float4*>(buf + (((w - 8) * ntiles + nt) * 32 + lane) * 4) =
+                    make_float4(P[nt][0], P[nt][1], P[nt][2], P[nt][3]);
+        }
+        if (NW == 16) __syncthreads();
+        if (w < 8) {
+#pragma unroll
+            for (int nt = 0; nt < ntiles; ++nt) {
+                float4* d = reinterpret_cast<float4*>(buf + ((w * ntiles + nt) * 32 + lane) * 4);
+                float4 v = make_float4(P[nt][0], P[nt][1], P[nt][2], P[nt][3]);
+                if (NW == 16) {
+                    const float4 o = *d;
+                    v.x += o.x, v.y += o.y, v.z += o.z, v.w += o.w;
+                }
+                *d = v;
+            }
+        }
+    };
 
     auto issue_tokens = [&](int m) {
         const uint32_t tb = sb + OFF_TOK + (m & 1) * TOKBUF;
         const size_t row0 = bh * size_t(T) + size_t(m) * BT;
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
-            const int c = tid + NTH * u, tile = c >> 7, row = (c >> 3) & 15, ch = c & 7;
+        for (int c = tid; c < 4 * 128; c += NTH) {
+            const int tile = c >> 7, row = (c >> 3) & 15, ch = c & 7;
             const __nv_bfloat16* src = tile == 0 ? Q : tile == 1 ? K : tile == 2 ? V : dZ;
             cp_async16(tb + tile * TILE + t64(row, 8 * ch), src + (row0 + row) * D + 8 * ch);
         }
@@ -226,10 +281,12 @@ mlp_backward_mma_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16
         const __nv_bfloat16* s1 = W1h + (bh * nblk + m) * NWT;
         const __nv_bfloat16* s2 = W2h + (bh * nblk + m) * NWT;
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            const int c = lane + 32 * u;
-            const int r1 = c >> 2, c1 = c & 3;
-            cp_async16(w1s + t32(r1, 8 * c1), s1 + size_t(r1) * HID + hw + 8 * c1);
+        for (int c = lane; c < 64 * (HS / 8); c += 32) {
+            const int r1 = c / (HS / 8), c1 = c % (HS / 8);
+            cp_async16(w1s + tl<HS>(r1, 8 * c1), s1 + size_t(r1) * HID + hw + 8 * c1);
+        }
+#pragma unroll
+        for (int c = lane; c < HS * 8; c += 32) {
             const int r2 = c >> 3, c2 = c & 7;
             cp_async16(w2s + t64(r2, 8 * c2), s2 + size_t(hw + r2) * D + 8 * c2);
         }
@@ -239,7 +296,7 @@ mlp_backward_mma_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16
         const __nv_bfloat16* s2 = W2h + (bh * nblk + m) * NWT;
         prefetch_l2(s1 + size_t(lane) * HID + hw);
         prefetch_l2(s1 + size_t(lane + 32) * HID + hw);
-        prefetch_l2(s2 + size_t(hw + lane) * D);
+        if (lane < HS) prefetch_l2(s2 + size_t(hw + lane) * D);
     };
 
     // ---- the running state gradient starts at dW_T (zero when absent); dW_T may be dW_0 itself
@@ -247,17 +304,17 @@ mlp_backward_mma_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16
 #pragma unroll
         for (int mt = 0; mt < 4; ++mt)
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
+            for (int j = 0; j < NJ; ++j)
 #pragma unroll
                 for (int h2 = 0; h2 < 2; ++h2) {
                     const int row = 16 * mt + g + 8 * h2, col = 8 * j + 2 * t;
                     const size_t at = size_t(row) * HID + hw + col;
                     float2 v = dW1_T ? *reinterpret_cast<const float2*>(dW1_T + bh * NWT + at) : make_float2(0.f, 0.f);
                     *reinterpret_cast<float2*>(dW1g + at) = v;
-                    *reinterpret_cast<uint32_t*>(smem + OFF_G1 + w * SZ_W1S + t32(row, col)) = pack_bf16(v.x, v.y);
+                    *reinterpret_cast<uint32_t*>(smem + OFF_G1 + w * SZ_W1S + tl<HS>(row, col)) = pack_bf16(v.x, v.y);
                 }
 #pragma unroll
-        for (int p = 0; p < 2; ++p)
+        for (int p = 0; p < NKH; ++p)
 #pragma unroll
             for (int nt = 0; nt < 8; ++nt)
 #pragma unroll
@@ -293,7 +350,7 @@ mlp_backward_mma_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16
         const size_t orow = bh * size_t(T) + size_t(n) * BT;
 
         // ================= F1: Zk = K W1, Zq = Q W1, S1 = Q K^T, E2 partial = Hk W2 (this warp's slice)
-        float Zk[4][4], Zq[4][4], S1[2][4];
+        float Zk[NJ][4], Zq[NJ][4], S1[2][4];
         {
             uint32_t aK[4][4], aQ[4][4];
 #pragma unroll
@@ -304,9 +361,9 @@ mlp_backward_mma_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
 #pragma unroll
-                for (int jp = 0; jp < 2; ++jp) {
+                for (int jp = 0; jp < NJ / 2; ++jp) {
                     uint32_t b[4];
-                    ldb_kn<true>(w1s, 16 * jp, 16 * kk, lane, b);
+                    ldb_kn<HS>(w1s, 16 * jp, 16 * kk, lane, b);
                     if (kk == 0) {
                         mma_bf16_16816_z(Zk[2 * jp], aK[kk], b[0], b[1]);
                         mma_bf16_16816_z(Zk[2 * jp + 1], aK[kk], b[2], b[3]);
@@ -322,7 +379,7 @@ mlp_backward_mma_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
                 uint32_t b[4];
-                ldb_nk<false>(Ks, 0, 16 * kk, lane, b);
+                ldb_nk<0>(Ks, 0, 16 * kk, lane, b);
                 if (kk == 0) {
                     mma_bf16_16816_z(S1[0], aQ[kk], b[0], b[1]);
                     mma_bf16_16816_z(S1[1], aQ[kk], b[2], b[3]);
@@ -332,11 +389,11 @@ mlp_backward_mma_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16
                 }
             }
         }
-        uint32_t HkA[2][4];
+        uint32_t HkA[NKH][4];
         {
-            float hk[4][4];
+            float hk[NJ][4];
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
+            for (int j = 0; j < NJ; ++j)
 #pragma unroll
                 for (int e = 0; e < 4; ++e) hk[j][e] = gelu3(Zk[j][e]).g;
             pack_slice(hk, HkA);
@@ -344,11 +401,11 @@ mlp_backward_mma_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16
         {
             float P[8][4];
 #pragma unroll
-            for (int kk = 0; kk < 2; ++kk)
+            for (int kk = 0; kk < NKH; ++kk)
 #pragma unroll
                 for (int p = 0; p < 4; ++p) {
                     uint32_t b[4];
-                    ldb_kn<false>(w2s, 16 * p, 16 * kk, lane, b);
+                    ldb_kn<0>(w2s, 16 * p, 16 * kk, lane, b);
                     if (kk == 0) {
                         mma_bf16_16816_z(P[2 * p], HkA[kk], b[0], b[1]);
                         mma_bf16_16816_z(P[2 * p + 1], HkA[kk], b[2], b[3]);
@@ -357,18 +414,15 @@ mlp_backward_mma_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16
                         mma_bf16_16816(P[2 * p + 1], HkA[kk], b[2], b[3]);
                     }
                 }
-#pragma unroll
-            for (int nt = 0; nt < 8; ++nt)
-                *reinterpret_cast<float4*>(part + ((w * 8 + nt) * 32 + lane) * 4) =
-                    make_float4(P[nt][0], P[nt][1], P[nt][2], P[nt][3]);
+            put_partial(part, P);
         }
         __syncthreads();
         // E2 = sum of the partials - V (thread: n-tile tid / 32, fragment position tid % 32)
-        {
+        if (tid < 256) {
             const int nt = tid >> 5, gl = (tid & 31) >> 2, tl = tid & 3, col = 8 * nt + 2 * tl;
             float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-            for (int ww = 0; ww < NW; ++ww) {
+            for (int ww = 0; ww < 8; ++ww) {
                 const float4 v = *reinterpret_cast<const float4*>(part + ((ww * 8 + nt) * 32 + (tid & 31)) * 4);
                 s.x += v.x, s.y += v.y, s.z += v.z, s.w += v.w;
             }
@@ -382,8 +436,8 @@ mlp_backward_mma_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16
         __syncthreads();
 
         // ================= F2
-        float Gk[4][4], dHk[4][4], dE1[4][4], dHq[4][4];
-        uint32_t E1A[2][4], HqA[2][4];
+        float Gk[NJ][4], dHk[NJ][4], dE1[NJ][4], dHq[NJ][4];
+        uint32_t E1A[NKH][4], HqA[NKH][4];
         {
             uint32_t aE[4][4];
 #pragma unroll
@@ -392,10 +446,10 @@ mlp_backward_mma_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
 #pragma unroll
-                for (int jp = 0; jp < 2; ++jp) {
+                for (int jp = 0; jp < NJ / 2; ++jp) {
                     uint32_t b[4], c[4];
-                    ldb_nk<false>(w2s, 16 * jp, 16 * kk, lane, b);
-                    ldb_nk<false>(g2s, 16 * jp, 16 * kk, lane, c);
+                    ldb_nk<0>(w2s, 16 * jp, 16 * kk, lane, b);
+                    ldb_nk<0>(g2s, 16 * jp, 16 * kk, lane, c);
                     if (kk == 0) {
                         mma_bf16_16816_z(Gk[2 * jp], aE[kk], b[0], b[1]);
                         mma_bf16_16816_z(Gk[2 * jp + 1], aE[kk], b[2], b[3]);
@@ -409,15 +463,15 @@ mlp_backward_mma_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16
                     }
                 }
 #pragma unroll
-            for (int j = 0; j < 4; ++j) scale_rows(dHk[j], -eg, -eg8);
+            for (int j = 0; j < NJ; ++j) scale_rows(dHk[j], -eg, -eg8);
         }
         float sa_g = 0.f, sa_g8 = 0.f;  // deta partials of this thread's rows: sum (K dW1') . E1 + (Hk dW2') . E2
         {
             // E1 = Gk . g'(Zk); from here on Zk holds g'(Zk) and Gk holds Gk . g''(Zk), all that the
             // later steps need of them.  P1 = K dW1' (over d); dE1 = -D P1
-            float e1[4][4];
+            float e1[NJ][4];
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
+            for (int j = 0; j < NJ; ++j)
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const Gelu r = gelu3(Zk[j][e]);
@@ -432,9 +486,9 @@ mlp_backward_mma_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
 #pragma unroll
-                for (int jp = 0; jp < 2; ++jp) {
+                for (int jp = 0; jp < NJ / 2; ++jp) {
                     uint32_t b[4];
-                    ldb_kn<true>(g1s, 16 * jp, 16 * kk, lane, b);
+                    ldb_kn<HS>(g1s, 16 * jp, 16 * kk, lane, b);
                     if (kk == 0) {
                         mma_bf16_16816_z(dE1[2 * jp], aK[kk], b[0], b[1]);
                         mma_bf16_16816_z(dE1[2 * jp + 1], aK[kk], b[2], b[3]);
@@ -444,7 +498,7 @@ mlp_backward_mma_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16
                     }
                 }
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
+            for (int j = 0; j < NJ; ++j) {
                 sa_g = fmaf(dE1[j][0], e1[j][0], fmaf(dE1[j][1], e1[j][1], sa_g));
                 sa_g8 = fmaf(dE1[j][2], e1[j][2], fmaf(dE1[j][3], e1[j][3], sa_g8));
                 scale_rows(dE1[j], -eg, -eg8);
@@ -468,14 +522,14 @@ mlp_backward_mma_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16
                 aS[3] = pack_bf16(v[1][2], v[1][3]);
             }
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
+            for (int j = 0; j < NJ; ++j) {
                 uint32_t b0, b1;
                 btok(E1A, j, b0, b1);
                 mma_bf16_16816(Zq[j], aS, b0, b1);
             }
-            float hq[4][4];
+            float hq[NJ][4];
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
+            for (int j = 0; j < NJ; ++j)
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const Gelu r = gelu3(Zq[j][e]);
@@ -492,9 +546,9 @@ mlp_backward_mma_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
 #pragma unroll
-                for (int jp = 0; jp < 2; ++jp) {
+                for (int jp = 0; jp < NJ / 2; ++jp) {
                     uint32_t b[4];
-                    ldb_nk<false>(w2s, 16 * jp, 16 * kk, lane, b);
+                    ldb_nk<0>(w2s, 16 * jp, 16 * kk, lane, b);
                     if (kk == 0) {
                         mma_bf16_16816_z(dHq[2 * jp], aZ[kk], b[0], b[1]);
                         mma_bf16_16816_z(dHq[2 * jp + 1], aZ[kk], b[2], b[3]);
@@ -510,16 +564,13 @@ mlp_backward_mma_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16
 #pragma unroll
             for (int tn = 0; tn < 2; ++tn)
 #pragma unroll
-                for (int kk = 0; kk < 2; ++kk) {
+                for (int kk = 0; kk < NKH; ++kk) {
                     if (kk == 0)
                         mma_bf16_16816_z(S2p[tn], HqA[kk], HkA[kk][tn], HkA[kk][2 + tn]);
                     else
                         mma_bf16_16816(S2p[tn], HqA[kk], HkA[kk][tn], HkA[kk][2 + tn]);
                 }
-#pragma unroll
-            for (int tn = 0; tn < 2; ++tn)
-                *reinterpret_cast<float4*>(psm + ((w * 2 + tn) * 32 + lane) * 4) =
-                    make_float4(S2p[tn][0], S2p[tn][1], S2p[tn][2], S2p[tn][3]);
+            put_partial(psm, S2p);
         }
         {
             // (Hk dW2')_j . E2_j over this warp's hidden units (the partial P2 dotted with E2)
@@ -527,9 +578,9 @@ mlp_backward_mma_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16
             for (int p = 0; p < 4; ++p) {
                 float P[2][4];
 #pragma unroll
-                for (int kk = 0; kk < 2; ++kk) {
+                for (int kk = 0; kk < NKH; ++kk) {
                     uint32_t b[4];
-                    ldb_kn<false>(g2s, 16 * p, 16 * kk, lane, b);
+                    ldb_kn<0>(g2s, 16 * p, 16 * kk, lane, b);
                     if (kk == 0) {
                         mma_bf16_16816_z(P[0], HkA[kk], b[0], b[1]);
                         mma_bf16_16816_z(P[1], HkA[kk], b[2], b[3]);
@@ -559,7 +610,7 @@ mlp_backward_mma_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16
             const int tn = tid >> 5, l = tid & 31, gl = l >> 2, tl = l & 3;
             float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-            for (int ww = 0; ww < NW; ++ww) {
+            for (int ww = 0; ww < 8; ++ww) {
                 const float4 v = *reinterpret_cast<const float4*>(psm + ((ww * 2 + tn) * 32 + l) * 4);
                 s.x += v.x, s.y += v.y, s.z += v.z, s.w += v.w;
             }
@@ -572,7 +623,7 @@ mlp_backward_mma_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16
         __syncthreads();
 
         // ================= B1: the Z = Hq W2 - (M . S2 D) E2 terms
-        uint32_t dZqA[2][4];
+        uint32_t dZqA[NKH][4];
         {
             // dA2 = -dZ E2^T (every warp; 16 x 16)
             float dA2[2][4];
@@ -583,7 +634,7 @@ mlp_backward_mma_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk) {
                     uint32_t b[4];
-                    ldb_nk<false>(sb + OFF_E2B, 0, 16 * kk, lane, b);
+                    ldb_nk<0>(sb + OFF_E2B, 0, 16 * kk, lane, b);
                     if (kk == 0) {
                         mma_bf16_16816_z(dA2[0], aZ[kk], b[0], b[1]);
                         mma_bf16_16816_z(dA2[1], aZ[kk], b[2], b[3]);
@@ -637,7 +688,7 @@ mlp_backward_mma_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16
             }
             // dHq += dS2 Hk, dHk += dS2^T Hq (over tokens)
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
+            for (int j = 0; j < NJ; ++j) {
                 uint32_t b0, b1;
                 btok(HkA, j, b0, b1);
                 mma_bf16_16816(dHq[j], aD, b0, b1);
@@ -645,7 +696,7 @@ mlp_backward_mma_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16
                 mma_bf16_16816(dHk[j], aDT, b0, b1);
             }
             // -(M . S2 D)^T dZ, d-columns 8 w .. 8 w + 7 (row j, over tokens i: -S2_ij eta_j for j <= i)
-            {
+            if (w < 8) {
                 uint32_t a[4];
                 float v[4][2];
 #pragma unroll
@@ -664,9 +715,9 @@ mlp_backward_mma_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16
                 *reinterpret_cast<float4*>(de2t + (w * 32 + lane) * 4) = make_float4(c[0], c[1], c[2], c[3]);
             }
             // dZq = dHq . g'(Zq)
-            float dzq[4][4];
+            float dzq[NJ][4];
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
+            for (int j = 0; j < NJ; ++j)
 #pragma unroll
                 for (int e = 0; e < 4; ++e) dzq[j][e] = dHq[j][e] * Zq[j][e];
             pack_slice(dzq, dZqA);
@@ -675,11 +726,11 @@ mlp_backward_mma_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16
             // dQ partial = dZq W1^T (over this warp's hidden units)
             float P[8][4];
 #pragma unroll
-            for (int kk = 0; kk < 2; ++kk)
+            for (int kk = 0; kk < NKH; ++kk)
 #pragma unroll
                 for (int p = 0; p < 4; ++p) {
                     uint32_t b[4];
-                    ldb_nk<true>(w1s, 16 * p, 16 * kk, lane, b);
+                    ldb_nk<HS>(w1s, 16 * p, 16 * kk, lane, b);
                     if (kk == 0) {
                         mma_bf16_16816_z(P[2 * p], dZqA[kk], b[0], b[1]);
                         mma_bf16_16816_z(P[2 * p + 1], dZqA[kk], b[2], b[3]);
@@ -688,16 +739,13 @@ mlp_backward_mma_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16
                         mma_bf16_16816(P[2 * p + 1], dZqA[kk], b[2], b[3]);
                     }
                 }
-#pragma unroll
-            for (int nt = 0; nt < 8; ++nt)
-                *reinterpret_cast<float4*>(part + ((w * 8 + nt) * 32 + lane) * 4) =
-                    make_float4(P[nt][0], P[nt][1], P[nt][2], P[nt][3]);
+            put_partial(part, P);
             // dA1 partial = -dZq E1^T
             float A1[2][4];
 #pragma unroll
             for (int tn = 0; tn < 2; ++tn)
 #pragma unroll
-                for (int kk = 0; kk < 2; ++kk) {
+                for (int kk = 0; kk < NKH; ++kk) {
                     if (kk == 0)
                         mma_bf16_16816_z(A1[tn], dZqA[kk], E1A[kk][tn], E1A[kk][2 + tn]);
                     else
@@ -705,15 +753,16 @@ mlp_backward_mma_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16
                 }
 #pragma unroll
             for (int tn = 0; tn < 2; ++tn)
-                *reinterpret_cast<float4*>(psm + ((w * 2 + tn) * 32 + lane) * 4) =
-                    make_float4(-A1[tn][0], -A1[tn][1], -A1[tn][2], -A1[tn][3]);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) A1[tn][e] = -A1[tn][e];
+            put_partial(psm, A1);
         }
         __syncthreads();
-        {
+        if (tid < 256) {
             const int nt = tid >> 5, l = tid & 31;
             float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-            for (int ww = 0; ww < NW; ++ww) {
+            for (int ww = 0; ww < 8; ++ww) {
                 const float4 v = *reinterpret_cast<const float4*>(part + ((ww * 8 + nt) * 32 + l) * 4);
                 s.x += v.x, s.y += v.y, s.z += v.z, s.w += v.w;
             }
@@ -722,7 +771,7 @@ mlp_backward_mma_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16
                 const int tn = tid >> 5, gl = l >> 2, tl = l & 3;
                 float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-                for (int ww = 0; ww < NW; ++ww) {
+                for (int ww = 0; ww < 8; ++ww) {
                     const float4 v = *reinterpret_cast<const float4*>(psm + ((ww * 2 + tn) * 32 + l) * 4);
                     a.x += v.x, a.y += v.y, a.z += v.z, a.w += v.w;
                 }
@@ -736,7 +785,7 @@ mlp_backward_mma_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16
         __syncthreads();
 
         // ================= B2: the Zq = Q W1 - (M . S1 D) E1 terms, then E1 = Gk . g'(Zk)
-        uint32_t dGkA[2][4];
+        uint32_t dGkA[NKH][4];
         {
             if (w == 0) {  // deta_j += sum_{i >= j} dA1_ij S1_ij
                 float cs[4];
@@ -779,14 +828,14 @@ mlp_backward_mma_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16
                 aT[2] = movt(a[1]);
                 aT[3] = movt(a[3]);
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
+                for (int j = 0; j < NJ; ++j) {
                     uint32_t b0, b1;
                     btok(dZqA, j, b0, b1);
                     mma_bf16_16816(dE1[j], aT, b0, b1);
                 }
             }
             // dQ += dS1 K and dS1^T Q, d-columns 8 w .. (dS1 = M . dA1 D)
-            {
+            if (w < 8) {
                 uint32_t a[4], aT[4];
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
@@ -812,9 +861,9 @@ mlp_backward_mma_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16
                 *reinterpret_cast<float4*>(dkt + (w * 32 + lane) * 4) = make_float4(k4[0], k4[1], k4[2], k4[3]);
             }
             // dGk = dE1 . g'(Zk) (packed), dZk = dE1 . Gk . g''(Zk) (into Gk)
-            float dgk[4][4];
+            float dgk[NJ][4];
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
+            for (int j = 0; j < NJ; ++j)
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     dgk[j][e] = dE1[j][e] * Zk[j][e];
@@ -826,11 +875,11 @@ mlp_backward_mma_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16
             // dE2 partial = -D (Hk dW2') + dGk W2 (over this warp's hidden units)
             float P[8][4];
 #pragma unroll
-            for (int kk = 0; kk < 2; ++kk)
+            for (int kk = 0; kk < NKH; ++kk)
 #pragma unroll
                 for (int p = 0; p < 4; ++p) {
                     uint32_t b[4];
-                    ldb_kn<false>(g2s, 16 * p, 16 * kk, lane, b);
+                    ldb_kn<0>(g2s, 16 * p, 16 * kk, lane, b);
                     if (kk == 0) {
                         mma_bf16_16816_z(P[2 * p], HkA[kk], b[0], b[1]);
                         mma_bf16_16816_z(P[2 * p + 1], HkA[kk], b[2], b[3]);
@@ -842,26 +891,23 @@ mlp_backward_mma_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16
 #pragma unroll
             for (int nt = 0; nt < 8; ++nt) scale_rows(P[nt], -eg, -eg8);
 #pragma unroll
-            for (int kk = 0; kk < 2; ++kk)
+            for (int kk = 0; kk < NKH; ++kk)
 #pragma unroll
                 for (int p = 0; p < 4; ++p) {
                     uint32_t b[4];
-                    ldb_kn<false>(w2s, 16 * p, 16 * kk, lane, b);
+                    ldb_kn<0>(w2s, 16 * p, 16 * kk, lane, b);
                     mma_bf16_16816(P[2 * p], dGkA[kk], b[0], b[1]);
                     mma_bf16_16816(P[2 * p + 1], dGkA[kk], b[2], b[3]);
                 }
-#pragma unroll
-            for (int nt = 0; nt < 8; ++nt)
-                *reinterpret_cast<float4*>(part + ((w * 8 + nt) * 32 + lane) * 4) =
-                    make_float4(P[nt][0], P[nt][1], P[nt][2], P[nt][3]);
+            put_partial(part, P);
         }
         __syncthreads();
-        {
+        if (tid < 256) {
             // dE2 = sum + the token term; dV = -dE2
             const int nt = tid >> 5, l = tid & 31, gl = l >> 2, tl = l & 3, col = 8 * nt + 2 * tl;
             float4 s = *reinterpret_cast<const float4*>(de2t + (nt * 32 + l) * 4);
 #pragma unroll
-            for (int ww = 0; ww < NW; ++ww) {
+            for (int ww = 0; ww < 8; ++ww) {
                 const float4 v = *reinterpret_cast<const float4*>(part + ((ww * 8 + nt) * 32 + l) * 4);
                 s.x += v.x, s.y += v.y, s.z += v.z, s.w += v.w;
             }
@@ -874,7 +920,7 @@ mlp_backward_mma_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16
         __syncthreads();
 
         // ================= B3: dHk += dE2 W2^T, dZk, the dK partial, the state gradient
-        uint32_t dZkA[2][4];
+        uint32_t dZkA[NKH][4];
         {
             uint32_t aD[4][4];
 #pragma unroll
@@ -882,25 +928,25 @@ mlp_backward_mma_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
 #pragma unroll
-                for (int jp = 0; jp < 2; ++jp) {
+                for (int jp = 0; jp < NJ / 2; ++jp) {
                     uint32_t b[4];
-                    ldb_nk<false>(w2s, 16 * jp, 16 * kk, lane, b);
+                    ldb_nk<0>(w2s, 16 * jp, 16 * kk, lane, b);
                     mma_bf16_16816(dHk[2 * jp], aD[kk], b[0], b[1]);
                     mma_bf16_16816(dHk[2 * jp + 1], aD[kk], b[2], b[3]);
                 }
-            float dzk[4][4];
+            float dzk[NJ][4];
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
+            for (int j = 0; j < NJ; ++j)
 #pragma unroll
                 for (int e = 0; e < 4; ++e) dzk[j][e] = fmaf(dHk[j][e], Zk[j][e], Gk[j][e]);
             pack_slice(dzk, dZkA);
         }
         // the running dW1 slice, loaded here so that its L2 round trip overlaps the dK partial
-        float2 u1[4][4][2];
+        float2 u1[4][NJ][2];
 #pragma unroll
         for (int mt = 0; mt < 4; ++mt)
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
+            for (int j = 0; j < NJ; ++j) {
                 const float* p0 = dW1g + size_t(16 * mt + g) * HID + hw + 8 * j + 2 * t;
                 u1[mt][j][0] = *reinterpret_cast<const float2*>(p0);
                 u1[mt][j][1] = *reinterpret_cast<const float2*>(p0 + 8 * HID);
@@ -909,11 +955,11 @@ mlp_backward_mma_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16
             // dK partial = -D (E1 dW1'^T) + dZk W1^T (over this warp's hidden units)
             float P[8][4];
 #pragma unroll
-            for (int kk = 0; kk < 2; ++kk)
+            for (int kk = 0; kk < NKH; ++kk)
 #pragma unroll
                 for (int p = 0; p < 4; ++p) {
                     uint32_t b[4];
-                    ldb_nk<true>(g1s, 16 * p, 16 * kk, lane, b);
+                    ldb_nk<HS>(g1s, 16 * p, 16 * kk, lane, b);
                     if (kk == 0) {
                         mma_bf16_16816_z(P[2 * p], E1A[kk], b[0], b[1]);
                         mma_bf16_16816_z(P[2 * p + 1], E1A[kk], b[2], b[3]);
@@ -925,18 +971,15 @@ mlp_backward_mma_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16
 #pragma unroll
             for (int nt = 0; nt < 8; ++nt) scale_rows(P[nt], -eg, -eg8);
 #pragma unroll
-            for (int kk = 0; kk < 2; ++kk)
+            for (int kk = 0; kk < NKH; ++kk)
 #pragma unroll
                 for (int p = 0; p < 4; ++p) {
                     uint32_t b[4];
-                    ldb_nk<true>(w1s, 16 * p, 16 * kk, lane, b);
+                    ldb_nk<HS>(w1s, 16 * p, 16 * kk, lane, b);
                     mma_bf16_16816(P[2 * p], dZkA[kk], b[0], b[1]);
                     mma_bf16_16816(P[2 * p + 1], dZkA[kk], b[2], b[3]);
                 }
-#pragma unroll
-            for (int nt = 0; nt < 8; ++nt)
-                *reinterpret_cast<float4*>(part + ((w * 8 + nt) * 32 + lane) * 4) =
-                    make_float4(P[nt][0], P[nt][1], P[nt][2], P[nt][3]);
+            put_partial(part, P);
         }
         // the block's state slices are read for the last time above: bring in the next block's
         __syncwarp();
@@ -944,9 +987,9 @@ mlp_backward_mma_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16
         cp_async_commit();
         {
             // the running dW2 slice, loaded before the dW1 products for the same reason
-            float2 u2[2][8][2];
+            float2 u2[NKH][8][2];
 #pragma unroll
-            for (int p = 0; p < 2; ++p)
+            for (int p = 0; p < NKH; ++p)
 #pragma unroll
                 for (int nt = 0; nt < 8; ++nt) {
                     const float* p0 = dW2g + size_t(hw + 16 * p + g) * D + 8 * nt + 2 * t;
@@ -960,7 +1003,7 @@ mlp_backward_mma_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16
                 lda_tokT(Qs, 16 * mt, lane, aQT);
                 lda_tokT(Ks, 16 * mt, lane, aKT);
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
+                for (int j = 0; j < NJ; ++j) {
                     const int r0 = 16 * mt + g, col = 8 * j + 2 * t;
                     float* p0 = dW1g + size_t(r0) * HID + hw + col;
                     float* p1 = p0 + 8 * HID;
@@ -972,13 +1015,14 @@ mlp_backward_mma_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16
                     mma_bf16_16816(c, aKT, b0, b1);
                     *reinterpret_cast<float2*>(p0) = make_float2(c[0], c[1]);
                     *reinterpret_cast<float2*>(p1) = make_float2(c[2], c[3]);
-                    *reinterpret_cast<uint32_t*>(smem + OFF_G1 + w * SZ_W1S + t32(r0, col)) = pack_bf16(c[0], c[1]);
-                    *reinterpret_cast<uint32_t*>(smem + OFF_G1 + w * SZ_W1S + t32(r0 + 8, col)) = pack_bf16(c[2], c[3]);
+                    *reinterpret_cast<uint32_t*>(smem + OFF_G1 + w * SZ_W1S + tl<HS>(r0, col)) = pack_bf16(c[0], c[1]);
+                    *reinterpret_cast<uint32_t*>(smem + OFF_G1 + w * SZ_W1S + tl<HS>(r0 + 8, col)) =
+                        pack_bf16(c[2], c[3]);
                 }
             }
             // dW2[slice, :] += Hq^T dZ + dGk^T E2 + Hk^T dE2 (over tokens); refresh the bf16 copy
 #pragma unroll
-            for (int p = 0; p < 2; ++p) {
+            for (int p = 0; p < NKH; ++p) {
                 uint32_t aHq[4], aGk[4], aHk[4];
                 atr(HqA, p, aHq);
                 atr(dGkA, p, aGk);
@@ -986,9 +1030,9 @@ mlp_backward_mma_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     uint32_t bz[4], be[4], bd[4];
-                    ldb_kn<false>(dZs, 16 * q, 0, lane, bz);
-                    ldb_kn<false>(sb + OFF_E2B, 16 * q, 0, lane, be);
-                    ldb_kn<false>(sb + OFF_DE2B, 16 * q, 0, lane, bd);
+                    ldb_kn<0>(dZs, 16 * q, 0, lane, bz);
+                    ldb_kn<0>(sb + OFF_E2B, 16 * q, 0, lane, be);
+                    ldb_kn<0>(sb + OFF_DE2B, 16 * q, 0, lane, bd);
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
                         const int r0 = 16 * p + g, col = 16 * q + 8 * h + 2 * t;
@@ -1009,12 +1053,12 @@ mlp_backward_mma_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16
             }
         }
         __syncthreads();
-        {
+        if (tid < 256) {
             // dK = sum + dS1^T Q; dQ; deta
             const int nt = tid >> 5, l = tid & 31, gl = l >> 2, tl = l & 3, col = 8 * nt + 2 * tl;
             float4 s = *reinterpret_cast<const float4*>(dkt + (nt * 32 + l) * 4);
 #pragma unroll
-            for (int ww = 0; ww < NW; ++ww) {
+            for (int ww = 0; ww < 8; ++ww) {
                 const float4 v = *reinterpret_cast<const float4*>(part + ((ww * 8 + nt) * 32 + l) * 4);
                 s.x += v.x, s.y += v.y, s.z += v.z, s.w += v.w;
             }
@@ -1040,18 +1084,28 @@ bool mlp_backward_mma_supported(const MlpBwdArgs& a) {
     return a.bf16 && a.d == D && a.hidden == HID && a.chunk == BT && a.T % BT == 0;
 }
 
-cudaError_t launch_mlp_backward_mma(const MlpBwdArgs& a, cudaStream_t s) {
-    if (!mlp_backward_mma_supported(a)) return cudaErrorNotSupported;
-    auto kern = mlp_backward_mma_kernel;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+template <int NW>
+cudaError_t launch_nw(const MlpBwdArgs& a, cudaStream_t s) {
+    using C = BwdCfg<NW>;
+    auto kern = mlp_backward_mma_kernel<NW>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    kern<<<unsigned(a.B) * unsigned(a.H), NTH, SMEM_BYTES, s>>>(
+    kern<<<unsigned(a.B) * unsigned(a.H), C::NTH, C::SMEM_BYTES, s>>>(
         static_cast<const __nv_bfloat16*>(a.Q), static_cast<const __nv_bfloat16*>(a.K),
         static_cast<const __nv_bfloat16*>(a.V), a.eta, static_cast<const __nv_bfloat16*>(a.W1_hist),
         static_cast<const __nv_bfloat16*>(a.W2_hist), static_cast<const __nv_bfloat16*>(a.dZ), a.dW1_T, a.dW2_T,
         static_cast<__nv_bfloat16*>(a.dQ), static_cast<__nv_bfloat16*>(a.dK), static_cast<__nv_bfloat16*>(a.dV),
         a.deta, a.dW1_0, a.dW2_0, a.T);
     return cudaGetLastError();
+}
+
+cudaError_t launch_mlp_backward_mma(const MlpBwdArgs& a, cudaStream_t s) {
+    if (!mlp_backward_mma_supported(a)) return cudaErrorNotSupported;
+    // eight warps of 32 hidden units each; TTT_MLP_BACKWARD_WARPS = 16 selects sixteen of 16 (correct, and
+    // measured slower on the TTT-MLP workload shape: 2.12 against 1.65 ms -- the per-warp work on the token
+    // side does not shrink, each reduction takes one more barrier, and 128 registers per thread)
+    const char* v = getenv("TTT_MLP_BACKWARD_WARPS");
+    return (v && !strcmp(v, "16")) ? launch_nw<16>(a, s) : launch_nw<8>(a, s);
 }
 
 }  // namespace ttt

@@ -163,3 +163,16 @@ def test_mlp_backward_mma_and_simt_kernels_agree(monkeypatch):
     b = _run(x, dZ, dW1, dW2, 16)[5]
     for name, u, v in zip(NAMES, a, b):
         assert rel_err(u, v.double().cpu().numpy()) <= TOL["bf16"], name
+
+
+def test_mlp_backward_mma_warp_layouts_agree(monkeypatch):
+    # eight warps of 32 hidden units (the default) and sixteen of 16 give the same gradients within the bar
+    x = WL.mlp_inputs(2, 2, 64, 64, 256, seed=4700, dtype="bf16", w_std=0.1)
+    dZ, dW1, dW2 = _grads(2, 2, 64, 64, 256, 4701, "bf16")
+    a = _run(x, dZ, dW1, dW2, 16)[5]
+    monkeypatch.setenv("TTT_MLP_BACKWARD_WARPS", "16")
+    b = _run(x, dZ, dW1, dW2, 16)[5]
+    ref = _oracle(x, dZ, dW1, dW2, 16)
+    for name, u, v, r in zip(NAMES, a, b, ref):
+        assert rel_err(u, r) <= TOL["bf16"] and rel_err(v, r) <= TOL["bf16"], name
+        assert rel_err(u, v.double().cpu().numpy()) <= TOL["bf16"], name
