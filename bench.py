@@ -222,12 +222,20 @@ def max_over_ranks(x: float, world: int) -> float:
     return float(t.item())
 
 
-def timed_loop(fn, steps, warmup, world, stream=None, sampler=None, min_warm_s=0.3):
+# Timed regions replay the K steps as one CUDA graph (the launches the steps make, captured in order with
+# their rotating inputs), so the device time is measured without the host's per-call launch work in the
+# way; --eager times per-call launches instead.
+GRAPH = True
+
+
+def timed_loop(fn, steps, warmup, world, stream=None, sampler=None, min_warm_s=0.3, graph=None):
     """Runs `fn(i)` warmup times untimed, then `steps` times between two barriers + syncs.
 
     Warm-up runs at least `warmup` steps and at least `min_warm_s` seconds (so the
     clocks have ramped up).  Returns (ms_per_step over the whole region, max over
-    ranks; mean per-launch ms from per-call CUDA events on the launching stream).
+    ranks; mean per-launch ms: from per-call CUDA events on the launching stream when
+    launching eagerly, the region divided by the steps when replaying a graph).  `graph` (default:
+    the module's GRAPH) is False for steps that are graph replays themselves.
     """
     stream = stream or torch.cuda.current_stream()
     t_start = time.perf_counter()
@@ -239,6 +247,27 @@ def timed_loop(fn, steps, warmup, world, stream=None, sampler=None, min_warm_s=0
             torch.cuda.synchronize()
     torch.cuda.synchronize()
     warmup = i
+    if GRAPH if graph is None else graph:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for j in range(steps):
+                fn(warmup + j)
+        torch.cuda.synchronize()
+        g.replay()  # one untimed replay: the graph's first launch uploads it
+        torch.cuda.synchronize()
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier(world)
+        torch.cuda.synchronize()
+        ctx = sampler if sampler is not None else _Null()
+        with ctx:
+            t0.record(stream)
+            g.replay()
+            t1.record(stream)
+            torch.cuda.synchronize()
+        barrier(world)
+        total = t0.elapsed_time(t1)
+        del g
+        return max_over_ranks(total / steps, world), total / steps
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
@@ -511,7 +540,7 @@ def bench_decode(T_mod, w, steps, warmup, world, peaks, graph_steps=1024, nrot=N
     with torch.cuda.graph(g):
         for i in range(graph_steps):
             T_mod.ttt_linear_decode_step(q[i], k[i], v[i], e[i], states[i % nrot], z[i])
-    ms, ms_launch = timed_loop(lambda i: g.replay(), steps, warmup, world)
+    ms, ms_launch = timed_loop(lambda i: g.replay(), steps, warmup, world, graph=False)
     per_step = ms_launch / graph_steps
     nbytes = decode_bytes(w.B, w.H, w.d)
     state_bytes = 2 * w.B * w.H * w.d * w.d * 4
@@ -547,7 +576,7 @@ def bench_mlp_decode(T_mod, w, steps, warmup, world, peaks, graph_steps=256, nro
         for i in range(graph_steps):
             W1, W2 = states[i % nrot]
             T_mod.ttt_mlp_decode_step(q[i], k[i], v[i], e[i], W1, W2, z[i])
-    ms, ms_launch = timed_loop(lambda i: g.replay(), steps, warmup, world)
+    ms, ms_launch = timed_loop(lambda i: g.replay(), steps, warmup, world, graph=False)
     per_step = ms_launch / graph_steps
     nbytes = mlp_decode_bytes(w.B, w.H, w.d, w.hidden)
     t_roof = nbytes / (peaks["hbm_gbs"] * 1e9)
@@ -703,7 +732,9 @@ def run_ours(args):
                    "global_batch": w.B * world, "seq_len": w.T, "heads": w.H, "head_dim": w.d, "chunk": w.chunk,
                    "parallelism": f"dp{world}" if world > 1 else "single-gpu",
                    "l2": f"{NROT} rotating input copies ({NROT * linear_bytes(w.B, w.H, w.T, w.d) / 1e6:.0f} MB > "
-                         f"126 MB L2)"},
+                         f"126 MB L2)",
+                   "timing": "the K steps replayed as one CUDA graph, CUDA events around the replay" if GRAPH
+                             else "per-call launches, CUDA events around the K steps"},
         "roofline": {"bound": "hbm", "achieved": head["achieved_gbs"],
                      "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": head["achieved_gbs"] / peaks["hbm_gbs"],
                      "traffic": ncu_traffic("linear_prefill", LINEAR_SRC),
@@ -811,6 +842,8 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--eager", action="store_true",
+                    help="time per-call launches instead of replaying the timed steps as a CUDA graph")
     ap.add_argument("--rows", choices=["all", "none", "linear_split", "mlp_prefill", "long_context",
                                        "decode", "mlp_decode", "backward", "momentum", "mlp_backward"],
                     default="all",
@@ -818,6 +851,8 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     args = ap.parse_args(argv)
+    global GRAPH
+    GRAPH = not args.eager
     args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps
     args.steps = max(1, args.steps)
     if args.impl == "reference":

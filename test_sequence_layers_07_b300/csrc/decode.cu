@@ -259,7 +259,7 @@ cudaError_t launch_stream(const DecodeArgs& a, cudaStream_t s, int* status) {
     const int groups = (BH + per - 1) / per;
     const unsigned grid = unsigned((groups + GPC - 1) / GPC);
     auto kern = linear_decode_stream_kernel<TI, D, GPC, NSTG>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::BYTES);
+    cudaError_t e = allow_dynamic_smem(reinterpret_cast<const void*>(kern), C::BYTES);
     if (e != cudaSuccess) return e;
     kern<<<grid, C::THREADS, C::BYTES, s>>>(static_cast<const TI*>(a.q), static_cast<const TI*>(a.k),
                                            static_cast<const TI*>(a.v), a.eta, a.W, static_cast<TI*>(a.z), BH, per,

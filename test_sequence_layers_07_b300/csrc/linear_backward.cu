@@ -174,7 +174,7 @@ template <typename TI, int D>
 cudaError_t launch_d(const LinearBwdArgs& a, cudaStream_t s) {
     auto kern = linear_backward_kernel<TI, D>;
     const size_t bytes = BwdSmem<D>::bytes(a.chunk);
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(bytes));
+    cudaError_t e = allow_dynamic_smem(reinterpret_cast<const void*>(kern), int(bytes));
     if (e != cudaSuccess) return e;
     kern<<<unsigned(a.B) * unsigned(a.H), kThreads, bytes, s>>>(
         static_cast<const TI*>(a.Q), static_cast<const TI*>(a.K), static_cast<const TI*>(a.V), a.eta,

@@ -632,7 +632,7 @@ cudaError_t launch_linear_backward_mma(const LinearBwdArgs& a, cudaStream_t s, i
     if ((e = make_tma_map_bf16(&mv, a.V, rows, D)) != cudaSuccess) return e;
     if ((e = make_tma_map_bf16(&mz, a.dZ, rows, D)) != cudaSuccess) return e;
     const int bytes = BYTES + 1024;
-    if ((e = cudaFuncSetAttribute(linear_backward_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) !=
+    if ((e = allow_dynamic_smem(reinterpret_cast<const void*>(linear_backward_mma_kernel), bytes)) !=
         cudaSuccess)
         return e;
     linear_backward_mma_kernel<<<unsigned(a.B) * unsigned(a.H), THREADS, bytes, s>>>(

@@ -317,7 +317,7 @@ linear_momentum_mma_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloa
 template <int CG>
 cudaError_t launch_cg(const LinearArgs& a, cudaStream_t s) {
     auto kern = linear_momentum_mma_kernel<CG>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    cudaError_t e = allow_dynamic_smem(reinterpret_cast<const void*>(kern), SMEM_BYTES);
     if (e != cudaSuccess) return e;
     kern<<<dim3(unsigned(a.B) * unsigned(a.H), 4 / CG), 32 * CG, SMEM_BYTES, s>>>(
         static_cast<const __nv_bfloat16*>(a.Q), static_cast<const __nv_bfloat16*>(a.K),

@@ -414,7 +414,7 @@ cudaError_t launch_cfg(const LinearArgs& a, cudaStream_t s, int* status) {
         return e;
     auto kern = linear_prefill_fused_kernel<D, CG, NST, SPS, SINGLE, HIST>;
     const int bytes = C::BYTES + 1024;  // + alignment slack
-    if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) != cudaSuccess) return e;
+    if ((e = allow_dynamic_smem(reinterpret_cast<const void*>(kern), bytes)) != cudaSuccess) return e;
     dim3 grid(unsigned(a.B) * unsigned(a.H), D / 16 / CG);
     kern<<<grid, C::THREADS, bytes, s>>>(mq, mk, mv, a.eta, a.W0, static_cast<__nv_bfloat16*>(a.Z), a.W_out, a.T,
                                          a.chunk, status, mh, a.wait_ns ? a.wait_ns : kWaitLimitNs);

@@ -268,7 +268,7 @@ cudaError_t launch_d(const LinearArgs& a, cudaStream_t s) {
     using C = GenCfg<D>;
     if (a.momentum) {
         auto kern = linear_prefill_generic_kernel<TI, D, true>;
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(C::BYTES));
+        cudaError_t e = allow_dynamic_smem(reinterpret_cast<const void*>(kern), int(C::BYTES));
         if (e != cudaSuccess) return e;
         dim3 grid(unsigned(a.B) * unsigned(a.H), C::SLICES);
         kern<<<grid, kThreads, C::BYTES, s>>>(static_cast<const TI*>(a.Q), static_cast<const TI*>(a.K),
@@ -277,7 +277,7 @@ cudaError_t launch_d(const LinearArgs& a, cudaStream_t s) {
         return cudaGetLastError();
     }
     auto kern = linear_prefill_generic_kernel<TI, D, false>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(C::BYTES));
+    cudaError_t e = allow_dynamic_smem(reinterpret_cast<const void*>(kern), int(C::BYTES));
     if (e != cudaSuccess) return e;
     dim3 grid(unsigned(a.B) * unsigned(a.H), C::SLICES);
     kern<<<grid, kThreads, C::BYTES, s>>>(static_cast<const TI*>(a.Q), static_cast<const TI*>(a.K),

@@ -595,7 +595,7 @@ cudaError_t launch_maps(const LinearArgs& a, const SegPlan& p, float* maps, cuda
     if ((e = make_tma_map_bf16(&mv, a.V, rows, D)) != cudaSuccess) return e;
     auto kern = linear_segmap_kernel<D, NG, NST, SPS>;
     const int bytes = C::BYTES + 1024;
-    if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) != cudaSuccess) return e;
+    if ((e = allow_dynamic_smem(reinterpret_cast<const void*>(kern), bytes)) != cudaSuccess) return e;
     dim3 grid(unsigned(a.B) * unsigned(a.H) * unsigned(p.nseg - 1), 2 * D / 16 / NG);
     kern<<<grid, C::THREADS, bytes, s>>>(mk, mv, a.eta, maps, a.T, a.chunk, p.seg_len, p.nseg, status);
     return cudaGetLastError();
@@ -606,7 +606,7 @@ cudaError_t launch_combine(const LinearArgs& a, const SegPlan& p, const float* m
     using C = CombineCfg<D>;
     auto kern = linear_segcombine_kernel<D>;
     cudaError_t e;
-    if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::BYTES)) != cudaSuccess)
+    if ((e = allow_dynamic_smem(reinterpret_cast<const void*>(kern), C::BYTES)) != cudaSuccess)
         return e;
     kern<<<dim3(unsigned(a.B) * unsigned(a.H), D / C::CW), C::NT, C::BYTES, s>>>(a.W0, maps, starts, p.nseg);
     return cudaGetLastError();
@@ -625,7 +625,7 @@ cudaError_t launch_scan64(const LinearArgs& a, const SegPlan& p, const float* st
     const int npairs = a.B * a.H * p.nseg;
     const int bytes = C::BYTES + 1024;
     auto run = [&](auto kern) -> cudaError_t {
-        cudaError_t e2 = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+        cudaError_t e2 = allow_dynamic_smem(reinterpret_cast<const void*>(kern), bytes);
         if (e2 != cudaSuccess) return e2;
         kern<<<unsigned((npairs + 1) / 2), C::THREADS, bytes, s>>>(mq, mk, mv, a.eta, a.W0, starts,
                                                                    static_cast<__nv_bfloat16*>(a.Z), a.W_out, a.T,

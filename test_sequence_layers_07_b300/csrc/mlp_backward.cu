@@ -474,7 +474,7 @@ cudaError_t launch_d(const MlpBwdArgs& a, cudaStream_t s) {
     const Lay L(a.chunk, a.d, a.hidden);
     const size_t bytes = L.floats * sizeof(float);
     auto kern = mlp_backward_kernel<TI, D>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(bytes));
+    cudaError_t e = allow_dynamic_smem(reinterpret_cast<const void*>(kern), int(bytes));
     if (e != cudaSuccess) return e;
     kern<<<unsigned(a.B) * unsigned(a.H), kNT, bytes, s>>>(
         static_cast<const TI*>(a.Q), static_cast<const TI*>(a.K), static_cast<const TI*>(a.V), a.eta,

@@ -1088,7 +1088,7 @@ template <int NW>
 cudaError_t launch_nw(const MlpBwdArgs& a, cudaStream_t s) {
     using C = BwdCfg<NW>;
     auto kern = mlp_backward_mma_kernel<NW>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    cudaError_t e = allow_dynamic_smem(reinterpret_cast<const void*>(kern), C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     kern<<<unsigned(a.B) * unsigned(a.H), C::NTH, C::SMEM_BYTES, s>>>(
         static_cast<const __nv_bfloat16*>(a.Q), static_cast<const __nv_bfloat16*>(a.K),

@@ -177,7 +177,7 @@ template <typename TI, int D, int HID>
 cudaError_t launch_dh(const MlpDecodeArgs& a, cudaStream_t s) {
     auto kern = mlp_decode_kernel<TI, D, HID>;
     constexpr size_t bytes = smem_bytes<D, HID>();
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(bytes));
+    cudaError_t e = allow_dynamic_smem(reinterpret_cast<const void*>(kern), int(bytes));
     if (e != cudaSuccess) return e;
     kern<<<unsigned(a.B) * unsigned(a.H), HID, bytes, s>>>(static_cast<const TI*>(a.q), static_cast<const TI*>(a.k),
                                                           static_cast<const TI*>(a.v), a.eta, a.W1, a.W2,

@@ -183,7 +183,7 @@ cudaError_t launch_mlp_prefill_generic(const MlpArgs& a, cudaStream_t s) {
     cudaError_t e;
     if (a.bf16) {
         auto kern = mlp_prefill_generic_kernel<__nv_bfloat16>;
-        if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(bytes))) != cudaSuccess)
+        if ((e = allow_dynamic_smem(reinterpret_cast<const void*>(kern), int(bytes))) != cudaSuccess)
             return e;
         kern<<<unsigned(a.B) * unsigned(a.H), kThreads, bytes, s>>>(
             static_cast<const __nv_bfloat16*>(a.Q), static_cast<const __nv_bfloat16*>(a.K),
@@ -192,7 +192,7 @@ cudaError_t launch_mlp_prefill_generic(const MlpArgs& a, cudaStream_t s) {
             static_cast<__nv_bfloat16*>(a.W2_hist));
     } else {
         auto kern = mlp_prefill_generic_kernel<float>;
-        if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(bytes))) != cudaSuccess)
+        if ((e = allow_dynamic_smem(reinterpret_cast<const void*>(kern), int(bytes))) != cudaSuccess)
             return e;
         kern<<<unsigned(a.B) * unsigned(a.H), kThreads, bytes, s>>>(
             static_cast<const float*>(a.Q), static_cast<const float*>(a.K), static_cast<const float*>(a.V), a.eta,

@@ -553,7 +553,7 @@ cudaError_t launch_mlp_prefill_mma(const MlpArgs& a, cudaStream_t s, int* status
         if ((e = make_tma_map_bf16_box(&h2, a.W2_hist, blocks * HID, D, D, HS, 128)) != cudaSuccess) return e;
     }
     auto run = [&](auto kern, int bytes) -> cudaError_t {
-        cudaError_t e2 = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+        cudaError_t e2 = allow_dynamic_smem(reinterpret_cast<const void*>(kern), bytes);
         if (e2 != cudaSuccess) return e2;
         kern<<<unsigned(a.B) * unsigned(a.H), THREADS, bytes, s>>>(mq, mk, mv, a.eta, a.W1_0, a.W2_0,
                                                                   static_cast<__nv_bfloat16*>(a.Z), a.W1_out,

@@ -569,7 +569,7 @@ cudaError_t launch_mlp_prefill_tc(const MlpArgs& a, cudaStream_t s, int* status)
     if ((e = make_tma_map_bf16(&mk, a.K, rows, D)) != cudaSuccess) return e;
     if ((e = make_tma_map_bf16(&mv, a.V, rows, D)) != cudaSuccess) return e;
     const int bytes = SMEM_BYTES + 1024;
-    if ((e = cudaFuncSetAttribute(mlp_prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) !=
+    if ((e = allow_dynamic_smem(reinterpret_cast<const void*>(mlp_prefill_tc_kernel), bytes)) !=
         cudaSuccess)
         return e;
     mlp_prefill_tc_kernel<<<unsigned(a.B) * unsigned(a.H), THREADS, bytes, s>>>(

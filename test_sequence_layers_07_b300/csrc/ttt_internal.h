@@ -169,6 +169,8 @@ cudaError_t launch_mlp_prefill_tc(const MlpArgs& a, cudaStream_t s, int* status)
 // TMA descriptor of a [rows][D] bf16 row-major tensor: boxes of 16 rows x 64
 // columns with the 128-byte swizzle (D a multiple of 64).
 cudaError_t make_tma_map_bf16(CUtensorMap* m, const void* base, uint64_t rows, int D);
+// cudaFuncSetAttribute(MaxDynamicSharedMemorySize, bytes) for `func`, once per kernel and CUDA context
+cudaError_t allow_dynamic_smem(const void* func, int bytes);
 // TMA descriptor of a [rows][64] fp32 row-major tensor: boxes of 64 rows x 32 columns (128 bytes),
 // 128-byte swizzle (two boxes cover a 64 x 64 block).
 cudaError_t make_tma_map_f32x64(CUtensorMap* m, const void* base, uint64_t rows);
