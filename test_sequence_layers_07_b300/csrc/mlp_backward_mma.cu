@@ -21,10 +21,11 @@
 // The block-start states come from the forward (ttt_mlp_prefill_hist), recorded in bf16.
 //
 // Design (ours, for sm_103a):
-//  * One CTA of eight warps per (batch, head), blocks in reverse order.  Warp w owns hidden units
-//    [32 w, 32 w + 32): every b x hidden quantity (Zk, Hk, Gk, E1, Zq, Hq, dHk, dHq, dE1, dZk, ...)
-//    lives in its registers as the MMA accumulator slice 16 x 32, so the element-wise steps (GELU
-//    and its derivatives, the products with g') need no shared memory.  An accumulator slice read
+//  * One CTA of NW warps per (batch, head) (eight by default; sixteen can be chosen), blocks in
+//    reverse order.  Warp w owns hidden units [HS w, HS w + HS), HS = 256 / NW: every b x hidden
+//    quantity (Zk, Hk, Gk, E1, Zq, Hq, dHk, dHq, dE1, dZk, ...) lives in its registers as the MMA
+//    accumulator slice 16 x HS, so the element-wise steps (GELU and its derivatives, the products
+//    with g') need no shared memory.  An accumulator slice read
 //    as bf16 pairs is the A fragment of the slice over its hidden columns and the B fragment of its
 //    transpose; the B fragment over tokens and the A fragment of the transpose come from movmatrix.
 //  * Products over d (K W1, Q W1, E2 W2^T, dZ W2^T, K dW1', E2 dW2'^T, dE2 W2^T) take their B
@@ -32,8 +33,8 @@
 //    copy of dW1', dW2', all in warp-private shared memory: no barrier guards them.
 //  * Products over the hidden dimension (E2, Hq Hk^T, dZq W1^T, dZq E1^T, the dE2 and dK sums) are
 //    partial per warp and summed in a fixed order through shared memory: five reductions a block,
-//    two barriers each.  Small token-by-token products (the masked score terms) run one 8-column
-//    tile per warp.
+//    two barriers each (three with sixteen warps, whose partials pair up first).  Small
+//    token-by-token products (the masked score terms) run one 8-column tile per warp (warps 0-7).
 //  * The running state gradient (fp32) lives in dW1_0 / dW2_0 (L2-resident): each warp reads its
 //    slices as accumulator fragments, adds the block's rank-16 terms by MMA, writes them back and
 //    refreshes its bf16 copy.
