@@ -446,7 +446,8 @@ cudaError_t launch_chunk(const LinearArgs& a, cudaStream_t s, int* status) {
 }  // namespace
 
 cudaError_t launch_linear_prefill_mma(const LinearArgs& a, cudaStream_t s, int* status) {
-    if (!a.bf16 || (a.d != 64 && a.d != 128) || a.chunk % 16 != 0 || a.T % a.chunk != 0) return cudaErrorNotSupported;
+    // a ragged last block (chunk does not divide T) of whole 16-token sub-blocks is fewer sub-blocks
+    if (!a.bf16 || (a.d != 64 && a.d != 128) || a.chunk % 16 != 0 || a.T % 16 != 0) return cudaErrorNotSupported;
     if (uint64_t(a.B) * a.H * a.T > 0x7fffffffull) return cudaErrorNotSupported;  // TMA row coordinate is int32
     int dev = 0, sms = 148;
     if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);

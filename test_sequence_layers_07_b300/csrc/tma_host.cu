@@ -36,9 +36,10 @@ struct MapKey {
     const void* base;
     uint64_t rows;
     int cols, box_cols, box_rows, swizzle, elt;
+    uint64_t planes;  // 0 for a 2D map, else the extent of the third dimension
     bool operator==(const MapKey& o) const {
         return base == o.base && rows == o.rows && cols == o.cols && box_cols == o.box_cols &&
-               box_rows == o.box_rows && swizzle == o.swizzle && elt == o.elt;
+               box_rows == o.box_rows && swizzle == o.swizzle && elt == o.elt && planes == o.planes;
     }
 };
 constexpr int kMapCache = 16;
@@ -63,7 +64,7 @@ void remember_map(const MapKey& k, const CUtensorMap& m) {
 
 // [rows][D] bf16 viewed as a 2D tensor; box = 16 rows x 64 columns, 128-byte swizzle.
 cudaError_t make_tma_map_bf16(CUtensorMap* m, const void* base, uint64_t rows, int D) {
-    const MapKey key{base, rows, D, 64, 16, 128, 2};
+    const MapKey key{base, rows, D, 64, 16, 128, 2, 0};
     if (cached_map(key, m)) return cudaSuccess;
     EncodeTiledFn enc;
     cudaError_t e = get_encoder(&enc);
@@ -80,13 +81,33 @@ cudaError_t make_tma_map_bf16(CUtensorMap* m, const void* base, uint64_t rows, i
     return cudaSuccess;
 }
 
+// [heads][T][D] bf16 viewed as a 3D tensor; box = 16 tokens x 64 columns of one head, 128-byte swizzle.
+// A box that reaches past a head's last token reads zeros there, not the next head's rows.
+cudaError_t make_tma_map_bf16_heads(CUtensorMap* m, const void* base, uint64_t heads, int T, int D) {
+    const MapKey key{base, uint64_t(T), D, 64, 16, 128, 2, heads};
+    if (cached_map(key, m)) return cudaSuccess;
+    EncodeTiledFn enc;
+    cudaError_t e = get_encoder(&enc);
+    if (e != cudaSuccess) return e;
+    cuuint64_t dims[3] = {cuuint64_t(D), cuuint64_t(T), cuuint64_t(heads)};
+    cuuint64_t strides[2] = {cuuint64_t(D) * 2, cuuint64_t(T) * D * 2};
+    cuuint32_t box[3] = {64, 16, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    remember_map(key, *m);
+    return cudaSuccess;
+}
+
 // [rows][D] bf16 viewed as a 2D tensor; box = box_rows x box_cols: a slice a warp stages for a TMA store
 // (box_cols * 2 bytes a multiple of 16).  swizzle_bytes: 0 (row-major in shared memory), 64 or 128 (the
 // 16-byte chunks of each box row XOR bits 7.. of the shared-memory offset, as the tensor core's swizzle
 // modes define; the box row is then at most that many bytes).
 cudaError_t make_tma_map_bf16_box(CUtensorMap* m, const void* base, uint64_t rows, int D, int box_cols,
                                   int box_rows, int swizzle_bytes) {
-    const MapKey key{base, rows, D, box_cols, box_rows, swizzle_bytes, 2};
+    const MapKey key{base, rows, D, box_cols, box_rows, swizzle_bytes, 2, 0};
     if (cached_map(key, m)) return cudaSuccess;
     EncodeTiledFn enc;
     cudaError_t e = get_encoder(&enc);

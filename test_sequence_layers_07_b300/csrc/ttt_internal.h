@@ -169,6 +169,9 @@ cudaError_t launch_mlp_prefill_tc(const MlpArgs& a, cudaStream_t s, int* status)
 // TMA descriptor of a [rows][D] bf16 row-major tensor: boxes of 16 rows x 64
 // columns with the 128-byte swizzle (D a multiple of 64).
 cudaError_t make_tma_map_bf16(CUtensorMap* m, const void* base, uint64_t rows, int D);
+// TMA descriptor of a [heads][T][D] bf16 tensor: boxes of 16 tokens x 64 columns of one head, 128-byte
+// swizzle; tokens past T read as zeros (T * D * 2 a multiple of 16 bytes).
+cudaError_t make_tma_map_bf16_heads(CUtensorMap* m, const void* base, uint64_t heads, int T, int D);
 // cudaFuncSetAttribute(MaxDynamicSharedMemorySize, bytes) for `func`, once per kernel and CUDA context
 cudaError_t allow_dynamic_smem(const void* func, int bytes);
 // TMA descriptor of a [rows][64] fp32 row-major tensor: boxes of 64 rows x 32 columns (128 bytes),

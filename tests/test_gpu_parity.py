@@ -396,3 +396,46 @@ def test_prefill_then_decode_hand_off(kind):
         assert rel_err(W1, A2) <= TOL["bf16"] and rel_err(W2, B2) <= TOL["bf16"]
     assert rel_err(Zp, Zr1) <= TOL["bf16"]
     assert rel_err(torch.stack(zs, 2), Zr2) <= TOL["bf16"]
+
+
+# bf16 with 16 | T but chunk not dividing T: the tensor-core kernels take the shorter last block as fewer
+# 16-token sub-blocks
+@pytest.mark.parametrize("d,kernel", [(64, "fused"), (64, "mma"), (128, "mma")])
+@pytest.mark.parametrize("B,H,T_,chunk", [(2, 3, 208, 64), (1, 2, 1040, 512), (2, 2, 96, 80), (3, 16, 272, 32)])
+def test_linear_tensor_core_kernels_ragged_last_block(d, kernel, B, H, T_, chunk):
+    x = WL.linear_inputs(B, H, T_, d, seed=900 + T_ + chunk + d, dtype="bf16")
+    with linear_kernel(kernel):
+        Z, W = run_linear(x, chunk)
+    r = f64(x)
+    Zr, Wr = O.linear_dual(r["Q"], r["K"], r["V"], r["eta"], r["W0"], chunk)
+    assert rel_err(Z, Zr) <= TOL["bf16"]
+    assert rel_err(W, Wr) <= TOL["bf16"]
+
+
+# bf16, d = 64, T not a multiple of 16: the fused kernel runs a partial last sub-block (its eta from
+# global memory, read only where the tokens exist; with 4 not dividing T every sub-block's eta comes
+# from there); T = 260 / 261 leave the last stage of 256 tokens holding only the partial sub-block
+@pytest.mark.parametrize("T_", [1, 7, 17, 203, 212, 260, 261, 2047])
+@pytest.mark.parametrize("chunk", [16, 64])
+def test_fused_partial_last_sub_block(T_, chunk):
+    x = WL.linear_inputs(2, 3, T_, 64, seed=950 + T_ + chunk, dtype="bf16")
+    with linear_kernel("fused"):
+        Z, W = run_linear(x, chunk)
+    r = f64(x)
+    Zr, Wr = O.linear_dual(r["Q"], r["K"], r["V"], r["eta"], r["W0"], chunk)
+    assert rel_err(Z, Zr) <= TOL["bf16"]
+    assert rel_err(W, Wr) <= TOL["bf16"]
+
+
+def test_fused_partial_sub_block_reads_no_rows_of_the_next_head():
+    # head 1 holds values whose products overflow; head 0 (T = 23: a partial second sub-block) must
+    # not see them, since the tokens past its end read as zeros rather than as head 1's rows
+    x = WL.linear_inputs(1, 2, 23, 64, seed=977, dtype="bf16")
+    for k in ("Q", "K", "V"):
+        x[k][:, 1] = 3.0e38
+    with linear_kernel("fused"):
+        Z, W = run_linear(x, 16)
+    r = f64({k: v[:, :1] for k, v in x.items()})
+    Zr, Wr = O.linear_dual(r["Q"], r["K"], r["V"], r["eta"], r["W0"], 16)
+    assert rel_err(Z[:, :1], Zr) <= TOL["bf16"]
+    assert rel_err(W[:, :1], Wr) <= TOL["bf16"]
