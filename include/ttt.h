@@ -87,10 +87,10 @@ typedef enum ttt_dtype {
  *   chunk    1..512; the last block may be shorter when chunk does not divide T
  *   d        16, 32, 64 or 128 (else TTT_ERR_UNSUPPORTED)
  *
- * Kernels: bf16 with 16 | chunk runs on warp-level tensor-core MMAs (d = 64,
- * any T: one warp per 16-column group; d = 128 with 16 | T: a recurrence warp
- * and a read-out warp per group); a shorter last block is fewer 16-token steps,
- * a partial last step weighs the tokens past T by zero.  Other shapes run on a
+ * Kernels: bf16 with 16 | chunk runs on warp-level tensor-core MMAs, for any T
+ * (d = 64: one warp per 16-column group; d = 128: a recurrence warp and a
+ * read-out warp per group); a shorter last block is fewer 16-token steps, a
+ * partial last step weighs the tokens past T by zero.  Other shapes run on a
  * generic SIMT kernel.  The
  * environment variable TTT_LINEAR_PREFILL_KERNEL = "fused", "tc", "mma" or
  * "generic" starts the choice at that kernel ("tc": d = 64 with the read-out

@@ -88,9 +88,11 @@ struct Cfg {
     static constexpr int THREADS = 32 * (2 * CG + 2);
 };
 
-// HIST: also write the state at the start of every block to W_hist [B*H][T/chunk][D][D], rounded
+// HIST: also write the state at the start of every block to W_hist [B*H][ceil(T/16)][D][D], rounded
 // to bf16 (what the backward reads); instantiated for blocks of 16 tokens only.
-template <int D, int CG, int NST, int SPS, int NX, bool SINGLE, bool HIST>
+// PART: T is not a multiple of 16 (a partial last sub-block); the instantiation for 16 | T compiles
+// none of the checks that case needs.
+template <int D, int CG, int NST, int SPS, int NX, bool SINGLE, bool HIST, bool PART>
 __global__ void __launch_bounds__(Cfg<D, CG, NST, SPS, NX>::THREADS, 1)
 linear_prefill_mma_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                           const __grid_constant__ CUtensorMap tmV, const float* __restrict__ eta,
@@ -110,9 +112,10 @@ linear_prefill_mma_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const size_t bh = blockIdx.x;
-    const int nsb = T / 16;                    // 16-token sub-blocks
+    const int nsb = (T + 15) / 16;             // 16-token sub-blocks (the last may be partial)
     const int nstg = (nsb + SPS - 1) / SPS;    // stages
     const int nsub = chunk / 16;               // sub-blocks per block
+    const bool ebulk = !PART || (T & 3) == 0;  // a head's eta starts 16-byte aligned
     const uint32_t sbase = smem_u32(smem);
     const int g = lane >> 2, t = lane & 3;
     const int lj = lane >> 3, lr = lane & 7;
@@ -145,6 +148,11 @@ linear_prefill_mma_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_
         return __all_sync(0xffffffffu, wait(bar, parity));
     };
     auto subs_in = [&](int si) { return nsb - si * SPS < SPS ? nsb - si * SPS : SPS; };
+    // a stage of SPS whole sub-blocks with its eta staged: its loops run without the checks for a
+    // partial sub-block
+    auto full_stage = [&](int si) {
+        return subs_in(si) == SPS && (!PART || (ebulk && 16 * SPS * (si + 1) <= T));
+    };
 
     // lane-dependent ldmatrix coordinates (byte offsets inside a sub-tile)
     uint32_t off_nk[KS], off_tk[NT / 2];
@@ -164,18 +172,23 @@ linear_prefill_mma_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_
                 const int s = si % NST, n = subs_in(si);
                 if (si >= NST && !wait(empty_bar[s], ((si / NST) - 1) & 1)) break;
                 const uint32_t fb = smem_u32(&full_bar[s]);
-                mbar_arrive_expect_tx(fb, uint32_t(n) * (3 * C::TILE + 64));
+                // eta of the stage's whole sub-blocks when a head's eta starts on a 16-byte boundary
+                // (4 | T); otherwise, and for a partial last sub-block, the chain reads eta from global
+                // memory.  Q/K/V boxes past the head's T read zeros.
+                const int tok = min(16 * n, T - 16 * si * SPS);
+                const uint32_t ebytes = ebulk ? uint32_t(tok * 4) & ~63u : 0u;
+                mbar_arrive_expect_tx(fb, uint32_t(n) * 3 * C::TILE + ebytes);
                 const uint32_t st = sbase + s * C::STAGE;
                 for (int i = 0; i < n; ++i) {
-                    const int y = int(bh * T) + 16 * (si * SPS + i);
+                    const int y = 16 * (si * SPS + i), z = int(bh);
 #pragma unroll
                     for (int box = 0; box < D / 64; ++box) {
-                        tma_load_2d(st + C::QOFF + i * C::TILE + box * 2048, &tmQ, 64 * box, y, fb);
-                        tma_load_2d(st + C::KOFF + i * C::TILE + box * 2048, &tmK, 64 * box, y, fb);
-                        tma_load_2d(st + C::VOFF + i * C::TILE + box * 2048, &tmV, 64 * box, y, fb);
+                        tma_load_3d(st + C::QOFF + i * C::TILE + box * 2048, &tmQ, 64 * box, y, z, fb);
+                        tma_load_3d(st + C::KOFF + i * C::TILE + box * 2048, &tmK, 64 * box, y, z, fb);
+                        tma_load_3d(st + C::VOFF + i * C::TILE + box * 2048, &tmV, 64 * box, y, z, fb);
                     }
                 }
-                bulk_load(st + C::EOFF, eta + bh * T + 16 * si * SPS, uint32_t(n) * 64, fb);
+                if (ebytes) bulk_load(st + C::EOFF, eta + bh * T + 16 * si * SPS, ebytes, fb);
                 ++issued;
             }
             // never retire the CTA with copies in flight (this wait ignores the abort flag)
@@ -246,16 +259,26 @@ linear_prefill_mma_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_
             uint32_t wa0[KS][4];
             uint32_t kb[KS][4], kt[NT / 2][4];
             float ne0 = 0, ne1 = 0, ne2 = 0, ne3 = 0, nv[8] = {};
-            auto load = [&](uint32_t st, int i) {
+            // sub-block i of the stage at st (sb in the head); chk: it may be partial or its eta may
+            // not be staged (a constant false on full stages)
+            auto load = [&](uint32_t st, int i, int sb, bool chk) {
 #pragma unroll
                 for (int ks = 0; ks < KS; ++ks) ldsm_x4(st + C::KOFF + i * C::TILE + off_nk[ks], kb[ks]);
 #pragma unroll
                 for (int kk = 0; kk < NT / 2; ++kk) ldsm_x4_trans(st + C::KOFF + i * C::TILE + off_tk[kk], kt[kk]);
                 uint32_t vv[4];
                 ldsm_x4_trans(st + C::VOFF + i * C::TILE + off_v, vv);
-                const float* es = reinterpret_cast<const float*>(smem + (st - sbase) + C::EOFF + i * 64);
-                const float2 e01 = *reinterpret_cast<const float2*>(es + 2 * t);
-                const float2 e23 = *reinterpret_cast<const float2*>(es + 8 + 2 * t);
+                float2 e01, e23;
+                if (!PART || !chk || (ebulk && 16 * sb + 16 <= T)) {
+                    const float* es = reinterpret_cast<const float*>(smem + (st - sbase) + C::EOFF + i * 64);
+                    e01 = *reinterpret_cast<const float2*>(es + 2 * t);
+                    e23 = *reinterpret_cast<const float2*>(es + 8 + 2 * t);
+                } else {  // eta from global memory; tokens past T weigh zero
+                    const float* eg = eta + bh * T;
+                    const int j = 16 * sb + 2 * t;
+                    e01 = make_float2(j < T ? eg[j] : 0.f, j + 1 < T ? eg[j + 1] : 0.f);
+                    e23 = make_float2(j + 8 < T ? eg[j + 8] : 0.f, j + 9 < T ? eg[j + 9] : 0.f);
+                }
                 ne0 = -e01.x; ne1 = -e01.y; ne2 = -e23.x; ne3 = -e23.y;
                 nv[0] = e01.x * bf16_lo(vv[0]); nv[1] = e01.y * bf16_hi(vv[0]);
                 nv[2] = e01.x * bf16_lo(vv[1]); nv[3] = e01.y * bf16_hi(vv[1]);
@@ -263,7 +286,7 @@ linear_prefill_mma_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_
                 nv[6] = e23.x * bf16_lo(vv[3]); nv[7] = e23.y * bf16_hi(vv[3]);
             };
             bool ok = wait_all(full_bar[0], 0);
-            if (ok) load(sbase, 0);
+            if (ok) load(sbase, 0, 0, !full_stage(0));
             for (int si = 0; ok && si < nstg; ++si) {
                 const int s = si % NST, n = subs_in(si), x = si % NX;
                 const uint32_t st = sbase + s * C::STAGE;
@@ -273,7 +296,7 @@ linear_prefill_mma_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_
                     const int sb = si * SPS + i;
                     if (SINGLE || sb % nsub == 0) {
                         if constexpr (HIST) {  // the state at the start of block sb / nsub, as bf16
-                            __nv_bfloat16* wh = W_hist + (bh * size_t(nsb / nsub) + sb / nsub) * D * D;
+                            __nv_bfloat16* wh = W_hist + (bh * size_t(nsb) + sb) * D * D;  // chunk 16
 #pragma unroll
                             for (int nt = 0; nt < NT; ++nt) {
                                 const int r = 8 * nt + 2 * t;
@@ -310,16 +333,16 @@ linear_prefill_mma_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_
                     }
                     *reinterpret_cast<uint4*>(gout + i * 512 + lane * 16) = make_uint4(ga[0], ga[1], ga[2], ga[3]);
                 };
-                if (n == SPS) {  // full stage: unrolled, so the compiler schedules across sub-blocks
+                if (full_stage(si)) {  // unrolled, so the compiler schedules across sub-blocks
 #pragma unroll
                     for (int i = 0; i < SPS; ++i) {
                         step(i);
-                        if (i + 1 < SPS) load(st, i + 1);
+                        if (i + 1 < SPS) load(st, i + 1, si * SPS + i + 1, false);
                     }
                 } else {
                     for (int i = 0; i < n; ++i) {
                         step(i);
-                        if (i + 1 < n) load(st, i + 1);
+                        if (i + 1 < n) load(st, i + 1, si * SPS + i + 1, true);
                     }
                 }
                 __syncwarp();
@@ -327,7 +350,7 @@ linear_prefill_mma_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_
                 if (si + 1 < nstg) {
                     const int s1 = (si + 1) % NST;
                     ok = wait_all(full_bar[s1], ((si + 1) / NST) & 1);
-                    if (ok) load(sbase + s1 * C::STAGE, 0);
+                    if (ok) load(sbase + s1 * C::STAGE, 0, (si + 1) * SPS, !full_stage(si + 1));
                 }
             }
             float* Wo = W_out + bh * D * D;
@@ -354,7 +377,8 @@ linear_prefill_mma_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_
                     break;
                 const uint32_t st = sbase + s * C::STAGE;
                 const uint8_t* gin = gslots + x * SPS * 512;
-                auto step = [&](int i) {
+                // chk: rows past T are not stored (only the last sub-block can be partial)
+                auto step = [&](int i, bool chk) {
                     uint32_t qb[KS][4], kt[NT / 2][4], wr[KS][4];
 #pragma unroll
                     for (int ks = 0; ks < KS; ++ks) ldsm_x4(st + C::QOFF + i * C::TILE + off_nk[ks], qb[ks]);
@@ -391,15 +415,15 @@ linear_prefill_mma_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_
                                  : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                                  : "r"(zst_r)
                                  : "memory");
-                    *reinterpret_cast<uint4*>(zp) = v;
+                    if (!PART || !chk || 16 * (si * SPS + i) + zrow < T) *reinterpret_cast<uint4*>(zp) = v;
                     zp += 16 * D;
                     __syncwarp();
                                 };
-                if (n == SPS) {
+                if (full_stage(si)) {
 #pragma unroll
-                    for (int i = 0; i < SPS; ++i) step(i);
+                    for (int i = 0; i < SPS; ++i) step(i, false);
                 } else {
-                    for (int i = 0; i < n; ++i) step(i);
+                    for (int i = 0; i < n; ++i) step(i, true);
                 }
                 __syncwarp();
                 // Q, K, the scores and the error operands of this stage are consumed; the chain
@@ -413,22 +437,28 @@ linear_prefill_mma_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_
 
 // ---------------------------------------------------------------- host side
 
-template <int D, int CG, int NST, int SPS, int NX, bool SINGLE, bool HIST = false>
-cudaError_t launch_cfg(const LinearArgs& a, cudaStream_t s, int* status) {
+template <int D, int CG, int NST, int SPS, int NX, bool SINGLE, bool HIST, bool PART>
+cudaError_t launch_part(const LinearArgs& a, cudaStream_t s, int* status) {
     using C = Cfg<D, CG, NST, SPS, NX>;
-    const uint64_t rows = uint64_t(a.B) * a.H * a.T;
+    const uint64_t heads = uint64_t(a.B) * a.H;
     CUtensorMap mq, mk, mv;
     cudaError_t e;
-    if ((e = make_tma_map_bf16(&mq, a.Q, rows, D)) != cudaSuccess) return e;
-    if ((e = make_tma_map_bf16(&mk, a.K, rows, D)) != cudaSuccess) return e;
-    if ((e = make_tma_map_bf16(&mv, a.V, rows, D)) != cudaSuccess) return e;
-    auto kern = linear_prefill_mma_kernel<D, CG, NST, SPS, NX, SINGLE, HIST>;
+    if ((e = make_tma_map_bf16_heads(&mq, a.Q, heads, a.T, D)) != cudaSuccess) return e;
+    if ((e = make_tma_map_bf16_heads(&mk, a.K, heads, a.T, D)) != cudaSuccess) return e;
+    if ((e = make_tma_map_bf16_heads(&mv, a.V, heads, a.T, D)) != cudaSuccess) return e;
+    auto kern = linear_prefill_mma_kernel<D, CG, NST, SPS, NX, SINGLE, HIST, PART>;
     const int bytes = C::BYTES + 1024;  // + alignment slack
     if ((e = allow_dynamic_smem(reinterpret_cast<const void*>(kern), bytes)) != cudaSuccess) return e;
     dim3 grid(unsigned(a.B) * unsigned(a.H), D / 16 / CG);
     kern<<<grid, C::THREADS, bytes, s>>>(mq, mk, mv, a.eta, a.W0, static_cast<__nv_bfloat16*>(a.Z), a.W_out, a.T,
                                          a.chunk, status, static_cast<__nv_bfloat16*>(a.W_hist));
     return cudaGetLastError();
+}
+
+template <int D, int CG, int NST, int SPS, int NX, bool SINGLE, bool HIST = false>
+cudaError_t launch_cfg(const LinearArgs& a, cudaStream_t s, int* status) {
+    if (a.T % 16) return launch_part<D, CG, NST, SPS, NX, SINGLE, HIST, true>(a, s, status);
+    return launch_part<D, CG, NST, SPS, NX, SINGLE, HIST, false>(a, s, status);
 }
 
 // Each mbarrier wait costs the waiting warp ~230 cycles on B300 even when the phase has
@@ -446,9 +476,10 @@ cudaError_t launch_chunk(const LinearArgs& a, cudaStream_t s, int* status) {
 }  // namespace
 
 cudaError_t launch_linear_prefill_mma(const LinearArgs& a, cudaStream_t s, int* status) {
-    // a ragged last block (chunk does not divide T) of whole 16-token sub-blocks is fewer sub-blocks
-    if (!a.bf16 || (a.d != 64 && a.d != 128) || a.chunk % 16 != 0 || a.T % 16 != 0) return cudaErrorNotSupported;
-    if (uint64_t(a.B) * a.H * a.T > 0x7fffffffull) return cudaErrorNotSupported;  // TMA row coordinate is int32
+    // any T: a ragged last block is fewer sub-blocks, and a partial last sub-block weighs its tokens
+    // past T by zero
+    if (!a.bf16 || (a.d != 64 && a.d != 128) || a.chunk % 16 != 0) return cudaErrorNotSupported;
+    if (uint64_t(a.B) * a.H > 0x7fffffffull) return cudaErrorNotSupported;  // TMA head coordinate is int32
     int dev = 0, sms = 148;
     if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     const long long bh = (long long)a.B * a.H;

@@ -112,8 +112,8 @@ ttt_status ttt_linear_prefill(const void* Q, const void* K, const void* V, const
     int* status = nullptr;
     cudaError_t e = status_ptr(&status);
     if (e != cudaSuccess) return cuda_fail(e, "ttt_linear_prefill status word");
-    // bf16, 16 | chunk: the fused warp-MMA kernel at d = 64 (any T), the split warp-MMA kernel
-    // at d = 128 (16 | T); the generic kernel otherwise.  TTT_LINEAR_PREFILL_KERNEL = "fused", "tc", "mma"
+    // bf16, 16 | chunk, any T: the fused warp-MMA kernel at d = 64, the split warp-MMA kernel at
+    // d = 128; the generic kernel otherwise.  TTT_LINEAR_PREFILL_KERNEL = "fused", "tc", "mma"
     // or "generic" makes the dispatch start at that kernel (the next one takes the shapes it does
     // not cover); "tc" is the kernel with the read-out on tcgen05.
     const int first = kernel_choice("TTT_LINEAR_PREFILL_KERNEL", "fused", "tc", "mma");
@@ -326,8 +326,8 @@ ttt_status ttt_linear_prefill_hist(const void* Q, const void* K, const void* V, 
     CHECK_PTR(W_hist);
     ttt::LinearArgs a{Q, K, V, eta, W0, Z, W_out, B, H, T, d, chunk, dtype == TTT_BF16 ? 1 : 0};
     a.W_hist = W_hist;
-    // the warp-MMA kernels record the block-start states for bf16, chunk 16, d = 64 (the fused
-    // kernel, any T) or d = 128 (16 | T); the generic kernel for every other shape
+    // the warp-MMA kernels record the block-start states for bf16, chunk 16, any T, d = 64 (the
+    // fused kernel) or d = 128 (the split kernel); the generic kernel for every other shape
     int* status = nullptr;
     cudaError_t e = status_ptr(&status);
     if (e != cudaSuccess) return cuda_fail(e, "ttt_linear_prefill_hist status word");

@@ -167,16 +167,17 @@ def test_recorded_states_headline_all_heads():
         assert rel_err(Wh[:, :, n], Wn) <= TOL["bf16"], n
 
 
+@pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("T_", [23, 205])
-def test_recorded_states_partial_last_sub_block(T_):
-    # bf16, d = 64, chunk 16, T not a multiple of 16: the fused forward records ceil(T / 16) states;
+def test_recorded_states_partial_last_sub_block(d, T_):
+    # bf16, chunk 16, T not a multiple of 16: the tensor-core forward records ceil(T / 16) states;
     # the gradients through them (SIMT backward) match the oracle
-    x = WL.linear_inputs(2, 2, T_, 64, seed=930 + T_, dtype="bf16", w_std=0.05)
-    g = WL.backward_inputs(2, 2, T_, 64, seed=931 + T_, dtype="bf16")
+    x = WL.linear_inputs(2, 2, T_, d, seed=930 + T_ + d, dtype="bf16", w_std=0.05)
+    g = WL.backward_inputs(2, 2, T_, d, seed=931 + T_ + d, dtype="bf16")
     Z, W, Wh, grads = _run(x, g, 16)
     r = f64(x)
     Zr, Wr = O.linear_dual(r["Q"], r["K"], r["V"], r["eta"], r["W0"], 16)
-    assert Wh.shape == (2, 2, (T_ + 15) // 16, 64, 64)
+    assert Wh.shape == (2, 2, (T_ + 15) // 16, d, d)
     assert rel_err(Z, Zr) <= TOL["bf16"] and rel_err(W, Wr) <= TOL["bf16"]
     for n in range(1, Wh.shape[2]):
         cut = {k: (v[:, :, :16 * n] if k != "W0" else v) for k, v in r.items()}

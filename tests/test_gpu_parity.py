@@ -412,14 +412,16 @@ def test_linear_tensor_core_kernels_ragged_last_block(d, kernel, B, H, T_, chunk
     assert rel_err(W, Wr) <= TOL["bf16"]
 
 
-# bf16, d = 64, T not a multiple of 16: the fused kernel runs a partial last sub-block (its eta from
+# bf16, T not a multiple of 16: the tensor-core kernels run a partial last sub-block (its eta from
 # global memory, read only where the tokens exist; with 4 not dividing T every sub-block's eta comes
-# from there); T = 260 / 261 leave the last stage of 256 tokens holding only the partial sub-block
-@pytest.mark.parametrize("T_", [1, 7, 17, 203, 212, 260, 261, 2047])
+# from there).  T = 260 / 261 leave the fused kernel's last stage of 256 tokens holding only the
+# partial sub-block; T = 67 / 68 do the same for the split kernel's stages of 64 tokens at d = 128.
+@pytest.mark.parametrize("d,kernel", [(64, "fused"), (64, "mma"), (128, "mma")])
+@pytest.mark.parametrize("T_", [1, 7, 17, 67, 68, 203, 212, 260, 261, 2047])
 @pytest.mark.parametrize("chunk", [16, 64])
-def test_fused_partial_last_sub_block(T_, chunk):
-    x = WL.linear_inputs(2, 3, T_, 64, seed=950 + T_ + chunk, dtype="bf16")
-    with linear_kernel("fused"):
+def test_tensor_core_partial_last_sub_block(d, kernel, T_, chunk):
+    x = WL.linear_inputs(2, 3, T_, d, seed=950 + T_ + chunk + d, dtype="bf16")
+    with linear_kernel(kernel):
         Z, W = run_linear(x, chunk)
     r = f64(x)
     Zr, Wr = O.linear_dual(r["Q"], r["K"], r["V"], r["eta"], r["W0"], chunk)
@@ -427,13 +429,14 @@ def test_fused_partial_last_sub_block(T_, chunk):
     assert rel_err(W, Wr) <= TOL["bf16"]
 
 
-def test_fused_partial_sub_block_reads_no_rows_of_the_next_head():
+@pytest.mark.parametrize("d,kernel", [(64, "fused"), (128, "mma")])
+def test_partial_sub_block_reads_no_rows_of_the_next_head(d, kernel):
     # head 1 holds values whose products overflow; head 0 (T = 23: a partial second sub-block) must
     # not see them, since the tokens past its end read as zeros rather than as head 1's rows
-    x = WL.linear_inputs(1, 2, 23, 64, seed=977, dtype="bf16")
+    x = WL.linear_inputs(1, 2, 23, d, seed=977, dtype="bf16")
     for k in ("Q", "K", "V"):
         x[k][:, 1] = 3.0e38
-    with linear_kernel("fused"):
+    with linear_kernel(kernel):
         Z, W = run_linear(x, 16)
     r = f64({k: v[:, :1] for k, v in x.items()})
     Zr, Wr = O.linear_dual(r["Q"], r["K"], r["V"], r["eta"], r["W0"], 16)
