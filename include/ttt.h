@@ -273,6 +273,11 @@ ttt_status ttt_linear_prefill_backward(const void* Q, const void* K, const void*
  *   d in {16, 32, 64}; hidden a multiple of 16 with d*hidden <= 16384;
  *   chunk 1..64 with chunk*hidden <= 4096 (last block may be shorter).
  *
+ * Kernels: bf16 with d = 64, hidden = 256 and chunk 16 runs on warp-level
+ * tensor-core MMAs for any T (a partial last block weighs its tokens past T by
+ * zero); other shapes on a SIMT kernel.  TTT_MLP_PREFILL_KERNEL = "tc" selects
+ * the tcgen05 form for that shape when 16 | T.
+ *
  * Source: "Test-Time Training (TTT) Layers for Sequence Modeling", section
  * "Variants: TTT-Linear vs. TTT-MLP" (two-layer MLP inner model); loss, step
  * and readout as for TTT-Linear.

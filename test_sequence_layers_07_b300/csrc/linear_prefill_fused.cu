@@ -90,7 +90,11 @@ struct FusedCfg {
 // HIST: also write the state at the start of every block to W_hist [B*H][ceil(T/16)][D][D], as bf16
 // (the operand the products use, and what the backward reads); instantiated for blocks of 16
 // tokens only.
-template <int D, int CG, int NST, int SPS, bool SINGLE, bool HIST>
+// PART: T is not a multiple of 16 (a partial last sub-block), or the rows of all heads exceed the int32
+// coordinate of a 2D tensor map.  Then Q/K/V come through per-head 3D maps (tokens past a head's end
+// read as zeros), eta by cp.async where a bulk copy cannot take it, and the rows of Z past T are not
+// stored; the instantiation for the common case compiles none of that.
+template <int D, int CG, int NST, int SPS, bool SINGLE, bool HIST, bool PART>
 __global__ void __launch_bounds__(FusedCfg<D, CG, NST, SPS>::THREADS, 1)
 linear_prefill_fused_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                             const __grid_constant__ CUtensorMap tmV, const float* __restrict__ eta,
@@ -109,10 +113,10 @@ linear_prefill_fused_kernel(const __grid_constant__ CUtensorMap tmQ, const __gri
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const size_t bh = blockIdx.x;
-    const int nsb = (T + 15) / 16;           // 16-token sub-blocks (the last may be partial)
+    const int nsb = PART ? (T + 15) / 16 : T / 16;  // 16-token sub-blocks (with PART the last may be partial)
     const int nstg = (nsb + SPS - 1) / SPS;  // stages
     const int nsub = chunk / 16;             // sub-blocks per block
-    const bool ebulk = (T & 3) == 0;         // a head's eta starts 16-byte aligned
+    const bool ebulk = (T & 3) == 0;         // a head's eta starts 16-byte aligned (PART)
     const uint32_t sbase = smem_u32(smem);
     const int g = lane >> 2, t = lane & 3;
     const int lj = lane >> 3, lr = lane & 7;
@@ -155,23 +159,46 @@ linear_prefill_fused_kernel(const __grid_constant__ CUtensorMap tmQ, const __gri
                 const int s = si % NST, n = subs_in(si);
                 if (si >= NST && !wait(empty_bar[s], ((si / NST) - 1) & 1)) break;
                 const uint32_t fb = smem_u32(&full_bar[s]);
-                // eta of the stage's whole sub-blocks when the head's eta starts on a 16-byte
-                // boundary (4 | T); a partial last sub-block, or every one when 4 does not divide T,
-                // reads its eta from global memory instead.  Q/K/V boxes past the head's T read zeros.
-                const int tok = min(16 * n, T - 16 * si * SPS);
-                const uint32_t ebytes = ebulk ? uint32_t(tok * 4) & ~63u : 0u;
-                mbar_arrive_expect_tx(fb, uint32_t(n) * 3 * C::TILE + ebytes);
                 const uint32_t st = sbase + s * C::STAGE;
-                for (int i = 0; i < n; ++i) {
-                    const int y = 16 * (si * SPS + i), z = int(bh);
-#pragma unroll
-                    for (int box = 0; box < D / 64; ++box) {
-                        tma_load_3d(st + C::QOFF + i * C::TILE + box * 2048, &tmQ, 64 * box, y, z, fb);
-                        tma_load_3d(st + C::KOFF + i * C::TILE + box * 2048, &tmK, 64 * box, y, z, fb);
-                        tma_load_3d(st + C::VOFF + i * C::TILE + box * 2048, &tmV, 64 * box, y, z, fb);
+                if constexpr (PART) {
+                    // eta: one bulk copy when every token of the stage exists and a head's eta starts
+                    // on a 16-byte boundary (4 | T); otherwise 4-byte cp.async copies that the
+                    // stage's mbarrier tracks, and zeros past T
+                    const int tok = min(16 * n, T - 16 * si * SPS);
+                    const bool eb = ebulk && tok == 16 * n;
+                    if (!eb) {
+                        const float* eg = eta + bh * T + 16 * si * SPS;
+                        float* es = reinterpret_cast<float*>(smem + s * C::STAGE + C::EOFF);
+                        for (int j = 0; j < 16 * n; ++j) {
+                            if (j < tok) cp_async4(st + C::EOFF + 4 * j, eg + j);
+                            else es[j] = 0.f;
+                        }
+                        cp_async_mbar_arrive(fb);  // before this thread's own arrive on the phase
                     }
+                    mbar_arrive_expect_tx(fb, uint32_t(n) * 3 * C::TILE + (eb ? uint32_t(n) * 64 : 0u));
+                    for (int i = 0; i < n; ++i) {
+                        const int y = 16 * (si * SPS + i), z = int(bh);
+#pragma unroll
+                        for (int box = 0; box < D / 64; ++box) {
+                            tma_load_3d(st + C::QOFF + i * C::TILE + box * 2048, &tmQ, 64 * box, y, z, fb);
+                            tma_load_3d(st + C::KOFF + i * C::TILE + box * 2048, &tmK, 64 * box, y, z, fb);
+                            tma_load_3d(st + C::VOFF + i * C::TILE + box * 2048, &tmV, 64 * box, y, z, fb);
+                        }
+                    }
+                    if (eb) bulk_load(st + C::EOFF, eta + bh * T + 16 * si * SPS, uint32_t(n) * 64, fb);
+                } else {
+                    mbar_arrive_expect_tx(fb, uint32_t(n) * (3 * C::TILE + 64));
+                    for (int i = 0; i < n; ++i) {
+                        const int y = int(bh * T) + 16 * (si * SPS + i);
+#pragma unroll
+                        for (int box = 0; box < D / 64; ++box) {
+                            tma_load_2d(st + C::QOFF + i * C::TILE + box * 2048, &tmQ, 64 * box, y, fb);
+                            tma_load_2d(st + C::KOFF + i * C::TILE + box * 2048, &tmK, 64 * box, y, fb);
+                            tma_load_2d(st + C::VOFF + i * C::TILE + box * 2048, &tmV, 64 * box, y, fb);
+                        }
+                    }
+                    bulk_load(st + C::EOFF, eta + bh * T + 16 * si * SPS, uint32_t(n) * 64, fb);
                 }
-                if (ebytes) bulk_load(st + C::EOFF, eta + bh * T + 16 * si * SPS, ebytes, fb);
                 ++issued;
             }
             // never retire the CTA with copies in flight (this wait ignores the abort flag)
@@ -211,9 +238,7 @@ linear_prefill_fused_kernel(const __grid_constant__ CUtensorMap tmQ, const __gri
         uint32_t kb[2][KS][4], qa[2][KS][4], kt[KS][4];
         float ne[2][4], nv[2][8];  // -eta of the sub-block's tokens, eta . V in the P^T layout
 
-        // chk: the sub-block may be partial or its eta may not be staged (a constant false on the
-        // stages that hold neither, so their unrolled loop body keeps no branches)
-        auto load_kq = [&](int buf, uint32_t st, int i, int sb, bool chk) {
+        auto load_kq = [&](int buf, uint32_t st, int i) {
             const uint32_t k0 = st + C::KOFF + i * C::TILE, q0 = st + C::QOFF + i * C::TILE;
 #pragma unroll
             for (int ks = 0; ks < KS; ++ks) ldsm_x4(k0 + off_nk[ks], kb[buf][ks]);
@@ -221,17 +246,9 @@ linear_prefill_fused_kernel(const __grid_constant__ CUtensorMap tmQ, const __gri
             for (int ks = 0; ks < KS; ++ks) ldsm_x4(q0 + off_tk[ks], qa[buf][ks]);
             uint32_t vv[4];
             ldsm_x4_trans(st + C::VOFF + i * C::TILE + off_v, vv);
-            float2 e01, e23;
-            if (!chk || (ebulk && 16 * sb + 16 <= T)) {
-                const float* es = reinterpret_cast<const float*>(smem + (st - sbase) + C::EOFF + i * 64);
-                e01 = *reinterpret_cast<const float2*>(es + 2 * t);
-                e23 = *reinterpret_cast<const float2*>(es + 8 + 2 * t);
-            } else {  // eta from global memory; tokens past T weigh zero
-                const float* eg = eta + bh * T;
-                const int j = 16 * sb + 2 * t;
-                e01 = make_float2(j < T ? eg[j] : 0.f, j + 1 < T ? eg[j + 1] : 0.f);
-                e23 = make_float2(j + 8 < T ? eg[j + 8] : 0.f, j + 9 < T ? eg[j + 9] : 0.f);
-            }
+            const float* es = reinterpret_cast<const float*>(smem + (st - sbase) + C::EOFF + i * 64);
+            const float2 e01 = *reinterpret_cast<const float2*>(es + 2 * t);  // zero past T
+            const float2 e23 = *reinterpret_cast<const float2*>(es + 8 + 2 * t);
             ne[buf][0] = -e01.x; ne[buf][1] = -e01.y; ne[buf][2] = -e23.x; ne[buf][3] = -e23.y;
             nv[buf][0] = e01.x * bf16_lo(vv[0]); nv[buf][1] = e01.y * bf16_hi(vv[0]);
             nv[buf][2] = e01.x * bf16_lo(vv[1]); nv[buf][3] = e01.y * bf16_hi(vv[1]);
@@ -250,14 +267,11 @@ linear_prefill_fused_kernel(const __grid_constant__ CUtensorMap tmQ, const __gri
         // chk: rows past T are not stored (only the last sub-block can be partial)
         auto store_z = [&](int sb, bool chk) {
             __nv_bfloat16* zr = zb + size_t(16 * sb + g) * D;  // rows 16 sb + g (+8), columns cw0 + 2t (+8)
-            if (!chk || 16 * sb + g < T) {
-                *reinterpret_cast<uint32_t*>(zr) = pack_bf16(zp[0][0], zp[0][1]);
-                *reinterpret_cast<uint32_t*>(zr + 8) = pack_bf16(zp[1][0], zp[1][1]);
-            }
-            if (!chk || 16 * sb + g + 8 < T) {
-                *reinterpret_cast<uint32_t*>(zr + 8 * D) = pack_bf16(zp[0][2], zp[0][3]);
-                *reinterpret_cast<uint32_t*>(zr + 8 * D + 8) = pack_bf16(zp[1][2], zp[1][3]);
-            }
+            const bool lo = !chk || 16 * sb + g < T, hi = !chk || 16 * sb + g + 8 < T;
+            if (lo) *reinterpret_cast<uint32_t*>(zr) = pack_bf16(zp[0][0], zp[0][1]);
+            if (hi) *reinterpret_cast<uint32_t*>(zr + 8 * D) = pack_bf16(zp[0][2], zp[0][3]);
+            if (lo) *reinterpret_cast<uint32_t*>(zr + 8) = pack_bf16(zp[1][0], zp[1][1]);
+            if (hi) *reinterpret_cast<uint32_t*>(zr + 8 * D + 8) = pack_bf16(zp[1][2], zp[1][3]);
         };
 
         bool ok = true;
@@ -293,17 +307,15 @@ linear_prefill_fused_kernel(const __grid_constant__ CUtensorMap tmQ, const __gri
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&sc_bar[s]));
-            // a full stage of whole sub-blocks with staged eta runs without the checks
-            const bool full = n == SPS && ebulk && 16 * SPS * (si + 1) <= T;
-            load_kq(0, st, 0, si * SPS, !full);
+            load_kq(0, st, 0);
             load_kt(st, 0);
             if (!(ok = wait_all(sc_bar[s], par))) break;
             // one 16-token sub-block; n is a compile-time SPS on full stages, so their loop body
             // has no branches and the compiler schedules across sub-blocks
-            auto step = [&](const int i, const int n, const bool chk) {
+            auto step = [&](const int i, const int n) {
                 const int b = i & 1, sb = si * SPS + i;
                 if (i > 0) load_kt(st, i);  // used by the update, well after K W and Q W
-                if (i + 1 < n) load_kq(b ^ 1, st, i + 1, sb + 1, chk);
+                if (i + 1 < n) load_kq(b ^ 1, st, i + 1);
                 const uint4 sf4 = *reinterpret_cast<const uint4*>(sc + i * 512 + lane * 16);
                 const bool bstart = SINGLE || sb % nsub == 0;
                 if (bstart) {
@@ -390,17 +402,17 @@ linear_prefill_fused_kernel(const __grid_constant__ CUtensorMap tmQ, const __gri
                 mma_bf16_16816(zp[0], sf, ga[0], ga[2]);
                 mma_bf16_16816(zp[1], sf, ga[1], ga[3]);
             };
-            if (full) {
+            if (n == SPS) {
 #pragma unroll
-                for (int i = 0; i < SPS; ++i) step(i, SPS, false);
+                for (int i = 0; i < SPS; ++i) step(i, SPS);
             } else {
 #pragma unroll
                 for (int i = 0; i < SPS; ++i) {
                     if (i >= n) break;
-                    step(i, n, true);
+                    step(i, n);
                 }
             }
-            store_z(si * SPS + n - 1, true);
+            store_z(si * SPS + n - 1, PART);  // the last sub-block of the head may be partial
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&empty_bar[s]));  // this warp's reads of the stage are done
         }
@@ -422,25 +434,39 @@ linear_prefill_fused_kernel(const __grid_constant__ CUtensorMap tmQ, const __gri
 
 // ---------------------------------------------------------------- host side
 
-template <int D, int CG, int NST, int SPS, bool SINGLE, bool HIST>
-cudaError_t launch_cfg(const LinearArgs& a, cudaStream_t s, int* status) {
+template <int D, int CG, int NST, int SPS, bool SINGLE, bool HIST, bool PART>
+cudaError_t launch_part(const LinearArgs& a, cudaStream_t s, int* status) {
     using C = FusedCfg<D, CG, NST, SPS>;
     const uint64_t heads = uint64_t(a.B) * a.H;
     CUtensorMap mq, mk, mv, mh;
     cudaError_t e;
-    if ((e = make_tma_map_bf16_heads(&mq, a.Q, heads, a.T, D)) != cudaSuccess) return e;
-    if ((e = make_tma_map_bf16_heads(&mk, a.K, heads, a.T, D)) != cudaSuccess) return e;
-    if ((e = make_tma_map_bf16_heads(&mv, a.V, heads, a.T, D)) != cudaSuccess) return e;
+    if (PART) {  // [heads][T][D]: the boxes of a partial sub-block read zeros past T
+        if ((e = make_tma_map_bf16_heads(&mq, a.Q, heads, a.T, D)) != cudaSuccess) return e;
+        if ((e = make_tma_map_bf16_heads(&mk, a.K, heads, a.T, D)) != cudaSuccess) return e;
+        if ((e = make_tma_map_bf16_heads(&mv, a.V, heads, a.T, D)) != cudaSuccess) return e;
+    } else {  // [heads * T][D]
+        if ((e = make_tma_map_bf16(&mq, a.Q, heads * a.T, D)) != cudaSuccess) return e;
+        if ((e = make_tma_map_bf16(&mk, a.K, heads * a.T, D)) != cudaSuccess) return e;
+        if ((e = make_tma_map_bf16(&mv, a.V, heads * a.T, D)) != cudaSuccess) return e;
+    }
     memset(&mh, 0, sizeof(mh));  // unused without the recorded states
     if (HIST && (e = make_tma_map_bf16_box(&mh, a.W_hist, heads * ((a.T + 15) / 16) * D, D, 16, 64, 0)) != cudaSuccess)
         return e;
-    auto kern = linear_prefill_fused_kernel<D, CG, NST, SPS, SINGLE, HIST>;
+    auto kern = linear_prefill_fused_kernel<D, CG, NST, SPS, SINGLE, HIST, PART>;
     const int bytes = C::BYTES + 1024;  // + alignment slack
     if ((e = allow_dynamic_smem(reinterpret_cast<const void*>(kern), bytes)) != cudaSuccess) return e;
     dim3 grid(unsigned(a.B) * unsigned(a.H), D / 16 / CG);
     kern<<<grid, C::THREADS, bytes, s>>>(mq, mk, mv, a.eta, a.W0, static_cast<__nv_bfloat16*>(a.Z), a.W_out, a.T,
                                          a.chunk, status, mh, a.wait_ns ? a.wait_ns : kWaitLimitNs);
     return cudaGetLastError();
+}
+
+template <int D, int CG, int NST, int SPS, bool SINGLE, bool HIST>
+cudaError_t launch_cfg(const LinearArgs& a, cudaStream_t s, int* status) {
+    // the 2D maps address rows bh * T + t with an int32 coordinate
+    if (a.T % 16 || uint64_t(a.B) * a.H * a.T > 0x7fffffffull)
+        return launch_part<D, CG, NST, SPS, SINGLE, HIST, true>(a, s, status);
+    return launch_part<D, CG, NST, SPS, SINGLE, HIST, false>(a, s, status);
 }
 
 // stages of 256 tokens, double-buffered: 2 x 97 KB of Q/K/V/eta + 16 KB of scores + 8 KB of state

@@ -90,8 +90,10 @@ struct Cfg {
 
 // HIST: also write the state at the start of every block to W_hist [B*H][ceil(T/16)][D][D], rounded
 // to bf16 (what the backward reads); instantiated for blocks of 16 tokens only.
-// PART: T is not a multiple of 16 (a partial last sub-block); the instantiation for 16 | T compiles
-// none of the checks that case needs.
+// PART: T is not a multiple of 16 (a partial last sub-block), or the rows of all heads exceed the int32
+// coordinate of a 2D tensor map.  Then Q/K/V come through per-head 3D maps (tokens past a head's end
+// read as zeros), eta by cp.async where a bulk copy cannot take it, and the rows of Z past T are not
+// stored; the instantiation for the common case compiles none of that.
 template <int D, int CG, int NST, int SPS, int NX, bool SINGLE, bool HIST, bool PART>
 __global__ void __launch_bounds__(Cfg<D, CG, NST, SPS, NX>::THREADS, 1)
 linear_prefill_mma_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -112,10 +114,10 @@ linear_prefill_mma_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const size_t bh = blockIdx.x;
-    const int nsb = (T + 15) / 16;             // 16-token sub-blocks (the last may be partial)
+    const int nsb = PART ? (T + 15) / 16 : T / 16;  // 16-token sub-blocks (with PART the last may be partial)
     const int nstg = (nsb + SPS - 1) / SPS;    // stages
     const int nsub = chunk / 16;               // sub-blocks per block
-    const bool ebulk = !PART || (T & 3) == 0;  // a head's eta starts 16-byte aligned
+    const bool ebulk = (T & 3) == 0;           // a head's eta starts 16-byte aligned (PART)
     const uint32_t sbase = smem_u32(smem);
     const int g = lane >> 2, t = lane & 3;
     const int lj = lane >> 3, lr = lane & 7;
@@ -148,11 +150,8 @@ linear_prefill_mma_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_
         return __all_sync(0xffffffffu, wait(bar, parity));
     };
     auto subs_in = [&](int si) { return nsb - si * SPS < SPS ? nsb - si * SPS : SPS; };
-    // a stage of SPS whole sub-blocks with its eta staged: its loops run without the checks for a
-    // partial sub-block
-    auto full_stage = [&](int si) {
-        return subs_in(si) == SPS && (!PART || (ebulk && 16 * SPS * (si + 1) <= T));
-    };
+    // a stage of SPS whole sub-blocks: its loops run without the checks for a partial sub-block
+    auto full_stage = [&](int si) { return subs_in(si) == SPS && (!PART || 16 * SPS * (si + 1) <= T); };
 
     // lane-dependent ldmatrix coordinates (byte offsets inside a sub-tile)
     uint32_t off_nk[KS], off_tk[NT / 2];
@@ -172,23 +171,46 @@ linear_prefill_mma_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_
                 const int s = si % NST, n = subs_in(si);
                 if (si >= NST && !wait(empty_bar[s], ((si / NST) - 1) & 1)) break;
                 const uint32_t fb = smem_u32(&full_bar[s]);
-                // eta of the stage's whole sub-blocks when a head's eta starts on a 16-byte boundary
-                // (4 | T); otherwise, and for a partial last sub-block, the chain reads eta from global
-                // memory.  Q/K/V boxes past the head's T read zeros.
-                const int tok = min(16 * n, T - 16 * si * SPS);
-                const uint32_t ebytes = ebulk ? uint32_t(tok * 4) & ~63u : 0u;
-                mbar_arrive_expect_tx(fb, uint32_t(n) * 3 * C::TILE + ebytes);
                 const uint32_t st = sbase + s * C::STAGE;
-                for (int i = 0; i < n; ++i) {
-                    const int y = 16 * (si * SPS + i), z = int(bh);
-#pragma unroll
-                    for (int box = 0; box < D / 64; ++box) {
-                        tma_load_3d(st + C::QOFF + i * C::TILE + box * 2048, &tmQ, 64 * box, y, z, fb);
-                        tma_load_3d(st + C::KOFF + i * C::TILE + box * 2048, &tmK, 64 * box, y, z, fb);
-                        tma_load_3d(st + C::VOFF + i * C::TILE + box * 2048, &tmV, 64 * box, y, z, fb);
+                if constexpr (PART) {
+                    // eta: one bulk copy when every token of the stage exists and a head's eta starts
+                    // on a 16-byte boundary (4 | T); otherwise 4-byte cp.async copies that the
+                    // stage's mbarrier tracks, and zeros past T.  Q/K/V boxes past T read zeros.
+                    const int tok = min(16 * n, T - 16 * si * SPS);
+                    const bool eb = ebulk && tok == 16 * n;
+                    if (!eb) {
+                        const float* eg = eta + bh * T + 16 * si * SPS;
+                        float* es = reinterpret_cast<float*>(smem + s * C::STAGE + C::EOFF);
+                        for (int j = 0; j < 16 * n; ++j) {
+                            if (j < tok) cp_async4(st + C::EOFF + 4 * j, eg + j);
+                            else es[j] = 0.f;
+                        }
+                        cp_async_mbar_arrive(fb);  // before this thread's own arrive on the phase
                     }
+                    mbar_arrive_expect_tx(fb, uint32_t(n) * 3 * C::TILE + (eb ? uint32_t(n) * 64 : 0u));
+                    for (int i = 0; i < n; ++i) {
+                        const int y = 16 * (si * SPS + i), z = int(bh);
+#pragma unroll
+                        for (int box = 0; box < D / 64; ++box) {
+                            tma_load_3d(st + C::QOFF + i * C::TILE + box * 2048, &tmQ, 64 * box, y, z, fb);
+                            tma_load_3d(st + C::KOFF + i * C::TILE + box * 2048, &tmK, 64 * box, y, z, fb);
+                            tma_load_3d(st + C::VOFF + i * C::TILE + box * 2048, &tmV, 64 * box, y, z, fb);
+                        }
+                    }
+                    if (eb) bulk_load(st + C::EOFF, eta + bh * T + 16 * si * SPS, uint32_t(n) * 64, fb);
+                } else {
+                    mbar_arrive_expect_tx(fb, uint32_t(n) * (3 * C::TILE + 64));
+                    for (int i = 0; i < n; ++i) {
+                        const int y = int(bh * T) + 16 * (si * SPS + i);
+#pragma unroll
+                        for (int box = 0; box < D / 64; ++box) {
+                            tma_load_2d(st + C::QOFF + i * C::TILE + box * 2048, &tmQ, 64 * box, y, fb);
+                            tma_load_2d(st + C::KOFF + i * C::TILE + box * 2048, &tmK, 64 * box, y, fb);
+                            tma_load_2d(st + C::VOFF + i * C::TILE + box * 2048, &tmV, 64 * box, y, fb);
+                        }
+                    }
+                    bulk_load(st + C::EOFF, eta + bh * T + 16 * si * SPS, uint32_t(n) * 64, fb);
                 }
-                if (ebytes) bulk_load(st + C::EOFF, eta + bh * T + 16 * si * SPS, ebytes, fb);
                 ++issued;
             }
             // never retire the CTA with copies in flight (this wait ignores the abort flag)
@@ -259,26 +281,16 @@ linear_prefill_mma_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_
             uint32_t wa0[KS][4];
             uint32_t kb[KS][4], kt[NT / 2][4];
             float ne0 = 0, ne1 = 0, ne2 = 0, ne3 = 0, nv[8] = {};
-            // sub-block i of the stage at st (sb in the head); chk: it may be partial or its eta may
-            // not be staged (a constant false on full stages)
-            auto load = [&](uint32_t st, int i, int sb, bool chk) {
+            auto load = [&](uint32_t st, int i) {
 #pragma unroll
                 for (int ks = 0; ks < KS; ++ks) ldsm_x4(st + C::KOFF + i * C::TILE + off_nk[ks], kb[ks]);
 #pragma unroll
                 for (int kk = 0; kk < NT / 2; ++kk) ldsm_x4_trans(st + C::KOFF + i * C::TILE + off_tk[kk], kt[kk]);
                 uint32_t vv[4];
                 ldsm_x4_trans(st + C::VOFF + i * C::TILE + off_v, vv);
-                float2 e01, e23;
-                if (!PART || !chk || (ebulk && 16 * sb + 16 <= T)) {
-                    const float* es = reinterpret_cast<const float*>(smem + (st - sbase) + C::EOFF + i * 64);
-                    e01 = *reinterpret_cast<const float2*>(es + 2 * t);
-                    e23 = *reinterpret_cast<const float2*>(es + 8 + 2 * t);
-                } else {  // eta from global memory; tokens past T weigh zero
-                    const float* eg = eta + bh * T;
-                    const int j = 16 * sb + 2 * t;
-                    e01 = make_float2(j < T ? eg[j] : 0.f, j + 1 < T ? eg[j + 1] : 0.f);
-                    e23 = make_float2(j + 8 < T ? eg[j + 8] : 0.f, j + 9 < T ? eg[j + 9] : 0.f);
-                }
+                const float* es = reinterpret_cast<const float*>(smem + (st - sbase) + C::EOFF + i * 64);
+                const float2 e01 = *reinterpret_cast<const float2*>(es + 2 * t);  // zero past T
+                const float2 e23 = *reinterpret_cast<const float2*>(es + 8 + 2 * t);
                 ne0 = -e01.x; ne1 = -e01.y; ne2 = -e23.x; ne3 = -e23.y;
                 nv[0] = e01.x * bf16_lo(vv[0]); nv[1] = e01.y * bf16_hi(vv[0]);
                 nv[2] = e01.x * bf16_lo(vv[1]); nv[3] = e01.y * bf16_hi(vv[1]);
@@ -286,7 +298,7 @@ linear_prefill_mma_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_
                 nv[6] = e23.x * bf16_lo(vv[3]); nv[7] = e23.y * bf16_hi(vv[3]);
             };
             bool ok = wait_all(full_bar[0], 0);
-            if (ok) load(sbase, 0, 0, !full_stage(0));
+            if (ok) load(sbase, 0);
             for (int si = 0; ok && si < nstg; ++si) {
                 const int s = si % NST, n = subs_in(si), x = si % NX;
                 const uint32_t st = sbase + s * C::STAGE;
@@ -333,16 +345,16 @@ linear_prefill_mma_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_
                     }
                     *reinterpret_cast<uint4*>(gout + i * 512 + lane * 16) = make_uint4(ga[0], ga[1], ga[2], ga[3]);
                 };
-                if (full_stage(si)) {  // unrolled, so the compiler schedules across sub-blocks
+                if (n == SPS) {  // full stage: unrolled, so the compiler schedules across sub-blocks
 #pragma unroll
                     for (int i = 0; i < SPS; ++i) {
                         step(i);
-                        if (i + 1 < SPS) load(st, i + 1, si * SPS + i + 1, false);
+                        if (i + 1 < SPS) load(st, i + 1);
                     }
                 } else {
                     for (int i = 0; i < n; ++i) {
                         step(i);
-                        if (i + 1 < n) load(st, i + 1, si * SPS + i + 1, true);
+                        if (i + 1 < n) load(st, i + 1);
                     }
                 }
                 __syncwarp();
@@ -350,7 +362,7 @@ linear_prefill_mma_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_
                 if (si + 1 < nstg) {
                     const int s1 = (si + 1) % NST;
                     ok = wait_all(full_bar[s1], ((si + 1) / NST) & 1);
-                    if (ok) load(sbase + s1 * C::STAGE, 0, (si + 1) * SPS, !full_stage(si + 1));
+                    if (ok) load(sbase + s1 * C::STAGE, 0);
                 }
             }
             float* Wo = W_out + bh * D * D;
@@ -443,9 +455,15 @@ cudaError_t launch_part(const LinearArgs& a, cudaStream_t s, int* status) {
     const uint64_t heads = uint64_t(a.B) * a.H;
     CUtensorMap mq, mk, mv;
     cudaError_t e;
-    if ((e = make_tma_map_bf16_heads(&mq, a.Q, heads, a.T, D)) != cudaSuccess) return e;
-    if ((e = make_tma_map_bf16_heads(&mk, a.K, heads, a.T, D)) != cudaSuccess) return e;
-    if ((e = make_tma_map_bf16_heads(&mv, a.V, heads, a.T, D)) != cudaSuccess) return e;
+    if (PART) {  // [heads][T][D]: the boxes of a partial sub-block read zeros past T
+        if ((e = make_tma_map_bf16_heads(&mq, a.Q, heads, a.T, D)) != cudaSuccess) return e;
+        if ((e = make_tma_map_bf16_heads(&mk, a.K, heads, a.T, D)) != cudaSuccess) return e;
+        if ((e = make_tma_map_bf16_heads(&mv, a.V, heads, a.T, D)) != cudaSuccess) return e;
+    } else {  // [heads * T][D]
+        if ((e = make_tma_map_bf16(&mq, a.Q, heads * a.T, D)) != cudaSuccess) return e;
+        if ((e = make_tma_map_bf16(&mk, a.K, heads * a.T, D)) != cudaSuccess) return e;
+        if ((e = make_tma_map_bf16(&mv, a.V, heads * a.T, D)) != cudaSuccess) return e;
+    }
     auto kern = linear_prefill_mma_kernel<D, CG, NST, SPS, NX, SINGLE, HIST, PART>;
     const int bytes = C::BYTES + 1024;  // + alignment slack
     if ((e = allow_dynamic_smem(reinterpret_cast<const void*>(kern), bytes)) != cudaSuccess) return e;
@@ -457,7 +475,9 @@ cudaError_t launch_part(const LinearArgs& a, cudaStream_t s, int* status) {
 
 template <int D, int CG, int NST, int SPS, int NX, bool SINGLE, bool HIST = false>
 cudaError_t launch_cfg(const LinearArgs& a, cudaStream_t s, int* status) {
-    if (a.T % 16) return launch_part<D, CG, NST, SPS, NX, SINGLE, HIST, true>(a, s, status);
+    // the 2D maps address rows bh * T + t with an int32 coordinate
+    if (a.T % 16 || uint64_t(a.B) * a.H * a.T > 0x7fffffffull)
+        return launch_part<D, CG, NST, SPS, NX, SINGLE, HIST, true>(a, s, status);
     return launch_part<D, CG, NST, SPS, NX, SINGLE, HIST, false>(a, s, status);
 }
 

@@ -138,7 +138,11 @@ __device__ __forceinline__ float bf16_at(const uint8_t* tile, int row, int col) 
 }
 
 // HIST: also write the state at the start of every block to W1_hist / W2_hist (bf16).
-template <bool HIST>
+// PART: T is not a multiple of 16 (a partial last block), or the rows of all heads exceed the int32
+// coordinate of a 2D tensor map.  Then Q/K/V come through per-head 3D maps (tokens past a head's end
+// read as zeros), eta by cp.async where a bulk copy cannot take it, and the rows of Z past T are not
+// stored; the instantiation for the common case compiles none of that.
+template <bool HIST, bool PART>
 __global__ void __launch_bounds__(THREADS, 1)
 mlp_prefill_mma_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const float* __restrict__ eta, const float* W1_0,
@@ -153,7 +157,7 @@ mlp_prefill_mma_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_con
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const size_t bh = blockIdx.x;
-    const int nblk = T / BT;
+    const int nblk = PART ? (T + BT - 1) / BT : T / BT;  // with PART the last block may be partial
     const uint32_t sb = smem_u32(smem);
     const int g = lane >> 2, t = lane & 3;
     const int lr = lane & 7, lm = lane >> 3;  // ldmatrix: row inside a tile, tile index
@@ -191,13 +195,35 @@ mlp_prefill_mma_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_con
     auto issue = [&](int m) {  // thread 0: TMA copies of block m into slot m % NST
         const int s = m % NST;
         const uint32_t fb = smem_u32(&full_bar[s]);
-        mbar_arrive_expect_tx(fb, 3 * TILE + 64);
         const uint32_t st = sb + s * SLOT;
-        const int y = int(bh * T) + BT * m;
-        tma_load_2d(st + S_K, &tmK, 0, y, fb);
-        tma_load_2d(st + S_Q, &tmQ, 0, y, fb);
-        tma_load_2d(st + S_V, &tmV, 0, y, fb);
-        bulk_load(st + S_ETA, eta + bh * T + BT * m, 64, fb);
+        if constexpr (PART) {
+            // eta by bulk copy when the block's 16 values exist and start on a 16-byte boundary
+            // (4 | T); otherwise by 4-byte cp.async copies that the slot's mbarrier tracks, and
+            // zeros past T (every read of the slot's previous block is done by now)
+            const bool ebulk = (T & 3) == 0 && BT * (m + 1) <= T;
+            if (!ebulk) {
+                float* es = reinterpret_cast<float*>(smem + s * SLOT + S_ETA);
+                const float* eg = eta + bh * T + BT * m;
+                for (int j = 0; j < BT; ++j) {
+                    if (BT * m + j < T) cp_async4(st + S_ETA + 4 * j, eg + j);
+                    else es[j] = 0.f;
+                }
+                cp_async_mbar_arrive(fb);  // before this thread's own arrive on the phase
+            }
+            mbar_arrive_expect_tx(fb, 3 * TILE + (ebulk ? 64 : 0));
+            const int y = BT * m, z = int(bh);
+            tma_load_3d(st + S_K, &tmK, 0, y, z, fb);
+            tma_load_3d(st + S_Q, &tmQ, 0, y, z, fb);
+            tma_load_3d(st + S_V, &tmV, 0, y, z, fb);
+            if (ebulk) bulk_load(st + S_ETA, eta + bh * T + BT * m, 64, fb);
+        } else {
+            mbar_arrive_expect_tx(fb, 3 * TILE + 64);
+            const int y = int(bh * T) + BT * m;
+            tma_load_2d(st + S_K, &tmK, 0, y, fb);
+            tma_load_2d(st + S_Q, &tmQ, 0, y, fb);
+            tma_load_2d(st + S_V, &tmV, 0, y, fb);
+            bulk_load(st + S_ETA, eta + bh * T + BT * m, 64, fb);
+        }
     };
     int issued = 0;  // thread 0's count of blocks whose copies it issued
     if (threadIdx.x == 0) {
@@ -400,8 +426,8 @@ mlp_prefill_mma_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_con
                 float c[4] = {zsum.x, zsum.y, zsum.z, zsum.w};
                 mma_bf16_16816(c, sa, nb0, nb1);
                 uint32_t* zr = reinterpret_cast<uint32_t*>(Z + (bh * T + size_t(BT) * (n - 1) + g) * D + 8 * warp + 2 * t);
-                zr[0] = pack_bf16(c[0], c[1]);
-                zr[8 * D / 2] = pack_bf16(c[2], c[3]);
+                if (!PART || BT * (n - 1) + g < T) zr[0] = pack_bf16(c[0], c[1]);  // rows past T: not stored
+                if (!PART || BT * (n - 1) + g + 8 < T) zr[8 * D / 2] = pack_bf16(c[2], c[3]);
             }
             if (!have) break;
 
@@ -533,22 +559,33 @@ mlp_prefill_mma_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_con
 }  // namespace
 
 bool mlp_prefill_mma_supported(const MlpArgs& a) {
-    return a.bf16 && a.d == D && a.hidden == HID && a.chunk == BT && a.T % BT == 0 &&
-           uint64_t(a.B) * a.H * a.T <= 0x7fffffffull;  // TMA row coordinate is int32
+    // any T (a partial last block weighs its tokens past T by zero); TMA coordinates are int32: the
+    // head index, and for the recorded states the rows of W2_hist
+    const uint64_t heads = uint64_t(a.B) * a.H;
+    return a.bf16 && a.d == D && a.hidden == HID && a.chunk == BT && heads <= 0x7fffffffull &&
+           (!a.W1_hist || heads * ((uint64_t(a.T) + BT - 1) / BT) * HID <= 0x7fffffffull);
 }
 
 cudaError_t launch_mlp_prefill_mma(const MlpArgs& a, cudaStream_t s, int* status) {
     if (!mlp_prefill_mma_supported(a)) return cudaErrorNotSupported;
-    const uint64_t rows = uint64_t(a.B) * a.H * a.T;
+    const uint64_t heads = uint64_t(a.B) * a.H;
     CUtensorMap mq, mk, mv, h1, h2;
     cudaError_t e;
-    if ((e = make_tma_map_bf16(&mq, a.Q, rows, D)) != cudaSuccess) return e;
-    if ((e = make_tma_map_bf16(&mk, a.K, rows, D)) != cudaSuccess) return e;
-    if ((e = make_tma_map_bf16(&mv, a.V, rows, D)) != cudaSuccess) return e;
+    // the 2D maps address rows bh * T + t with an int32 coordinate
+    const bool part = a.T % BT || heads * a.T > 0x7fffffffull;
+    if (part) {  // [heads][T][D]: the boxes of a partial block read zeros past T
+        if ((e = make_tma_map_bf16_heads(&mq, a.Q, heads, a.T, D)) != cudaSuccess) return e;
+        if ((e = make_tma_map_bf16_heads(&mk, a.K, heads, a.T, D)) != cudaSuccess) return e;
+        if ((e = make_tma_map_bf16_heads(&mv, a.V, heads, a.T, D)) != cudaSuccess) return e;
+    } else {  // [heads * T][D]
+        if ((e = make_tma_map_bf16(&mq, a.Q, heads * a.T, D)) != cudaSuccess) return e;
+        if ((e = make_tma_map_bf16(&mk, a.K, heads * a.T, D)) != cudaSuccess) return e;
+        if ((e = make_tma_map_bf16(&mv, a.V, heads * a.T, D)) != cudaSuccess) return e;
+    }
     memset(&h1, 0, sizeof(h1));  // unused without the recorded states
     memset(&h2, 0, sizeof(h2));
     if (a.W1_hist) {  // W1_hist as [blocks * d][hidden], W2_hist as [blocks * hidden][d]
-        const uint64_t blocks = uint64_t(a.B) * a.H * (a.T / BT);
+        const uint64_t blocks = heads * ((a.T + BT - 1) / BT);
         if ((e = make_tma_map_bf16_box(&h1, a.W1_hist, blocks * D, HID, HS, D, 64)) != cudaSuccess) return e;
         if ((e = make_tma_map_bf16_box(&h2, a.W2_hist, blocks * HID, D, D, HS, 128)) != cudaSuccess) return e;
     }
@@ -561,8 +598,11 @@ cudaError_t launch_mlp_prefill_mma(const MlpArgs& a, cudaStream_t s, int* status
         return cudaGetLastError();
     };
     // + 1024 bytes of alignment slack
-    return a.W1_hist ? run(mlp_prefill_mma_kernel<true>, SMEM_BYTES_HIST + 1024)
-                     : run(mlp_prefill_mma_kernel<false>, SMEM_BYTES + 1024);
+    if (a.W1_hist)
+        return part ? run(mlp_prefill_mma_kernel<true, true>, SMEM_BYTES_HIST + 1024)
+                    : run(mlp_prefill_mma_kernel<true, false>, SMEM_BYTES_HIST + 1024);
+    return part ? run(mlp_prefill_mma_kernel<false, true>, SMEM_BYTES + 1024)
+                : run(mlp_prefill_mma_kernel<false, false>, SMEM_BYTES + 1024);
 }
 
 }  // namespace ttt

@@ -425,7 +425,7 @@ ttt_status ttt_mlp_prefill(const void* Q, const void* K, const void* V, const fl
     int* status = nullptr;
     cudaError_t e = status_ptr(&status);
     if (e != cudaSuccess) return cuda_fail(e, "ttt_mlp_prefill status word");
-    // bf16, d = 64, hidden = 256, chunk = 16, 16 | T: the warp-MMA kernel (state in registers), else
+    // bf16, d = 64, hidden = 256, chunk = 16, any T: the warp-MMA kernel (state in registers), else
     // the tcgen05 kernel; the generic kernel otherwise.  TTT_MLP_PREFILL_KERNEL = "mma", "tc" or
     // "generic" makes the dispatch start at that kernel.
     const int first = kernel_choice("TTT_MLP_PREFILL_KERNEL", "mma", "tc");
@@ -529,7 +529,7 @@ ttt_status ttt_mlp_prefill_backward(const void* Q, const void* K, const void* V,
     CHECK_PTR(deta);
     ttt::MlpBwdArgs a{Q, K, V, eta, W1_hist, W2_hist, dZ, dW1_T, dW2_T, dQ, dK, dV, deta, dW1_0, dW2_0,
                       B, H, T, d, hidden, chunk, dtype == TTT_BF16 ? 1 : 0};
-    // bf16, d = 64, hidden = 256, chunk 16, 16 | T: the warp-MMA kernel; the SIMT kernel otherwise
+    // bf16, d = 64, hidden = 256, chunk 16, any T: the warp-MMA kernel; the SIMT kernel otherwise
     // (TTT_MLP_BACKWARD_KERNEL = "simt" forces the SIMT kernel)
     const char* kv = getenv("TTT_MLP_BACKWARD_KERNEL");
     cudaError_t e = cudaErrorNotSupported;

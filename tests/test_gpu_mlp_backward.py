@@ -56,7 +56,8 @@ CASES = [  # B, H, T, d, hidden, chunk, dtype, with state gradients
     (1, 3, 24, 32, 128, 1, "f32", False),  # online steps
     (2, 1, 40, 16, 256, 16, "f32", True),
     (1, 2, 64, 64, 256, 16, "bf16", True),  # the warp-MMA forward records the states
-    (2, 2, 50, 64, 256, 16, "bf16", False),  # ragged: the SIMT forward records them
+    (2, 2, 50, 64, 256, 16, "bf16", False),  # a partial last block: the warp-MMA forward records the states,
+                                             # the SIMT backward reads them
     (1, 2, 48, 32, 64, 8, "bf16", True),
 ]
 
@@ -87,6 +88,22 @@ def test_mlp_recorded_states_are_the_block_start_states(dtype):
         cut = {k: (v[:, :, :16 * n] if k not in ("W1", "W2") else v) for k, v in r.items()}
         _, A, Bm = O.mlp_dual(cut["Q"], cut["K"], cut["V"], cut["eta"], cut["W1"], cut["W2"], 16)
         assert rel_err(H1[:, :, n], A) <= TOL[dtype] and rel_err(H2[:, :, n], Bm) <= TOL[dtype]
+
+
+def test_mlp_recorded_states_partial_last_block():
+    # bf16, d = 64, hidden = 256, T = 45: the warp-MMA forward records ceil(45 / 16) = 3 states
+    x = WL.mlp_inputs(1, 2, 45, 64, 256, seed=4210, dtype="bf16", w_std=0.1)
+    g = cuda(x)
+    Z, W1, W2, H1, H2 = T.mlp_prefill_hist(g["Q"], g["K"], g["V"], g["eta"], g["W1"], g["W2"], 16)
+    torch.cuda.synchronize()
+    assert H1.shape == (1, 2, 3, 64, 256) and H2.shape == (1, 2, 3, 256, 64)
+    r = f64(x)
+    Zr, W1r, W2r = O.mlp_dual(r["Q"], r["K"], r["V"], r["eta"], r["W1"], r["W2"], 16)
+    assert rel_err(Z, Zr) <= TOL["bf16"] and rel_err(W1, W1r) <= TOL["bf16"] and rel_err(W2, W2r) <= TOL["bf16"]
+    for n in (1, 2):
+        cut = {k: (v[:, :, :16 * n] if k not in ("W1", "W2") else v) for k, v in r.items()}
+        _, A, Bm = O.mlp_dual(cut["Q"], cut["K"], cut["V"], cut["eta"], cut["W1"], cut["W2"], 16)
+        assert rel_err(H1[:, :, n], A) <= TOL["bf16"] and rel_err(H2[:, :, n], Bm) <= TOL["bf16"]
 
 
 def test_mlp_backward_without_tokens_passes_the_state_gradient_through():

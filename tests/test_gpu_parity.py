@@ -442,3 +442,31 @@ def test_partial_sub_block_reads_no_rows_of_the_next_head(d, kernel):
     Zr, Wr = O.linear_dual(r["Q"], r["K"], r["V"], r["eta"], r["W0"], 16)
     assert rel_err(Z[:, :1], Zr) <= TOL["bf16"]
     assert rel_err(W[:, :1], Wr) <= TOL["bf16"]
+
+
+# TTT-MLP, bf16, d = 64, hidden = 256, blocks of 16, T not a multiple of 16: the warp-MMA kernel runs
+# a partial last block (its eta stored by the producer thread, zero past T; with 4 not dividing T
+# every block's eta is stored that way)
+@pytest.mark.parametrize("T_", [1, 7, 17, 50, 203, 1001])
+def test_mlp_mma_partial_last_block(T_):
+    x = WL.mlp_inputs(2, 3, T_, 64, 256, seed=520 + T_, dtype="bf16", w_std=0.05)
+    with mlp_kernel("mma"):
+        Z, W1, W2 = run_mlp(x, 16)
+    r = f64(x)
+    Zr, W1r, W2r = O.mlp_dual(r["Q"], r["K"], r["V"], r["eta"], r["W1"], r["W2"], 16)
+    assert rel_err(Z, Zr) <= TOL["bf16"]
+    assert rel_err(W1, W1r) <= TOL["bf16"]
+    assert rel_err(W2, W2r) <= TOL["bf16"]
+
+
+def test_mlp_mma_partial_block_reads_no_rows_of_the_next_head():
+    # head 1 holds values whose products overflow; head 0 (T = 21) must not see them
+    x = WL.mlp_inputs(1, 2, 21, 64, 256, seed=531, dtype="bf16", w_std=0.05)
+    for k in ("Q", "K", "V"):
+        x[k][:, 1] = 3.0e38
+    with mlp_kernel("mma"):
+        Z, W1, W2 = run_mlp(x, 16)
+    r = f64({k: v[:, :1] for k, v in x.items()})
+    Zr, W1r, W2r = O.mlp_dual(r["Q"], r["K"], r["V"], r["eta"], r["W1"], r["W2"], 16)
+    assert rel_err(Z[:, :1], Zr) <= TOL["bf16"]
+    assert rel_err(W1[:, :1], W1r) <= TOL["bf16"] and rel_err(W2[:, :1], W2r) <= TOL["bf16"]
