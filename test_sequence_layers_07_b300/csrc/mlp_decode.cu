@@ -14,10 +14,14 @@
 // Bandwidth-bound: each step reads and writes the 2*d*hidden fp32 state of a
 // head exactly once.  One CTA per (batch, head), one thread per hidden unit j:
 // the thread keeps column j of W1 in registers (coalesced loads and stores
-// across the warp); W2 is staged in shared memory with rows padded to d+1
-// words, so both the row walk (e2 W2^T) and the column walks (a W2, hq W2) are
+// across the warp); W2 is copied into shared memory by 16-byte cp.async, so
+// u = k W1 runs while it lands and no register holds it on the way.  Its rows
+// are unpadded with the 16-byte chunks of row r permuted by an XOR of r: the
+// row walk (e2 W2^T, 16-byte reads) and the column walks (a W2, hq W2) are
 // bank-conflict free.  Column sums over the hidden units are split over
-// hidden/d thread groups and finished through shared memory.
+// hidden/d thread groups and finished through shared memory.  At hidden = 256
+// two CTAs share an SM (up to 128 registers a thread); three, at 80 registers,
+// spill and measured slower.
 #include "ttt_common.cuh"
 #include "ttt_internal.h"
 
@@ -43,6 +47,25 @@ __device__ __forceinline__ float gelu_f(float x) {
     return 0.5f * x * (1.f + t);
 }
 
+// word offset of W2[r][c] in shared memory: chunk c/4 of row r at position (c/4) XOR f(r), f(r) chosen so
+// that eight consecutive rows put a given chunk in eight distinct 16-byte bank groups
+template <int D>
+__device__ __forceinline__ int w2_chunk(int r, int x) {
+    constexpr int NCH = D / 4;
+    const int f = NCH >= 8 ? (r & 7) : ((r >> 1) & (NCH - 1));
+    return r * D + ((x ^ f) << 2);
+}
+template <int D>
+__device__ __forceinline__ int w2_off(int r, int c) {
+    return w2_chunk<D>(r, c >> 2) + (c & 3);
+}
+
+__device__ __forceinline__ void cp_async16(float* dst, const float* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
+                 "l"(src)
+                 : "memory");
+}
+
 template <int HID>
 __device__ __forceinline__ float block_sum(float v, float* red) {
     v = warp_sum(v);
@@ -57,14 +80,14 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
 }
 
 template <typename TI, int D, int HID>
-__global__ void __launch_bounds__(HID)
+__global__ void __launch_bounds__(HID, HID == 256 ? 2 : 1)
 mlp_decode_kernel(const TI* __restrict__ q, const TI* __restrict__ k, const TI* __restrict__ v,
                   const float* __restrict__ eta, float* __restrict__ W1, float* __restrict__ W2, TI* __restrict__ z) {
-    constexpr int LD = D + 1;      // padded row of W2 in shared memory
+    constexpr int NCH = D / 4;      // 16-byte chunks of a row of W2
     constexpr int PARTS = HID / D;  // thread groups of a column sum
-    extern __shared__ float sm[];
-    float* w2s = sm;                          // [HID][LD]
-    float* ks = w2s + HID * LD;               // [D]
+    extern __shared__ __align__(16) float sm[];
+    float* w2s = sm;                          // [HID][D], chunks permuted (w2_off)
+    float* ks = w2s + HID * D;                // [D]
     float* qs = ks + D;                       // [D]
     float* vs = qs + D;                       // [D]
     float* av = vs + D;                       // [HID]  GELU(k W1)
@@ -78,17 +101,13 @@ mlp_decode_kernel(const TI* __restrict__ q, const TI* __restrict__ k, const TI* 
     float* W1h = W1 + bh * D * HID;
     float* W2h = W2 + bh * HID * D;
 
-    // column j of W1, and W2 into shared memory (coalesced reads)
+    // W2 into shared memory by cp.async (coalesced 16-byte pieces), column j of W1 into registers
+#pragma unroll 4
+    for (int idx = j; idx < HID * NCH; idx += HID) cp_async16(w2s + w2_chunk<D>(idx / NCH, idx % NCH), W2h + 4 * idx);
+    asm volatile("cp.async.commit_group;" ::: "memory");
     float w1[D];
 #pragma unroll
     for (int i = 0; i < D; ++i) w1[i] = W1h[i * HID + j];
-#pragma unroll 4
-    for (int idx = j; idx < HID * D / 4; idx += HID) {
-        const float4 f = reinterpret_cast<const float4*>(W2h)[idx];
-        const int r = (4 * idx) / D, c = (4 * idx) % D;
-        float* dst = w2s + r * LD + c;
-        dst[0] = f.x; dst[1] = f.y; dst[2] = f.z; dst[3] = f.w;
-    }
     if (j < D) {
         ks[j] = to_f32(k[bh * D + j]);
         qs[j] = to_f32(q[bh * D + j]);
@@ -108,14 +127,15 @@ mlp_decode_kernel(const TI* __restrict__ q, const TI* __restrict__ k, const TI* 
     float gp;
     const float aj = gelu_d(u, gp);
     av[j] = aj;
-    __syncthreads();
+    asm volatile("cp.async.wait_group 0;" ::: "memory");  // this thread's pieces of W2 have landed
+    __syncthreads();                                       // everyone's have
 
     // p = a W2: column c of W2 summed over this thread's share of the hidden units
     const int c = j % D, pi = j / D;
     {
         float s = 0.f;
 #pragma unroll 8
-        for (int r = pi * (HID / PARTS); r < (pi + 1) * (HID / PARTS); ++r) s = fmaf(av[r], w2s[r * LD + c], s);
+        for (int r = pi * (HID / PARTS); r < (pi + 1) * (HID / PARTS); ++r) s = fmaf(av[r], w2s[w2_off<D>(r, c)], s);
         part[pi * D + c] = s;
     }
     __syncthreads();
@@ -127,11 +147,16 @@ mlp_decode_kernel(const TI* __restrict__ q, const TI* __restrict__ k, const TI* 
     }
     __syncthreads();
 
-    // e1 = (e2 W2^T) . GELU'(u): row j of W2
-    float g = 0.f;
-#pragma unroll 8
-    for (int cc = 0; cc < D; ++cc) g = fmaf(e2s[cc], w2s[j * LD + cc], g);
-    const float e1 = g * gp;
+    // e1 = (e2 W2^T) . GELU'(u): row j of W2, 16 bytes at a time
+    float g0 = 0.f, g1 = 0.f;
+#pragma unroll
+    for (int x = 0; x < NCH; ++x) {
+        const float4 w = *reinterpret_cast<const float4*>(w2s + w2_chunk<D>(j, x));
+        const float4 e = *reinterpret_cast<const float4*>(e2s + 4 * x);
+        g0 = fmaf(e.x, w.x, fmaf(e.y, w.y, g0));
+        g1 = fmaf(e.z, w.z, fmaf(e.w, w.w, g1));
+    }
+    const float e1 = (g0 + g1) * gp;
 
     // W1 <- W1 - eta k^T e1 (column j, in registers), written back
 #pragma unroll
@@ -145,7 +170,7 @@ mlp_decode_kernel(const TI* __restrict__ q, const TI* __restrict__ k, const TI* 
     {
         float s = 0.f;
 #pragma unroll 8
-        for (int r = pi * (HID / PARTS); r < (pi + 1) * (HID / PARTS); ++r) s = fmaf(hqv[r], w2s[r * LD + c], s);
+        for (int r = pi * (HID / PARTS); r < (pi + 1) * (HID / PARTS); ++r) s = fmaf(hqv[r], w2s[w2_off<D>(r, c)], s);
         part[pi * D + c] = s;
     }
     __syncthreads();
@@ -158,19 +183,19 @@ mlp_decode_kernel(const TI* __restrict__ q, const TI* __restrict__ k, const TI* 
 
     // W2 <- W2 - eta a^T e2, written back (coalesced)
 #pragma unroll 4
-    for (int idx = j; idx < HID * D / 4; idx += HID) {
-        const int r = (4 * idx) / D, cc = (4 * idx) % D;
-        const float* src = w2s + r * LD + cc;
+    for (int idx = j; idx < HID * NCH; idx += HID) {
+        const int r = idx / NCH, cc = 4 * (idx % NCH);
+        const float4 w = *reinterpret_cast<const float4*>(w2s + w2_chunk<D>(r, idx % NCH));
+        const float4 e = *reinterpret_cast<const float4*>(e2s + cc);
         const float s = -et * av[r];
-        reinterpret_cast<float4*>(W2h)[idx] =
-            make_float4(fmaf(s, e2s[cc], src[0]), fmaf(s, e2s[cc + 1], src[1]), fmaf(s, e2s[cc + 2], src[2]),
-                        fmaf(s, e2s[cc + 3], src[3]));
+        reinterpret_cast<float4*>(W2h)[idx] = make_float4(fmaf(s, e.x, w.x), fmaf(s, e.y, w.y), fmaf(s, e.z, w.z),
+                                                          fmaf(s, e.w, w.w));
     }
 }
 
 template <int D, int HID>
 constexpr size_t smem_bytes() {
-    return sizeof(float) * (size_t(HID) * (D + 1) + 3 * D + 2 * HID + (HID / D) * D + D + HID / 32);
+    return sizeof(float) * (size_t(HID) * D + 3 * D + 2 * HID + (HID / D) * D + D + HID / 32);
 }
 
 template <typename TI, int D, int HID>
