@@ -101,13 +101,14 @@ mlp_decode_kernel(const TI* __restrict__ q, const TI* __restrict__ k, const TI* 
     float* W1h = W1 + bh * D * HID;
     float* W2h = W2 + bh * HID * D;
 
-    // W2 into shared memory by cp.async (coalesced 16-byte pieces), column j of W1 into registers
-#pragma unroll 4
-    for (int idx = j; idx < HID * NCH; idx += HID) cp_async16(w2s + w2_chunk<D>(idx / NCH, idx % NCH), W2h + 4 * idx);
-    asm volatile("cp.async.commit_group;" ::: "memory");
+    // column j of W1 into registers, then W2 into shared memory by cp.async (coalesced 16-byte pieces):
+    // W1's loads go first, so that u = k W1 can run while W2 is still landing
     float w1[D];
 #pragma unroll
     for (int i = 0; i < D; ++i) w1[i] = W1h[i * HID + j];
+#pragma unroll 4
+    for (int idx = j; idx < HID * NCH; idx += HID) cp_async16(w2s + w2_chunk<D>(idx / NCH, idx % NCH), W2h + 4 * idx);
+    asm volatile("cp.async.commit_group;" ::: "memory");
     if (j < D) {
         ks[j] = to_f32(k[bh * D + j]);
         qs[j] = to_f32(q[bh * D + j]);
