@@ -251,8 +251,9 @@ ttt_status ttt_linear_prefill_hist(const void* Q, const void* K, const void* V, 
  *   deta_j = -sum_c E_jc (K dW')_jc + sum_i M_ij dA_ij S_ij,
  *   dW = dW' + Q^T dZ + K^T dE.
  * Accumulation in fp32; outputs rounded to dtype (RN-even).  bf16 with d = 64
- * and chunk 16 runs on the tensor cores, every other shape on a SIMT fp32
- * kernel; TTT_LINEAR_BACKWARD_KERNEL = "simt" forces the SIMT kernel.
+ * and chunk 16 runs on the tensor cores for any T (a partial last block weighs
+ * its tokens past T by zero), every other shape on a SIMT fp32 kernel;
+ * TTT_LINEAR_BACKWARD_KERNEL = "simt" forces the SIMT kernel.
  */
 ttt_status ttt_linear_prefill_backward(const void* Q, const void* K, const void* V, const float* eta,
                                        const void* W_hist, const void* dZ, const float* dW_T, void* dQ,

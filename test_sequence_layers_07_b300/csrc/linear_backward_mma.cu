@@ -111,6 +111,12 @@ __device__ __forceinline__ float2 bf16x2_at(const uint8_t* tile, int row, int co
     return make_float2(bf16_lo(v), bf16_hi(v));
 }
 
+// PART: T is not a multiple of 16 (a partial last block, the first one processed), or the rows of
+// all heads exceed the int32 coordinate of a 2D tensor map.  Then Q/K/V/dZ come through per-head 3D
+// maps (tokens past a head's end read as zeros, so they add nothing to any gradient), eta by cp.async
+// where a bulk copy cannot take it (zeros past T), and no output row past T is stored; the
+// instantiation for the common case compiles none of that.
+template <bool PART>
 __global__ void __launch_bounds__(THREADS, 1)
 linear_backward_mma_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                            const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmZ,
@@ -129,7 +135,7 @@ linear_backward_mma_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const size_t bh = blockIdx.x;
-    const int nsb = T / 16;                  // blocks (of 16 tokens)
+    const int nsb = PART ? (T + 15) / 16 : T / 16;  // blocks of 16 tokens (with PART the last may be partial)
     const int nstg = (nsb + SPS - 1) / SPS;  // stages
     const uint32_t sbase = smem_u32(smem);
     const int g = lane >> 2, t = lane & 3;
@@ -190,16 +196,42 @@ linear_backward_mma_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid
                 const int s = si % NST, n = subs_in(si), hi = hi_of(si);
                 if (si >= NST && !wait(empty_bar[s], ((si / NST) - 1) & 1)) break;
                 const uint32_t fb = smem_u32(&full_bar[s]);
-                mbar_arrive_expect_tx(fb, uint32_t(n) * (4 * TILE + 64));
                 const uint32_t st = sbase + s * STAGE;
-                for (int i = 0; i < n; ++i) {
-                    const int y = int(bh * T) + 16 * (hi - i);
-                    tma_load_2d(st + QOFF + i * TILE, &tmQ, 0, y, fb);
-                    tma_load_2d(st + KOFF + i * TILE, &tmK, 0, y, fb);
-                    tma_load_2d(st + VOFF + i * TILE, &tmV, 0, y, fb);
-                    tma_load_2d(st + ZOFF + i * TILE, &tmZ, 0, y, fb);
+                if constexpr (PART) {
+                    // eta of blocks hi - n + 1 .. hi (token order): one bulk copy when all their tokens
+                    // exist and a head's eta starts on a 16-byte boundary (4 | T); otherwise 4-byte
+                    // cp.async copies that the stage's mbarrier tracks, and zeros past T
+                    const int t0 = 16 * (hi - n + 1), tok = min(16 * n, T - t0);
+                    const bool eb = (T & 3) == 0 && tok == 16 * n;
+                    if (!eb) {
+                        const float* eg = eta + bh * T + t0;
+                        float* es = reinterpret_cast<float*>(smem + s * STAGE + EOFF);
+                        for (int j = 0; j < 16 * n; ++j) {
+                            if (j < tok) cp_async4(st + EOFF + 4 * j, eg + j);
+                            else es[j] = 0.f;
+                        }
+                        cp_async_mbar_arrive(fb);  // before this thread's own arrive on the phase
+                    }
+                    mbar_arrive_expect_tx(fb, uint32_t(n) * 4 * TILE + (eb ? uint32_t(n) * 64 : 0u));
+                    for (int i = 0; i < n; ++i) {
+                        const int y = 16 * (hi - i), z = int(bh);
+                        tma_load_3d(st + QOFF + i * TILE, &tmQ, 0, y, z, fb);
+                        tma_load_3d(st + KOFF + i * TILE, &tmK, 0, y, z, fb);
+                        tma_load_3d(st + VOFF + i * TILE, &tmV, 0, y, z, fb);
+                        tma_load_3d(st + ZOFF + i * TILE, &tmZ, 0, y, z, fb);
+                    }
+                    if (eb) bulk_load(st + EOFF, eta + bh * T + t0, uint32_t(n) * 64, fb);
+                } else {
+                    mbar_arrive_expect_tx(fb, uint32_t(n) * (4 * TILE + 64));
+                    for (int i = 0; i < n; ++i) {
+                        const int y = int(bh * T) + 16 * (hi - i);
+                        tma_load_2d(st + QOFF + i * TILE, &tmQ, 0, y, fb);
+                        tma_load_2d(st + KOFF + i * TILE, &tmK, 0, y, fb);
+                        tma_load_2d(st + VOFF + i * TILE, &tmV, 0, y, fb);
+                        tma_load_2d(st + ZOFF + i * TILE, &tmZ, 0, y, fb);
+                    }
+                    bulk_load(st + EOFF, eta + bh * T + 16 * (hi - n + 1), uint32_t(n) * 64, fb);
                 }
-                bulk_load(st + EOFF, eta + bh * T + 16 * (hi - n + 1), uint32_t(n) * 64, fb);
                 ++issued;
             }
             for (int si = issued > NST ? issued - NST : 0; si < issued; ++si)
@@ -411,7 +443,7 @@ linear_backward_mma_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid
                 cp_async_wait2();  // this thread's chunks of the state of block p
                 // ---- barrier A: the state of block p is in, every warp is done with block p - 1
                 if (bar_readout_any(err)) { err = true; break; }
-                if (p >= 1 && r == 0 && lane < 16)
+                if (p >= 1 && r == 0 && lane < 16 && (!PART || 16 * (sb + 1) + lane < T))
                     deta[bh * T + 16 * (sb + 1) + lane] =
                         dep[64 + lane] + ((dep[lane] + dep[16 + lane]) + (dep[32 + lane] + dep[48 + lane]));
                 fetch_w(p + 3);  // into the slot of block p - 1
@@ -598,12 +630,14 @@ linear_backward_mma_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid
                     const uint4 vq = *reinterpret_cast<const uint4*>(stg + orow * 32 + ohalf * 16);
                     const uint4 vk = *reinterpret_cast<const uint4*>(stg + 512 + orow * 32 + ohalf * 16);
                     const size_t o = (row0 + orow) * D + 16 * r + 8 * ohalf;
-                    *reinterpret_cast<uint4*>(dQ + o) = vq;
-                    *reinterpret_cast<uint4*>(dK + o) = vk;
                     uint4 dv = *reinterpret_cast<const uint4*>(smem + DE_OFF + (s * SPS + i) * TILE +
                                                               swz(orow, 16 * r + 8 * ohalf));
                     dv.x ^= 0x80008000u; dv.y ^= 0x80008000u; dv.z ^= 0x80008000u; dv.w ^= 0x80008000u;
-                    *reinterpret_cast<uint4*>(dV + o) = dv;
+                    if (!PART || 16 * sb + orow < T) {  // rows past T are not stored
+                        *reinterpret_cast<uint4*>(dQ + o) = vq;
+                        *reinterpret_cast<uint4*>(dK + o) = vk;
+                        *reinterpret_cast<uint4*>(dV + o) = dv;
+                    }
                     __syncwarp();
                 }
             }
@@ -612,33 +646,47 @@ linear_backward_mma_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid
             if (lane == 0) mbar_arrive(smem_u32(&empty_bar[s]));
         }
         // deta of the last block processed (block 0 of the sequence)
-        if (!bar_readout_any(err) && p == nsb && r == 0 && lane < 16)
+        if (!bar_readout_any(err) && p == nsb && r == 0 && lane < 16 && (!PART || lane < T))
             deta[bh * T + lane] = dep[64 + lane] + ((dep[lane] + dep[16 + lane]) + (dep[32 + lane] + dep[48 + lane]));
         cp_async_wait0();
     }
     __syncthreads();
 }
 
-}  // namespace
-
-cudaError_t launch_linear_backward_mma(const LinearBwdArgs& a, cudaStream_t s, int* status) {
-    if (!a.bf16 || a.d != D || a.chunk != 16 || a.T % 16 != 0) return cudaErrorNotSupported;
-    if (uint64_t(a.B) * a.H * a.T > 0x7fffffffull) return cudaErrorNotSupported;  // TMA row coordinate is int32
-    const uint64_t rows = uint64_t(a.B) * a.H * a.T;
+template <bool PART>
+cudaError_t launch_part(const LinearBwdArgs& a, cudaStream_t s, int* status) {
+    const uint64_t heads = uint64_t(a.B) * a.H;
     CUtensorMap mq, mk, mv, mz;
     cudaError_t e;
-    if ((e = make_tma_map_bf16(&mq, a.Q, rows, D)) != cudaSuccess) return e;
-    if ((e = make_tma_map_bf16(&mk, a.K, rows, D)) != cudaSuccess) return e;
-    if ((e = make_tma_map_bf16(&mv, a.V, rows, D)) != cudaSuccess) return e;
-    if ((e = make_tma_map_bf16(&mz, a.dZ, rows, D)) != cudaSuccess) return e;
+    if (PART) {  // [heads][T][D]: the boxes of a partial block read zeros past T
+        if ((e = make_tma_map_bf16_heads(&mq, a.Q, heads, a.T, D)) != cudaSuccess) return e;
+        if ((e = make_tma_map_bf16_heads(&mk, a.K, heads, a.T, D)) != cudaSuccess) return e;
+        if ((e = make_tma_map_bf16_heads(&mv, a.V, heads, a.T, D)) != cudaSuccess) return e;
+        if ((e = make_tma_map_bf16_heads(&mz, a.dZ, heads, a.T, D)) != cudaSuccess) return e;
+    } else {  // [heads * T][D]
+        if ((e = make_tma_map_bf16(&mq, a.Q, heads * a.T, D)) != cudaSuccess) return e;
+        if ((e = make_tma_map_bf16(&mk, a.K, heads * a.T, D)) != cudaSuccess) return e;
+        if ((e = make_tma_map_bf16(&mv, a.V, heads * a.T, D)) != cudaSuccess) return e;
+        if ((e = make_tma_map_bf16(&mz, a.dZ, heads * a.T, D)) != cudaSuccess) return e;
+    }
     const int bytes = BYTES + 1024;
-    if ((e = allow_dynamic_smem(reinterpret_cast<const void*>(linear_backward_mma_kernel), bytes)) !=
-        cudaSuccess)
-        return e;
-    linear_backward_mma_kernel<<<unsigned(a.B) * unsigned(a.H), THREADS, bytes, s>>>(
+    auto kern = linear_backward_mma_kernel<PART>;
+    if ((e = allow_dynamic_smem(reinterpret_cast<const void*>(kern), bytes)) != cudaSuccess) return e;
+    kern<<<unsigned(a.B) * unsigned(a.H), THREADS, bytes, s>>>(
         mq, mk, mv, mz, a.eta, static_cast<const __nv_bfloat16*>(a.W_hist), a.dW_T, static_cast<__nv_bfloat16*>(a.dQ), static_cast<__nv_bfloat16*>(a.dK),
         static_cast<__nv_bfloat16*>(a.dV), a.deta, a.dW0, a.T, status);
     return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_linear_backward_mma(const LinearBwdArgs& a, cudaStream_t s, int* status) {
+    // any T: a partial last block weighs its tokens past T by zero
+    if (!a.bf16 || a.d != D || a.chunk != 16) return cudaErrorNotSupported;
+    if (uint64_t(a.B) * a.H > 0x7fffffffull) return cudaErrorNotSupported;  // TMA head coordinate is int32
+    // the 2D maps address rows bh * T + t with an int32 coordinate
+    if (a.T % 16 || uint64_t(a.B) * a.H * a.T > 0x7fffffffull) return launch_part<true>(a, s, status);
+    return launch_part<false>(a, s, status);
 }
 
 }  // namespace ttt

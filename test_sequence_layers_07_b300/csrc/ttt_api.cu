@@ -374,7 +374,7 @@ ttt_status ttt_linear_prefill_backward(const void* Q, const void* K, const void*
     CHECK_PTR(deta);
     ttt::LinearBwdArgs a{Q, K, V, eta, W_hist, dZ, dW_T, dQ, dK, dV, deta, dW0, B, H, T, d, chunk,
                          dtype == TTT_BF16 ? 1 : 0};
-    // bf16, d = 64, chunk 16, 16 | T: the tensor-core kernel; the SIMT kernel otherwise
+    // bf16, d = 64, chunk 16, any T: the tensor-core kernel; the SIMT kernel otherwise
     // (TTT_LINEAR_BACKWARD_KERNEL = "simt" forces the SIMT kernel)
     const char* kv = getenv("TTT_LINEAR_BACKWARD_KERNEL");
     cudaError_t e = cudaErrorNotSupported;

@@ -67,10 +67,12 @@ def test_backward_matches_oracle(B, H, T_, d, chunk, dtype, with_dWT):
 
 @pytest.mark.parametrize("kernel", ["mma", "simt"])
 @pytest.mark.parametrize("B,H,T_,with_dWT", [(1, 1, 16, True), (2, 3, 48, False), (1, 2, 208, True),
-                                             (4, 40, 64, True), (1, 2, 1040, False)])
+                                             (4, 40, 64, True), (1, 2, 1040, False), (2, 3, 1037, True),
+                                             (1, 2, 1036, False), (2, 1, 7, True), (1, 3, 67, True)])
 def test_backward_kernels_d64_blocks_of_16(kernel, B, H, T_, with_dWT, monkeypatch):
     # bf16, d = 64, blocks of 16: the tensor-core backward (default) and the SIMT one; stages of
-    # four blocks with and without a short last stage, and more CTAs than SMs
+    # four blocks with and without a short last stage, more CTAs than SMs, and T not a multiple of
+    # 16 (a partial last block, the first processed; with 4 not dividing T every eta by cp.async)
     if kernel == "simt":
         monkeypatch.setenv("TTT_LINEAR_BACKWARD_KERNEL", "simt")
     else:
