@@ -335,7 +335,8 @@ ttt_status ttt_mlp_prefill_hist(const void* Q, const void* K, const void* V, con
  *   dQ = dZq W1^T + dS1 K,  dK = -D E1 dW1'^T + dS1^T Q + dZk W1^T,  dV = -dE2,
  *   with dS1 = M . (-dZq E1^T) D, dS2 = M . (-dZ E2^T) D, and deta from the same terms.
  * Accumulation in fp32, outputs rounded to dtype (RN-even). bf16 with d = 64, hidden = 256,
- * chunk = 16 and 16 | T runs on warp-level tensor-core MMAs with bf16 operands (the recorded
+ * chunk = 16 (any T: a partial last block weighs its tokens past T by zero) runs on
+ * warp-level tensor-core MMAs with bf16 operands (the recorded
  * states, the intermediates and a bf16 copy of the running state gradient); every other shape on
  * fp32 SIMT arithmetic. TTT_MLP_BACKWARD_KERNEL = "simt" forces the SIMT kernel.
  */

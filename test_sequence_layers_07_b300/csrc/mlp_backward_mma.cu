@@ -118,6 +118,15 @@ __device__ __forceinline__ void ldsm_x2_trans(uint32_t addr, uint32_t& r0, uint3
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
+// the same with zeros instead of the source when `valid` is false (nothing is read from src then)
+__device__ __forceinline__ void cp_async16_or_zero(uint32_t dst, const void* src, bool valid) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(valid ? 16 : 0)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async4_or_zero(uint32_t dst, const void* src, bool valid) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(valid ? 4 : 0)
+                 : "memory");
+}
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait0() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
@@ -205,7 +214,10 @@ __device__ __forceinline__ void scale_rows(float (&x)[4], float sg, float sg8) {
     x[0] *= sg, x[1] *= sg, x[2] *= sg8, x[3] *= sg8;
 }
 
-template <int NW_>
+// PART: T is not a multiple of 16 (a partial last block, the first processed): its tokens past T
+// are copied in as zeros (eta too), so they add nothing to any gradient, and no output row past T is
+// stored; the instantiation for 16 | T compiles none of that.
+template <int NW_, bool PART>
 __global__ void __launch_bounds__(32 * NW_, 1)
 mlp_backward_mma_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restrict__ K,
                         const __nv_bfloat16* __restrict__ V, const float* __restrict__ eta,
@@ -224,7 +236,7 @@ mlp_backward_mma_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16
     const uint32_t sb = smem_u32(smem);
     const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
     const size_t bh = blockIdx.x;
-    const int nblk = T / BT;
+    const int nblk = PART ? (T + BT - 1) / BT : T / BT;
     constexpr size_t NWT = size_t(D) * HID;
     dW1g += bh * NWT;
     dW2g += bh * NWT;
@@ -270,13 +282,28 @@ mlp_backward_mma_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16
     auto issue_tokens = [&](int m) {
         const uint32_t tb = sb + OFF_TOK + (m & 1) * TOKBUF;
         const size_t row0 = bh * size_t(T) + size_t(m) * BT;
+        if (PART && BT * (m + 1) > T) {  // the partial last block: zeros past T, eta by 4-byte copies
+#pragma unroll
+            for (int c = tid; c < 4 * 128; c += NTH) {
+                const int tile = c >> 7, row = (c >> 3) & 15, ch = c & 7;
+                const __nv_bfloat16* src = tile == 0 ? Q : tile == 1 ? K : tile == 2 ? V : dZ;
+                const bool in = BT * m + row < T;
+                cp_async16_or_zero(tb + tile * TILE + t64(row, 8 * ch), src + (row0 + (in ? row : 0)) * D + 8 * ch, in);
+            }
+            if (tid < BT) cp_async4_or_zero(tb + 4 * TILE + 4 * tid, eta + row0 + (BT * m + tid < T ? tid : 0), BT * m + tid < T);
+            return;
+        }
 #pragma unroll
         for (int c = tid; c < 4 * 128; c += NTH) {
             const int tile = c >> 7, row = (c >> 3) & 15, ch = c & 7;
             const __nv_bfloat16* src = tile == 0 ? Q : tile == 1 ? K : tile == 2 ? V : dZ;
             cp_async16(tb + tile * TILE + t64(row, 8 * ch), src + (row0 + row) * D + 8 * ch);
         }
-        if (tid < 4) cp_async16(tb + 4 * TILE + 16 * tid, eta + row0 + 4 * tid);
+        if (PART && (T & 3)) {  // a head's eta not 16-byte aligned: 4-byte copies
+            if (tid < BT) cp_async4_or_zero(tb + 4 * TILE + 4 * tid, eta + row0 + tid, true);
+        } else if (tid < 4) {
+            cp_async16(tb + 4 * TILE + 16 * tid, eta + row0 + 4 * tid);
+        }
     };
     auto issue_state = [&](int m) {  // this warp's slices of the block-start state of block m
         const __nv_bfloat16* s1 = W1h + (bh * nblk + m) * NWT;
@@ -915,8 +942,8 @@ mlp_backward_mma_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16
             *reinterpret_cast<uint32_t*>(smem + OFF_DE2B + t64(gl, col)) = pack_bf16(s.x, s.y);
             *reinterpret_cast<uint32_t*>(smem + OFF_DE2B + t64(gl + 8, col)) = pack_bf16(s.z, s.w);
             __nv_bfloat162 o0 = __floats2bfloat162_rn(-s.x, -s.y), o1 = __floats2bfloat162_rn(-s.z, -s.w);
-            *reinterpret_cast<__nv_bfloat162*>(dV + (orow + gl) * D + col) = o0;
-            *reinterpret_cast<__nv_bfloat162*>(dV + (orow + gl + 8) * D + col) = o1;
+            if (!PART || BT * n + gl < T) *reinterpret_cast<__nv_bfloat162*>(dV + (orow + gl) * D + col) = o0;
+            if (!PART || BT * n + gl + 8 < T) *reinterpret_cast<__nv_bfloat162*>(dV + (orow + gl + 8) * D + col) = o1;
         }
         __syncthreads();
 
@@ -1063,16 +1090,20 @@ mlp_backward_mma_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16
                 const float4 v = *reinterpret_cast<const float4*>(part + ((ww * 8 + nt) * 32 + l) * 4);
                 s.x += v.x, s.y += v.y, s.z += v.z, s.w += v.w;
             }
-            *reinterpret_cast<__nv_bfloat162*>(dK + (orow + gl) * D + col) = __floats2bfloat162_rn(s.x, s.y);
-            *reinterpret_cast<__nv_bfloat162*>(dK + (orow + gl + 8) * D + col) = __floats2bfloat162_rn(s.z, s.w);
             const float4 q = *reinterpret_cast<const float4*>(dqf + (nt * 32 + l) * 4);
-            *reinterpret_cast<__nv_bfloat162*>(dQ + (orow + gl) * D + col) = __floats2bfloat162_rn(q.x, q.y);
-            *reinterpret_cast<__nv_bfloat162*>(dQ + (orow + gl + 8) * D + col) = __floats2bfloat162_rn(q.z, q.w);
+            if (!PART || BT * n + gl < T) {  // rows past T are not stored
+                *reinterpret_cast<__nv_bfloat162*>(dK + (orow + gl) * D + col) = __floats2bfloat162_rn(s.x, s.y);
+                *reinterpret_cast<__nv_bfloat162*>(dQ + (orow + gl) * D + col) = __floats2bfloat162_rn(q.x, q.y);
+            }
+            if (!PART || BT * n + gl + 8 < T) {
+                *reinterpret_cast<__nv_bfloat162*>(dK + (orow + gl + 8) * D + col) = __floats2bfloat162_rn(s.z, s.w);
+                *reinterpret_cast<__nv_bfloat162*>(dQ + (orow + gl + 8) * D + col) = __floats2bfloat162_rn(q.z, q.w);
+            }
             if (tid < BT) {
                 float d = detac[tid];
 #pragma unroll
                 for (int ww = 0; ww < NW; ++ww) d += detap[ww * 16 + tid];
-                deta[orow + tid] = d;
+                if (!PART || BT * n + tid < T) deta[orow + tid] = d;
             }
         }
     }
@@ -1082,13 +1113,13 @@ mlp_backward_mma_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16
 }  // namespace
 
 bool mlp_backward_mma_supported(const MlpBwdArgs& a) {
-    return a.bf16 && a.d == D && a.hidden == HID && a.chunk == BT && a.T % BT == 0;
+    return a.bf16 && a.d == D && a.hidden == HID && a.chunk == BT;  // any T
 }
 
-template <int NW>
+template <int NW, bool PART>
 cudaError_t launch_nw(const MlpBwdArgs& a, cudaStream_t s) {
     using C = BwdCfg<NW>;
-    auto kern = mlp_backward_mma_kernel<NW>;
+    auto kern = mlp_backward_mma_kernel<NW, PART>;
     cudaError_t e = allow_dynamic_smem(reinterpret_cast<const void*>(kern), C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     kern<<<unsigned(a.B) * unsigned(a.H), C::NTH, C::SMEM_BYTES, s>>>(
@@ -1106,7 +1137,8 @@ cudaError_t launch_mlp_backward_mma(const MlpBwdArgs& a, cudaStream_t s) {
     // measured slower on the TTT-MLP workload shape: 2.12 against 1.65 ms -- the per-warp work on the token
     // side does not shrink, each reduction takes one more barrier, and 128 registers per thread)
     const char* v = getenv("TTT_MLP_BACKWARD_WARPS");
-    return (v && !strcmp(v, "16")) ? launch_nw<16>(a, s) : launch_nw<8>(a, s);
+    if (a.T % BT) return (v && !strcmp(v, "16")) ? launch_nw<16, true>(a, s) : launch_nw<8, true>(a, s);
+    return (v && !strcmp(v, "16")) ? launch_nw<16, false>(a, s) : launch_nw<8, false>(a, s);
 }
 
 }  // namespace ttt

@@ -144,12 +144,14 @@ def test_mlp_backward_workload_shape_all_heads():
           **{n: (got, want) for n, got, want in zip(NAMES, grads, ref)})
 
 
-# bf16, d = 64, hidden = 256, chunk 16 with 16 | T runs the warp-MMA kernel; these cases span
-# several blocks and heads of it
+# bf16, d = 64, hidden = 256, chunk 16 runs the warp-MMA kernel; these cases span several blocks
+# and heads of it, and T not a multiple of 16 (a partial last block, the first processed; with 4 not
+# dividing T eta comes by 4-byte copies)
 @pytest.mark.parametrize("with_state", [True, False])
-def test_mlp_backward_mma_shape_matches_oracle(with_state):
-    x = WL.mlp_inputs(2, 3, 96, 64, 256, seed=4400, dtype="bf16", w_std=0.1)
-    dZ, dW1, dW2 = _grads(2, 3, 96, 64, 256, 4401, "bf16", with_state)
+@pytest.mark.parametrize("T_", [96, 45, 204, 1001])
+def test_mlp_backward_mma_shape_matches_oracle(with_state, T_):
+    x = WL.mlp_inputs(2, 3, T_, 64, 256, seed=4400 + T_, dtype="bf16", w_std=0.1)
+    dZ, dW1, dW2 = _grads(2, 3, T_, 64, 256, 4401 + T_, "bf16", with_state)
     grads = _run(x, dZ, dW1, dW2, 16)[5]
     ref = _oracle(x, dZ, dW1, dW2, 16)
     for name, got, want in zip(NAMES, grads, ref):
