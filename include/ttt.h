@@ -189,9 +189,10 @@ ttt_status ttt_linear_prefill_noalloc(const void* Q, const void* K, const void* 
  *   M0       [B][H][d][d]  fp32   momentum at the start, or NULL for zero
  *   M_out    [B][H][d][d]  fp32   momentum after the last token (written; may be M0)
  *   W_out    may be W0; beta in [0, 1] (else TTT_ERR_INVALID_ARG)
- *   Other arguments as ttt_linear_prefill.  bf16 with d = 64, chunk = 16 and 16 | T runs on
- *   warp-level tensor-core MMAs (bf16 operands, fp32 state and momentum); every other shape on
- *   the SIMT fp32 kernel.  TTT_LINEAR_MOMENTUM_KERNEL = "simt" forces the SIMT kernel.
+ *   Other arguments as ttt_linear_prefill.  bf16 with d = 64 and chunk = 16 runs on warp-level
+ *   tensor-core MMAs for any T (bf16 operands, fp32 state and momentum; a partial last chunk
+ *   weighs its tokens past T by zero and decays the momentum by beta per token it holds); every
+ *   other shape on the SIMT fp32 kernel.  TTT_LINEAR_MOMENTUM_KERNEL = "simt" forces the SIMT kernel.
  *
  * Source: E^2-TTT article (zhichai.net), section "Technical Details and Practical
  * Implications" (momentum gradient descent, squared loss, gradients at the

@@ -44,10 +44,22 @@ __device__ __forceinline__ uint32_t sw(int row, int col) {
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
+// the same with zeros instead of the source when `valid` is false (nothing is read from src then)
+__device__ __forceinline__ void cp_async16_or_zero(uint32_t dst, const void* src, bool valid) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(valid ? 16 : 0)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async4_or_zero(uint32_t dst, const void* src, bool valid) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(valid ? 4 : 0)
+                 : "memory");
+}
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait0() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 
-template <int CG>
+// PART: T is not a multiple of 16 (a partial last chunk).  Its tokens past T are copied in as zeros
+// (eta too), which leaves W and Z exact, and its momentum takes the chunk's own length n:
+// M <- beta^n M + K^T diag(beta^(n-1-j)) E.  The instantiation for 16 | T compiles none of that.
+template <int CG, bool PART>
 __global__ void __launch_bounds__(32 * CG)
 linear_momentum_mma_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restrict__ K,
                            const __nv_bfloat16* __restrict__ V, const float* __restrict__ eta, const float* W0,
@@ -59,20 +71,38 @@ linear_momentum_mma_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloa
     const int lj = lane >> 3, lr = lane & 7;
     const size_t bh = blockIdx.x;
     const int cw0 = (blockIdx.y * CG + warp) * 16;  // first output column of this warp's group
-    const int nblk = T / 16, nstg = (nblk + SPS - 1) / SPS;
+    const int nblk = PART ? (T + 15) / 16 : T / 16, nstg = (nblk + SPS - 1) / SPS;
     float* tws = reinterpret_cast<float*>(smem + OFF_TW);
 
     auto issue = [&](int si) {
         const uint32_t b = sb + (si & 1) * STAGE;
         const int n = min(SPS, nblk - si * SPS);
         const size_t row0 = bh * size_t(T) + size_t(si) * SPS * 16;
-        for (int c = tid; c < n * 384; c += 32 * CG) {
-            const int i = c / 384, r = c % 384, tile = r >> 7, row = (r >> 3) & 15, ch = r & 7;
-            const __nv_bfloat16* src = tile == 0 ? Q : tile == 1 ? K : V;
-            cp_async16(b + i * CHUNK + tile * TILE + sw(row, 8 * ch), src + (row0 + 16 * i + row) * D + 8 * ch);
+        const int t0 = si * SPS * 16;  // first token of the stage
+        if (PART && t0 + 16 * n > T) {  // the stage holds the partial last chunk: zeros past T
+            for (int c = tid; c < n * 384; c += 32 * CG) {
+                const int i = c / 384, r = c % 384, tile = r >> 7, row = (r >> 3) & 15, ch = r & 7;
+                const __nv_bfloat16* src = tile == 0 ? Q : tile == 1 ? K : V;
+                const bool in = t0 + 16 * i + row < T;
+                cp_async16_or_zero(b + i * CHUNK + tile * TILE + sw(row, 8 * ch),
+                                   src + (row0 + (in ? 16 * i + row : 0)) * D + 8 * ch, in);
+            }
+        } else {
+            for (int c = tid; c < n * 384; c += 32 * CG) {
+                const int i = c / 384, r = c % 384, tile = r >> 7, row = (r >> 3) & 15, ch = r & 7;
+                const __nv_bfloat16* src = tile == 0 ? Q : tile == 1 ? K : V;
+                cp_async16(b + i * CHUNK + tile * TILE + sw(row, 8 * ch), src + (row0 + 16 * i + row) * D + 8 * ch);
+            }
         }
-        for (int c = tid; c < n * 4; c += 32 * CG)
-            cp_async16(b + (c >> 2) * CHUNK + 3 * TILE + 16 * (c & 3), eta + row0 + 4 * c);
+        if (PART && ((T & 3) || t0 + 16 * n > T)) {  // eta by 4-byte copies: unaligned, or zeros past T
+            for (int c = tid; c < n * 16; c += 32 * CG) {
+                const bool in = t0 + c < T;
+                cp_async4_or_zero(b + (c >> 4) * CHUNK + 3 * TILE + 4 * (c & 15), eta + row0 + (in ? c : 0), in);
+            }
+        } else {
+            for (int c = tid; c < n * 4; c += 32 * CG)
+                cp_async16(b + (c >> 2) * CHUNK + 3 * TILE + 16 * (c & 3), eta + row0 + 4 * c);
+        }
     };
 
     // ldmatrix coordinates: B with n = token, k = d (K in W^T K^T and Q K^T); A with m = token, k = d
@@ -257,18 +287,21 @@ linear_momentum_mma_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloa
                 mma_bf16_16816(zp[0], ac, ea[0], ea[2]);
                 mma_bf16_16816(zp[1], ac, ea[1], ea[3]);
                 __nv_bfloat16* zr = zb + size_t(16 * (si * SPS + i) + g) * D;  // rows g (+8), columns cw0 + 2t (+8)
-                *reinterpret_cast<uint32_t*>(zr) = pack_bf16(zp[0][0], zp[0][1]);
-                *reinterpret_cast<uint32_t*>(zr + 8 * D) = pack_bf16(zp[0][2], zp[0][3]);
-                *reinterpret_cast<uint32_t*>(zr + 8) = pack_bf16(zp[1][0], zp[1][1]);
-                *reinterpret_cast<uint32_t*>(zr + 8 * D + 8) = pack_bf16(zp[1][2], zp[1][3]);
+                const bool lo = !PART || 16 * (si * SPS + i) + g < T, hi = !PART || 16 * (si * SPS + i) + g + 8 < T;
+                if (lo) *reinterpret_cast<uint32_t*>(zr) = pack_bf16(zp[0][0], zp[0][1]);
+                if (hi) *reinterpret_cast<uint32_t*>(zr + 8 * D) = pack_bf16(zp[0][2], zp[0][3]);
+                if (lo) *reinterpret_cast<uint32_t*>(zr + 8) = pack_bf16(zp[1][0], zp[1][1]);
+                if (hi) *reinterpret_cast<uint32_t*>(zr + 8 * D + 8) = pack_bf16(zp[1][2], zp[1][3]);
             }
-            // W^T <- W^T - c_15 M^T - E^T diag(Bs) K;  M^T <- beta^16 M^T + E^T diag(beta^(15-j)) K
+            // W^T <- W^T - c_15 M^T - E^T diag(Bs) K;  M^T <- beta^n M^T + E^T diag(beta^(n-1-j)) K, n the
+            // chunk's tokens (16 but for a partial last chunk, whose E is zero past n)
             {
+                const int ntok = PART ? min(16, T - 16 * (si * SPS + i)) : 16;
                 float bsj[4], pj[4];
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     bsj[q] = tw[16 + jc[q]];
-                    pj[q] = tw[33 + 15 - jc[q]];
+                    pj[q] = PART ? (jc[q] < ntok ? tw[33 + ntok - 1 - jc[q]] : 0.f) : tw[33 + 15 - jc[q]];
                 }
                 const uint32_t gw[4] = {pack_bf16(-bsj[0] * e[0][0], -bsj[1] * e[0][1]),
                                         pack_bf16(-bsj[0] * e[0][2], -bsj[1] * e[0][3]),
@@ -278,7 +311,7 @@ linear_momentum_mma_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloa
                                         pack_bf16(pj[0] * e[0][2], pj[1] * e[0][3]),
                                         pack_bf16(pj[2] * e[1][0], pj[3] * e[1][1]),
                                         pack_bf16(pj[2] * e[1][2], pj[3] * e[1][3])};
-                const float c15 = tw[15], b16 = tw[49];
+                const float c15 = tw[15], b16 = PART ? tw[33 + ntok] : tw[49];  // beta^n
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
@@ -314,9 +347,9 @@ linear_momentum_mma_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloa
     }
 }
 
-template <int CG>
-cudaError_t launch_cg(const LinearArgs& a, cudaStream_t s) {
-    auto kern = linear_momentum_mma_kernel<CG>;
+template <int CG, bool PART>
+cudaError_t launch_part(const LinearArgs& a, cudaStream_t s) {
+    auto kern = linear_momentum_mma_kernel<CG, PART>;
     cudaError_t e = allow_dynamic_smem(reinterpret_cast<const void*>(kern), SMEM_BYTES);
     if (e != cudaSuccess) return e;
     kern<<<dim3(unsigned(a.B) * unsigned(a.H), 4 / CG), 32 * CG, SMEM_BYTES, s>>>(
@@ -326,10 +359,15 @@ cudaError_t launch_cg(const LinearArgs& a, cudaStream_t s) {
     return cudaGetLastError();
 }
 
+template <int CG>
+cudaError_t launch_cg(const LinearArgs& a, cudaStream_t s) {
+    return a.T % 16 ? launch_part<CG, true>(a, s) : launch_part<CG, false>(a, s);
+}
+
 }  // namespace
 
 bool linear_momentum_mma_supported(const LinearArgs& a) {
-    return a.momentum && a.bf16 && a.d == D && a.chunk == 16 && a.T % 16 == 0;
+    return a.momentum && a.bf16 && a.d == D && a.chunk == 16;  // any T
 }
 
 cudaError_t launch_linear_momentum_mma(const LinearArgs& a, cudaStream_t s) {

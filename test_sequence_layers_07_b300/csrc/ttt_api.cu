@@ -295,7 +295,7 @@ ttt_status ttt_linear_momentum_prefill(const void* Q, const void* K, const void*
     a.M0 = M0;
     a.M_out = M_out;
     a.beta = beta;
-    // bf16, d = 64, chunk 16, 16 | T: the warp-MMA kernel; the SIMT kernel otherwise
+    // bf16, d = 64, chunk 16, any T: the warp-MMA kernel; the SIMT kernel otherwise
     // (TTT_LINEAR_MOMENTUM_KERNEL = "simt" forces the SIMT kernel)
     const char* kv = getenv("TTT_LINEAR_MOMENTUM_KERNEL");
     cudaError_t e = cudaErrorNotSupported;

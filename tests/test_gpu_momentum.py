@@ -102,11 +102,13 @@ def test_momentum_headline_shape_all_heads():
     check("linear_momentum B=8 H=12 d=64 T=2048 b=16 beta=0.9", TOL["bf16"], Z=(Z, Zr), W=(W, Wr), M=(M, Mr))
 
 
-# bf16, d = 64, chunk 16 with 16 | T runs the warp-MMA kernel
+# bf16, d = 64, chunk 16 runs the warp-MMA kernel; T = 157 / 7 / 1001 end in a partial chunk (its
+# momentum decays by beta per token it holds, not per 16), 1001 with several stages
 @pytest.mark.parametrize("beta", [0.0, 0.5, 0.9, 1.0])
 @pytest.mark.parametrize("B,H", [(2, 3), (1, 1)])  # 6 heads: one CTA per head; 1 head: one per column group
-def test_momentum_mma_shape(beta, B, H):
-    x = WL.linear_inputs(B, H, 160, 64, seed=3600 + B * H, dtype="bf16")
+@pytest.mark.parametrize("T_", [160, 157, 7, 1001])
+def test_momentum_mma_shape(beta, B, H, T_):
+    x = WL.linear_inputs(B, H, T_, 64, seed=3600 + B * H + T_, dtype="bf16")
     M0 = _m0(x, 3601, zero=(beta == 0.5))
     g = cuda(x)
     Z, W, M = T.linear_momentum_prefill(g["Q"], g["K"], g["V"], g["eta"], g["W0"],
