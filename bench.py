@@ -650,9 +650,35 @@ def bench_e2e(T_mod, w, steps, warmup, world):
         raise RuntimeError("pipelined end-to-end steps disagree with a plain call")
     h2d = sum(v.numel() * v.element_size() for v in host.values())
     d2h = Zh.numel() * Zh.element_size() + Wh.numel() * Wh.element_size()
+    # what the host link gives for the same bytes in the same run: the step's uploads alone, and its
+    # uploads and downloads at once (the lower bound of a pipelined step)
+    def copies(down):
+        with torch.cuda.stream(s_up):
+            for k in dev[0]:
+                dev[0][k].copy_(host[k], non_blocking=True)
+        if down:
+            with torch.cuda.stream(s_dn):
+                Zh.copy_(outs[0][0], non_blocking=True)
+                Wh.copy_(outs[0][1], non_blocking=True)
+    link = {}
+    for name, down in (("h2d_ms", False), ("h2d_with_d2h_ms", True)):
+        copies(down)
+        torch.cuda.synchronize()
+        a, z = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(s_up)
+        s_dn.wait_event(a)
+        for _ in range(20):
+            copies(down)
+        for st in (s_up, s_dn):
+            cur.wait_stream(st)
+        z.record(cur)
+        torch.cuda.synchronize()
+        link[name] = a.elapsed_time(z) / 20
+    link["h2d_gbs"] = h2d / (link["h2d_ms"] * 1e6)
     return {"value": w.B * w.T / (ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": ms,
-            "pipelining": "upload, prefill and download on three streams, two device buffer sets"}
+            "pipelining": "upload, prefill and download on three streams, two device buffer sets",
+            "host_link": link}
 
 
 def cpu_model() -> str:
