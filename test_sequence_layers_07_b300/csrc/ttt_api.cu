@@ -627,6 +627,6 @@ const char* ttt_status_string(ttt_status s) {
 
 const char* ttt_last_error(void) { return g_last_error; }
 
-int ttt_version(void) { return 10400; }
+int ttt_version(void) { return 10500; }  // 1.5: the tensor-core kernels take any T
 
 }  // extern "C"
