@@ -73,7 +73,7 @@ __device__ __forceinline__ void pack_state(const float (&w)[2 * KS][4], uint32_t
     }
 }
 
-template <int D, int CG, int NST, int SPS>
+template <int D, int CG, int NST, int SPS, bool HIST = false>
 struct FusedCfg {
     static constexpr int KS = D / 16;        // k-steps over the input dimension
     static constexpr int NT = D / 8;         // 8-wide n-tiles of the state over the input dimension
@@ -81,9 +81,12 @@ struct FusedCfg {
     // a stage holds SPS sub-blocks: Q sub-tiles, then K, then V, then eta
     static constexpr int QOFF = 0, KOFF = SPS * TILE, VOFF = 2 * SPS * TILE, EOFF = 3 * SPS * TILE;
     static constexpr int STAGE = (EOFF + SPS * 64 + 1023) / 1024 * 1024;
-    static constexpr int SC_OFF = NST * STAGE;  // masked scores [NST][SPS][32 lanes] x 16 B
-    static constexpr int HS_OFF = SC_OFF + NST * SPS * 512;  // per warp: a [D][16] bf16 state slice
-    static constexpr int BYTES = HS_OFF + CG * D * 32;
+    // masked scores [NST][SPS]: 32 lanes x 16 B; with the recorded states, the three registers of the
+    // fragment that can be nonzero, word-major ([3][32 lanes] x 4 B), to make room for a second slice
+    static constexpr int SCB = HIST ? 384 : 512;
+    static constexpr int SC_OFF = NST * STAGE;
+    static constexpr int HS_OFF = SC_OFF + NST * SPS * SCB;  // per warp: [D][16] bf16 state slices (two with HIST)
+    static constexpr int BYTES = HS_OFF + CG * D * (HIST ? 64 : 32);
     static constexpr int THREADS = 32 * (CG + 1);
 };
 
@@ -95,12 +98,12 @@ struct FusedCfg {
 // read as zeros), eta by cp.async where a bulk copy cannot take it, and the rows of Z past T are not
 // stored; the instantiation for the common case compiles none of that.
 template <int D, int CG, int NST, int SPS, bool SINGLE, bool HIST, bool PART>
-__global__ void __launch_bounds__(FusedCfg<D, CG, NST, SPS>::THREADS, 1)
+__global__ void __launch_bounds__(FusedCfg<D, CG, NST, SPS, HIST>::THREADS, 1)
 linear_prefill_fused_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                             const __grid_constant__ CUtensorMap tmV, const float* __restrict__ eta,
                             const float* W0, __nv_bfloat16* __restrict__ Z, float* W_out, int T, int chunk,
                             int* status, const __grid_constant__ CUtensorMap tmH, uint64_t wait_ns) {
-    using C = FusedCfg<D, CG, NST, SPS>;
+    using C = FusedCfg<D, CG, NST, SPS, HIST>;
     constexpr int KS = C::KS, NT = C::NT;
 
     extern __shared__ uint8_t smem_dyn[];
@@ -279,7 +282,7 @@ linear_prefill_fused_kernel(const __grid_constant__ CUtensorMap tmQ, const __gri
             const int s = si % NST, n = subs_in(si);
             const uint32_t par = (si / NST) & 1;
             const uint32_t st = sbase + s * C::STAGE;
-            uint8_t* sc = smem + C::SC_OFF + s * SPS * 512;
+            uint8_t* sc = smem + C::SC_OFF + s * SPS * C::SCB;
             if (!(ok = wait_all(full_bar[s], par))) break;
             // this warp's share of the stage's masked scores S = tril(Q K^T), as A fragments
             // (rows query i, cols key j); the second fragment buffers serve as scratch
@@ -303,7 +306,14 @@ linear_prefill_fused_kernel(const __grid_constant__ CUtensorMap tmQ, const __gri
                 f.y = pack_bf16(sa[0][2], sa[0][3]);
                 f.z = 0u;
                 f.w = pack_bf16(m0 ? sa[1][2] : 0.f, m1 ? sa[1][3] : 0.f);
-                *reinterpret_cast<uint4*>(sc + i * 512 + lane * 16) = f;
+                if constexpr (HIST) {
+                    uint32_t* r = reinterpret_cast<uint32_t*>(sc + i * C::SCB) + lane;
+                    r[0] = f.x;
+                    r[32] = f.y;
+                    r[64] = f.w;
+                } else {
+                    *reinterpret_cast<uint4*>(sc + i * 512 + lane * 16) = f;
+                }
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&sc_bar[s]));
@@ -316,28 +326,42 @@ linear_prefill_fused_kernel(const __grid_constant__ CUtensorMap tmQ, const __gri
                 const int b = i & 1, sb = si * SPS + i;
                 if (i > 0) load_kt(st, i);  // used by the update, well after K W and Q W
                 if (i + 1 < n) load_kq(b ^ 1, st, i + 1);
-                const uint4 sf4 = *reinterpret_cast<const uint4*>(sc + i * 512 + lane * 16);
+                uint4 sf4;
+                if constexpr (HIST) {
+                    const uint32_t* r = reinterpret_cast<const uint32_t*>(sc + i * C::SCB) + lane;
+                    sf4 = make_uint4(r[0], r[32], 0u, r[64]);
+                } else {
+                    sf4 = *reinterpret_cast<const uint4*>(sc + i * 512 + lane * 16);
+                }
                 const bool bstart = SINGLE || sb % nsub == 0;
                 if (bstart) {
                     pack_state<KS>(w, wa0);
                     if constexpr (HIST) {
-                        // the bf16 state at the start of block sb / nsub: the A fragments of W^T
-                        // stored transposed (stmatrix) into this warp's [D][16] slice, which one
-                        // TMA store writes to W_hist[block][d_in][cw0 ..]; the warp moves on at once
-                        // (a plain store would hold its source registers until the memory system
-                        // takes them, stalling the chain)
-                        const uint32_t hs = sbase + C::HS_OFF + cg * D * 32;
-                        if (lane == 0) bulk_wait_read_all();  // the previous block's store has read the slice
-                        __syncwarp();
+                        // the bf16 state at the start of block sb (blocks of 16): the A fragments of
+                        // W^T stored transposed (stmatrix) into one of this warp's two [D][16] slices;
+                        // a pair of blocks shares one proxy fence, after which two TMA stores write
+                        // the slices to W_hist[block][d_in][cw0 ..] and the warp moves on (a plain
+                        // store would hold its source registers until the memory system takes them,
+                        // stalling the chain)
+                        const uint32_t hs = sbase + C::HS_OFF + cg * D * 64;
+                        if ((sb & 1) == 0) {
+                            if (lane == 0) bulk_wait_read_all();  // the previous pair's stores have read both slices
+                            __syncwarp();
+                        }
+                        const uint32_t slice = hs + (sb & 1) * D * 32;
 #pragma unroll
                         for (int ks = 0; ks < KS; ++ks)
-                            stsm_x4_trans(hs + (16 * ks + 8 * (lj >> 1) + lr) * 32 + (lj & 1) * 16, wa0[ks][0],
+                            stsm_x4_trans(slice + (16 * ks + 8 * (lj >> 1) + lr) * 32 + (lj & 1) * 16, wa0[ks][0],
                                           wa0[ks][1], wa0[ks][2], wa0[ks][3]);
-                        fence_proxy_async_smem();
-                        __syncwarp();
-                        if (lane == 0) {
-                            tma_store_2d(&tmH, cw0, int((bh * size_t(nsb) + sb) * D), hs);
-                            bulk_commit();
+                        if ((sb & 1) == 1 || sb == nsb - 1) {  // the pair is complete (or the head ends)
+                            fence_proxy_async_smem();
+                            __syncwarp();
+                            if (lane == 0) {
+                                const int first = sb & ~1;
+                                tma_store_2d(&tmH, cw0, int((bh * size_t(nsb) + first) * D), hs);
+                                if (sb != first) tma_store_2d(&tmH, cw0, int((bh * size_t(nsb) + sb) * D), hs + D * 32);
+                                bulk_commit();
+                            }
                         }
                     }
                 }
@@ -436,7 +460,7 @@ linear_prefill_fused_kernel(const __grid_constant__ CUtensorMap tmQ, const __gri
 
 template <int D, int CG, int NST, int SPS, bool SINGLE, bool HIST, bool PART>
 cudaError_t launch_part(const LinearArgs& a, cudaStream_t s, int* status) {
-    using C = FusedCfg<D, CG, NST, SPS>;
+    using C = FusedCfg<D, CG, NST, SPS, HIST>;
     const uint64_t heads = uint64_t(a.B) * a.H;
     CUtensorMap mq, mk, mv, mh;
     cudaError_t e;
@@ -470,7 +494,7 @@ cudaError_t launch_cfg(const LinearArgs& a, cudaStream_t s, int* status) {
 }
 
 // stages of 256 tokens, double-buffered: 2 x 97 KB of Q/K/V/eta + 16 KB of scores + 8 KB of state
-// staging per CTA
+// staging per CTA (with the recorded states: 12 KB of scores + 16 KB of staging)
 constexpr int kSps = 16, kNst = 2;
 
 template <int CG>
